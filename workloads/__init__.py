@@ -1,0 +1,488 @@
+"""Seeded synthetic workloads for one flattened mixed-batch step.
+
+This module only builds inputs: the request structure (cached and scheduled
+token counts), the persistent token table, a page table whose physical page ids
+are a seeded random permutation, and random bf16 activations standing in for the
+Q/K/V projections and the hidden states.  None of the step's own arithmetic is
+here: no prefix sums, positions, slots, attention or gathers.  Both the CPU
+oracle (``oracle/``) and the CUDA library consume what this module returns, and
+neither is imported from here.
+
+Recipe (all synthetic; the pages name no dataset):
+
+* host structure: ``numpy.random.Generator(PCG64(seed))`` with
+  ``seed = 1000 * config + step``;
+* token ids uniform in [0, 32000);
+* physical page ids: a seeded permutation of every page but the reserved null
+  page (id 0 unless stated); unused page-table entries hold -1;
+* Q/K/V/hidden: bf16 draws of N(0, 1) from a seeded ``torch.Generator``;
+* cached history K/V: one contiguous bf16 tensor per request, placed page by
+  page into the pool (the pool starts filled with N(0, 1) noise so stale or
+  misplaced data is visible).
+"""
+from __future__ import annotations
+
+import dataclasses
+from dataclasses import dataclass, field
+from typing import Iterator, List, Optional
+
+import numpy as np
+
+VOCAB = 32000
+
+# Capture sizes quoted for vLLM's piecewise CUDA graphs (vLLM book, ch. 8,
+# "8.4.3 实际效果" and "8.5 pad_for_cudagraph").
+GRAPH_CAPTURE_SIZES = (1, 2, 4, 8, 16, 24, 32, 48, 64, 96, 128, 192, 256)
+
+
+@dataclass(frozen=True)
+class Dims:
+    """Static sizes of the persistent batch and the paged KV pool (one layer)."""
+
+    block_size: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    max_num_reqs: int
+    max_model_len: int
+    max_blocks_per_req: int
+    num_blocks: int
+    null_block: int = 0
+
+    @property
+    def num_slots(self) -> int:
+        return self.num_blocks * self.block_size
+
+
+@dataclass
+class BatchSpec:
+    """Host-side description of one scheduled step (what the scheduler hands the runner)."""
+
+    name: str
+    dims: Dims
+    num_computed: np.ndarray  # int32 [R]   tokens already in the KV cache
+    num_scheduled: np.ndarray  # int32 [R]  tokens scheduled this step
+    num_reqs_padded: int
+    num_tokens_padded: int
+    token_table: np.ndarray  # int32 [max_num_reqs, max_model_len]
+    block_table: np.ndarray  # int32 [max_num_reqs, max_blocks_per_req], -1 = unused
+    hidden_size: int
+    seed: int
+    num_prompt: Optional[np.ndarray] = None  # int32 [R] prompt lengths, where known
+
+    @property
+    def num_reqs(self) -> int:
+        return int(self.num_scheduled.shape[0])
+
+    @property
+    def num_tokens(self) -> int:
+        # the scheduler's own total (total_num_scheduled_tokens)
+        return int(self.num_scheduled.sum(dtype=np.int64))
+
+
+# --------------------------------------------------------------------------- #
+# page allocation (a seeded free list; the KV-cache manager's job, not the step's)
+# --------------------------------------------------------------------------- #
+class PagePool:
+    """Free list of physical pages in seeded random order; the null page is never handed out."""
+
+    def __init__(self, num_blocks: int, null_block: int, rng: np.random.Generator):
+        ids = np.array([b for b in range(num_blocks) if b != null_block], dtype=np.int64)
+        self.free: List[int] = [int(x) for x in rng.permutation(ids)]
+        self.in_use = 0
+        self.peak = 0
+
+    def take(self, n: int) -> List[int]:
+        if n > len(self.free):
+            raise RuntimeError(f"page pool exhausted: need {n}, have {len(self.free)}")
+        out, self.free = self.free[:n], self.free[n:]
+        self.in_use += n
+        self.peak = max(self.peak, self.in_use)
+        return out
+
+    def give_back(self, pages: List[int]) -> None:
+        self.free.extend(pages)
+        self.in_use -= len(pages)
+
+
+def pages_for(num_tokens: int, block_size: int) -> int:
+    """Pages a request must own to hold ``num_tokens`` tokens (allocator rule)."""
+    return -(-int(num_tokens) // block_size)
+
+
+def _build_spec(name, dims, computed, scheduled, rng, hidden_size, seed,
+                num_reqs_padded=None, num_tokens_padded=None, num_prompt=None) -> BatchSpec:
+    computed = np.asarray(computed, dtype=np.int32)
+    scheduled = np.asarray(scheduled, dtype=np.int32)
+    R = computed.shape[0]
+    assert R <= dims.max_num_reqs
+    token_table = np.zeros((dims.max_num_reqs, dims.max_model_len), dtype=np.int32)
+    block_table = np.full((dims.max_num_reqs, dims.max_blocks_per_req), -1, dtype=np.int32)
+    pool = PagePool(dims.num_blocks, dims.null_block, rng)
+    for i in range(R):
+        total = int(computed[i]) + int(scheduled[i])
+        token_table[i, :total] = rng.integers(0, VOCAB, size=total, dtype=np.int32)
+        n = pages_for(total, dims.block_size)
+        block_table[i, :n] = pool.take(n)
+    n_tok = int(scheduled.sum(dtype=np.int64))
+    return BatchSpec(name=name, dims=dims, num_computed=computed, num_scheduled=scheduled,
+                     num_reqs_padded=R if num_reqs_padded is None else num_reqs_padded,
+                     num_tokens_padded=n_tok if num_tokens_padded is None else num_tokens_padded,
+                     token_table=token_table, block_table=block_table, hidden_size=hidden_size,
+                     seed=seed, num_prompt=None if num_prompt is None else np.asarray(num_prompt, np.int32))
+
+
+def _pool_blocks_for(computed, scheduled, block_size, slack=1.25) -> int:
+    need = sum(pages_for(int(c) + int(q), block_size) for c, q in zip(computed, scheduled))
+    return int(np.ceil(need * slack)) + 1
+
+
+def _round_up(x: int, m: int) -> int:
+    return -(-x // m) * m
+
+
+# --------------------------------------------------------------------------- #
+# the five workloads
+# --------------------------------------------------------------------------- #
+def config1(step: int = 0, num_tokens_padded: Optional[int] = None) -> BatchSpec:
+    """Pages' worked example: A prefill 7, B decode with 5 cached, C chunk 10 cached + 12 new.
+
+    block_size 16, 64 physical pages, 4 q heads / 2 kv heads, head_dim 64.
+    """
+    seed = 1000 * 1 + step
+    rng = np.random.default_rng(seed)
+    dims = Dims(block_size=16, num_q_heads=4, num_kv_heads=2, head_dim=64, max_num_reqs=4,
+                max_model_len=64, max_blocks_per_req=4, num_blocks=64, null_block=0)
+    return _build_spec("worked example A/B/C", dims, [0, 5, 10], [7, 1, 12], rng, 256, seed,
+                       num_tokens_padded=num_tokens_padded)
+
+
+def config2(step: int = 0) -> BatchSpec:
+    """Padding example: query_lens [2000, 512, 1 x 6]; decodes have 1000..4000 cached tokens.
+
+    32 q heads / 8 kv heads, head_dim 128, block_size 16, hidden 4096.
+    """
+    seed = 1000 * 2 + step
+    rng = np.random.default_rng(seed)
+    scheduled = [2000, 512] + [1] * 6
+    computed = [0, 0] + [int(x) for x in rng.integers(1000, 4000, size=6, endpoint=True)]
+    M = _round_up(max(c + q for c, q in zip(computed, scheduled)), 16) + 16
+    dims = Dims(block_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128, max_num_reqs=8,
+                max_model_len=M, max_blocks_per_req=M // 16,
+                num_blocks=_pool_blocks_for(computed, scheduled, 16))
+    return _build_spec("padding example (2 prefills + 6 decodes)", dims, computed, scheduled, rng,
+                       4096, seed)
+
+
+def config3(step: int = 0, num_real: int = 256) -> BatchSpec:
+    """Pure decode: ``num_real`` requests x 1 token, cached context U[512, 8192], padded to 256.
+
+    ``num_real=256`` is the workload as stated (no padding tokens); ``num_real=250`` exercises the
+    null-page route for 6 padding tokens and 6 padding requests.
+    """
+    seed = 1000 * 3 + step + (0 if num_real == 256 else 500)
+    rng = np.random.default_rng(seed)
+    computed = [int(x) for x in rng.integers(512, 8192, size=num_real, endpoint=True)]
+    scheduled = [1] * num_real
+    M = _round_up(8192 + 1, 16)
+    dims = Dims(block_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128, max_num_reqs=256,
+                max_model_len=M, max_blocks_per_req=M // 16,
+                num_blocks=_pool_blocks_for(computed, scheduled, 16))
+    return _build_spec(f"pure decode ({num_real} real, padded to 256)", dims, computed, scheduled, rng,
+                       4096, seed, num_reqs_padded=256, num_tokens_padded=256)
+
+
+def config5(step: int = 0, pool_gb: float = 0.0) -> BatchSpec:
+    """Long context: 8 decodes at 131072 cached + one 4096-token chunk with 65536 cached.
+
+    64 q heads / 8 kv heads, head_dim 128, block_size 16.  One layer of the KV cache is
+    materialised; ``pool_gb`` > 0 spreads the pages over a larger pool of that many GB (K+V).
+    """
+    seed = 1000 * 5 + step
+    rng = np.random.default_rng(seed)
+    computed = [131072] * 8 + [65536]
+    scheduled = [1] * 8 + [4096]
+    M = 131072 + 16
+    nb = _pool_blocks_for(computed, scheduled, 16)
+    if pool_gb > 0:
+        page_bytes = 2 * 16 * 8 * 128 * 2
+        nb = max(nb, int(pool_gb * 1e9 // page_bytes))
+    dims = Dims(block_size=16, num_q_heads=64, num_kv_heads=8, head_dim=128, max_num_reqs=9,
+                max_model_len=M, max_blocks_per_req=M // 16, num_blocks=nb)
+    return _build_spec("long context (8 x 131072 decodes + 4096 chunk at 65536)", dims, computed,
+                       scheduled, rng, 8192, seed)
+
+
+def random_batch(seed: int, *, max_reqs: int = 6, max_q: int = 40, max_c: int = 90,
+                 block_size: int = 16, num_q_heads: int = 4, num_kv_heads: int = 2,
+                 head_dim: int = 64, pad_tokens: int = 0, pad_reqs: int = 0,
+                 decode_frac: float = 0.4, hidden_size: int = 128) -> BatchSpec:
+    """A small ragged mix for fuzzing: a seeded blend of decodes, fresh prefills and chunks."""
+    rng = np.random.default_rng(seed)
+    R = int(rng.integers(1, max_reqs + 1))
+    computed, scheduled = [], []
+    for _ in range(R):
+        u = rng.random()
+        if u < decode_frac:
+            computed.append(int(rng.integers(1, max_c + 1)))
+            scheduled.append(1)
+        elif u < decode_frac + 0.3:
+            computed.append(0)
+            scheduled.append(int(rng.integers(1, max_q + 1)))
+        else:
+            computed.append(int(rng.integers(1, max_c + 1)))
+            scheduled.append(int(rng.integers(1, max_q + 1)))
+    M = _round_up(max_c + max_q + 1, block_size) + block_size
+    dims = Dims(block_size=block_size, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                head_dim=head_dim, max_num_reqs=R + pad_reqs + 1, max_model_len=M,
+                max_blocks_per_req=M // block_size,
+                num_blocks=_pool_blocks_for(computed, scheduled, block_size) + 3)
+    n = sum(scheduled)
+    return _build_spec(f"random mix seed={seed}", dims, computed, scheduled, rng, hidden_size, seed,
+                       num_reqs_padded=R + pad_reqs, num_tokens_padded=n + pad_tokens)
+
+
+def batch_from_lists(num_computed, num_scheduled, *, block_size=16, num_q_heads=4, num_kv_heads=2,
+                     head_dim=64, seed=0, num_reqs_padded=None, num_tokens_padded=None,
+                     hidden_size=128, extra_blocks=3, max_model_len=None) -> BatchSpec:
+    """A batch with the given per-request counts (and seeded pages/tokens)."""
+    rng = np.random.default_rng(seed)
+    mx = max([c + q for c, q in zip(num_computed, num_scheduled)] + [1])
+    M = max_model_len or (_round_up(mx, block_size) + block_size)
+    R = len(num_scheduled)
+    dims = Dims(block_size=block_size, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                head_dim=head_dim, max_num_reqs=max(R, num_reqs_padded or 0, 1), max_model_len=M,
+                max_blocks_per_req=M // block_size,
+                num_blocks=_pool_blocks_for(num_computed, num_scheduled, block_size) + extra_blocks)
+    return _build_spec("explicit", dims, num_computed, num_scheduled, rng, hidden_size, seed,
+                       num_reqs_padded=num_reqs_padded, num_tokens_padded=num_tokens_padded)
+
+
+# --------------------------------------------------------------------------- #
+# chunked-prefill mixed workload: a persistent batch evolved over many steps
+# --------------------------------------------------------------------------- #
+@dataclass
+class _Req:
+    uid: int
+    kind: str  # "chunk" or "decode"
+    computed: int
+    prompt_len: int
+    tokens: np.ndarray
+    pages: List[int] = field(default_factory=list)
+
+
+class MixedChunkSimulator:
+    """Persistent-batch harness for the 8192-token-budget chunked-prefill workload.
+
+    The batch starts with 4 chunked-prefill rows (chunks of U[1024, 2048] tokens on top of
+    U[0, 16384] prior context) and 128 decode rows (context U[256, 32768]).  Every row finishes
+    with probability 5% per step (or when it nears the model length); a fresh request of the same
+    kind arrives one step later.  Finished rows leave holes: arrivals fill the lowest holes first,
+    then append at the tail, and the remaining holes are closed by moving tail rows down
+    (condense).  Page tables grow as sequences cross page boundaries.  Chunk lengths are drawn
+    first and then shrunk in proportion until the step's total fits the token budget.
+    """
+
+    BUDGET = 8192
+    N_CHUNK = 4
+    N_DECODE = 128
+    FINISH_P = 0.05
+
+    def __init__(self, seed: int = 4000, num_blocks: int = 180_001, max_model_len: int = 65536,
+                 max_num_reqs: int = 160):
+        self.rng = np.random.default_rng(seed)
+        self.seed = seed
+        self.dims = Dims(block_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128,
+                         max_num_reqs=max_num_reqs, max_model_len=max_model_len,
+                         max_blocks_per_req=max_model_len // 16, num_blocks=num_blocks)
+        self.pool = PagePool(num_blocks, 0, self.rng)
+        self.rows: List[Optional[_Req]] = []
+        self.arrivals: List[str] = []
+        self.next_uid = 0
+        self.step_index = 0
+        self.moves = 0
+        self.token_table = np.zeros((max_num_reqs, max_model_len), dtype=np.int32)
+        self.block_table = np.full((max_num_reqs, self.dims.max_blocks_per_req), -1, dtype=np.int32)
+        for kind in ["chunk"] * self.N_CHUNK + ["decode"] * self.N_DECODE:
+            self.rows.append(self._fresh(kind))
+            self._install(len(self.rows) - 1, self.rows[-1])
+
+    def _fresh(self, kind: str) -> _Req:
+        M = self.dims.max_model_len
+        if kind == "chunk":
+            c = int(self.rng.integers(0, 16384, endpoint=True))
+            prompt = min(M - 1, c + int(self.rng.integers(4096, 24576, endpoint=True)))
+        else:
+            c = int(self.rng.integers(256, 32768, endpoint=True))
+            prompt = c
+        toks = self.rng.integers(0, VOCAB, size=M, dtype=np.int32)
+        r = _Req(uid=self.next_uid, kind=kind, computed=c, prompt_len=prompt, tokens=toks)
+        self.next_uid += 1
+        return r
+
+    def _install(self, row: int, r: _Req) -> None:
+        self.token_table[row, :] = r.tokens
+        self.block_table[row, :] = -1
+        if r.pages:
+            self.block_table[row, :len(r.pages)] = r.pages
+
+    def _clear(self, row: int) -> None:
+        self.token_table[row] = 0
+        self.block_table[row] = -1
+        self.rows[row] = None
+
+    def _update_states(self) -> None:
+        M = self.dims.max_model_len
+        holes, finished = [], []
+        for i, r in enumerate(self.rows):
+            if r.computed + 2048 >= M or self.rng.random() < self.FINISH_P:
+                self.pool.give_back(r.pages)
+                self._clear(i)
+                holes.append(i)
+                finished.append(r.kind)
+        for kind in self.arrivals:
+            r = self._fresh(kind)
+            if holes:
+                row = holes.pop(0)
+                self.rows[row] = r
+            else:
+                self.rows.append(r)
+                row = len(self.rows) - 1
+            self._install(row, r)
+        self.arrivals = finished
+        # condense: close the remaining holes with rows taken from the tail
+        while holes:
+            last = len(self.rows) - 1
+            if self.rows[last] is None:
+                self.rows.pop()
+                holes.remove(last)
+                continue
+            h = holes.pop(0)
+            self.token_table[h] = self.token_table[last]
+            self.block_table[h] = self.block_table[last]
+            self.rows[h] = self.rows[last]
+            self._clear(last)
+            self.rows.pop()
+            self.moves += 1
+
+    def next_step(self) -> BatchSpec:
+        if self.step_index > 0:
+            self._update_states()
+        q = [int(self.rng.integers(1024, 2048, endpoint=True)) if r.kind == "chunk" else 1
+             for r in self.rows]
+        chunk_idx = [i for i, r in enumerate(self.rows) if r.kind == "chunk"]
+        total = sum(q)
+        if total > self.BUDGET and chunk_idx:
+            room = self.BUDGET - (total - sum(q[i] for i in chunk_idx))
+            scale = room / sum(q[i] for i in chunk_idx)
+            for i in chunk_idx:
+                q[i] = max(1, int(q[i] * scale))
+        for i, r in enumerate(self.rows):
+            need = pages_for(r.computed + q[i], self.dims.block_size)
+            if need > len(r.pages):
+                r.pages.extend(self.pool.take(need - len(r.pages)))
+                self.block_table[i, :len(r.pages)] = r.pages
+        spec = BatchSpec(name=f"chunked-prefill mix step {self.step_index}", dims=self.dims,
+                         num_computed=np.array([r.computed for r in self.rows], np.int32),
+                         num_scheduled=np.array(q, np.int32),
+                         num_reqs_padded=len(self.rows), num_tokens_padded=int(sum(q)),
+                         token_table=self.token_table.copy(), block_table=self.block_table.copy(),
+                         hidden_size=4096, seed=self.seed * 1000 + self.step_index,
+                         num_prompt=np.array([r.prompt_len for r in self.rows], np.int32))
+        for i, r in enumerate(self.rows):
+            r.computed += q[i]
+            if r.kind == "decode":
+                r.prompt_len = r.computed
+        self.step_index += 1
+        return spec
+
+
+def config4_steps(num_steps: int = 100, seed: int = 4000) -> Iterator[BatchSpec]:
+    sim = MixedChunkSimulator(seed=seed)
+    for _ in range(num_steps):
+        yield sim.next_step()
+
+
+# --------------------------------------------------------------------------- #
+# activations and the paged pool (torch; CPU or CUDA)
+# --------------------------------------------------------------------------- #
+@dataclass
+class Tensors:
+    """bf16 tensors of one step: new Q/K/V rows, hidden rows, per-request history, the pool."""
+
+    q: "object"  # [N_pad, nh, hd]
+    k: "object"  # [N_pad, nkv, hd]
+    v: "object"  # [N_pad, nkv, hd]
+    hidden: "object"  # [N_pad, H]
+    hist_k: list  # per request [c_i, nkv, hd]
+    hist_v: list
+    k_cache: "object"  # [num_blocks * B, nkv, hd]
+    v_cache: "object"
+
+
+def make_tensors(spec: BatchSpec, device="cpu", with_pool: bool = True, with_history: bool = True):
+    """Seeded bf16 activations; the history of request i is placed page by page into the pool."""
+    import torch
+
+    d = spec.dims
+    g = torch.Generator(device=device)
+    g.manual_seed(spec.seed)
+    Np = spec.num_tokens_padded
+    bf = torch.bfloat16
+
+    def randn(*shape):
+        return torch.randn(*shape, generator=g, device=device, dtype=torch.float32).to(bf)
+
+    q = randn(Np, d.num_q_heads, d.head_dim)
+    k = randn(Np, d.num_kv_heads, d.head_dim)
+    v = randn(Np, d.num_kv_heads, d.head_dim)
+    hidden = randn(Np, spec.hidden_size)
+    hist_k, hist_v = [], []
+    if with_history:
+        for i in range(spec.num_reqs):
+            c = int(spec.num_computed[i])
+            hist_k.append(randn(c, d.num_kv_heads, d.head_dim))
+            hist_v.append(randn(c, d.num_kv_heads, d.head_dim))
+    k_cache = v_cache = None
+    if with_pool:
+        k_cache = randn(d.num_slots, d.num_kv_heads, d.head_dim)
+        v_cache = randn(d.num_slots, d.num_kv_heads, d.head_dim)
+        if with_history:
+            place_history(spec, hist_k, k_cache)
+            place_history(spec, hist_v, v_cache)
+    return Tensors(q=q, k=k, v=v, hidden=hidden, hist_k=hist_k, hist_v=hist_v,
+                   k_cache=k_cache, v_cache=v_cache)
+
+
+def place_history(spec: BatchSpec, hist: list, cache) -> None:
+    """Copy each request's contiguous history into its pages, one whole page at a time."""
+    import torch
+
+    d = spec.dims
+    B = d.block_size
+    pages = cache.view(d.num_blocks, B, d.num_kv_heads, d.head_dim)
+    for i, h in enumerate(hist):
+        c = h.shape[0]
+        full = c // B
+        row = torch.as_tensor(spec.block_table[i], device=cache.device, dtype=torch.long)
+        if full:
+            pages[row[:full]] = h[: full * B].view(full, B, d.num_kv_heads, d.head_dim)
+        rem = c - full * B
+        if rem:
+            pages[int(spec.block_table[i, full]), :rem] = h[full * B:]
+
+
+def device_tables(spec: BatchSpec, device):
+    """The persistent arrays as int32 device tensors (token table, page table, counters)."""
+    import torch
+
+    def t(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
+
+    return dict(token_table=t(spec.token_table), block_table=t(spec.block_table),
+                num_computed=t(spec.num_computed), num_scheduled=t(spec.num_scheduled))
+
+
+def with_padding(spec: BatchSpec, num_reqs_padded: int, num_tokens_padded: int) -> BatchSpec:
+    return dataclasses.replace(spec, num_reqs_padded=num_reqs_padded,
+                               num_tokens_padded=num_tokens_padded)
