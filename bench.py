@@ -1,0 +1,467 @@
+#!/usr/bin/env python
+"""Throughput of one flattened mixed-batch step on GB300 (prepare_inputs -> kv_write ->
+paged_attention -> gather_rows, one attention layer, synthetic bf16 activations).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C]
+
+Prints ONE JSON line on rank 0.  The headline workload is the pages' padding example
+(query lens [2000, 512, 1 x 6]; 32 q / 8 kv heads, head_dim 128, block 16, hidden 4096).
+``--config`` selects another workload for local study (1 worked example, 3 pure decode,
+4 chunked-prefill mix step 0, 5 long context); those lines are not the headline.
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the launching
+stream with a 512 MiB write between steps (outside the events) so every step starts with a
+cold L2; barrier + synchronize around the whole region; max over ranks.  Under torchrun every
+rank runs its own independent batch (data parallel, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "mixed-step tokens/s; decode-attn HBM GB/s & prefill TFLOPS vs peak"
+UNIT = "tokens/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# dram bytes (read + write) per attention call measured by ncu for the attention kernels as
+# they stand, keyed by the hash of their sources; null once the sources change.
+KNOWN_TRAFFIC = {}
+
+
+# ----------------------------------------------------------------------------- workloads
+def make_spec(config: int, rank: int = 0):
+    import workloads as wl
+
+    if config == 1:
+        return wl.config1(step=rank)
+    if config == 2:
+        return wl.config2(step=rank)
+    if config == 3:
+        return wl.config3(step=rank)
+    if config == 4:
+        return wl.MixedChunkSimulator(seed=4000 + 7919 * rank).next_step()
+    if config == 5:
+        return wl.config5(step=rank)
+    raise SystemExit(f"unknown config {config}")
+
+
+def workload_name(spec, config):
+    d = spec.dims
+    return {
+        "workload": {1: "pages' worked example A/B/C", 2: "pages' padding example",
+                     3: "pure decode x256", 4: "chunked-prefill mix (step 0)",
+                     5: "long-context 70B-like"}[config],
+        "query_lens": (spec.num_scheduled.tolist() if spec.num_reqs <= 8
+                       else f"{spec.num_reqs} requests"),
+        "num_reqs": spec.num_reqs, "num_tokens": spec.num_tokens,
+        "num_tokens_padded": spec.num_tokens_padded, "q_heads": d.num_q_heads,
+        "kv_heads": d.num_kv_heads, "head_dim": d.head_dim, "block_size": d.block_size,
+        "hidden": spec.hidden_size, "kv_pages": d.num_blocks,
+        "l2": "flushed before every timed step (512 MiB write, outside the events)",
+    }
+
+
+def work_counts(spec):
+    """Algorithmic work of the step (what the pages define, not what the kernels do)."""
+    d = spec.dims
+    g = d.num_q_heads // d.num_kv_heads
+    dec_bytes = pre_flops = dec_flops = 0
+    for c, q in zip(spec.num_computed.tolist(), spec.num_scheduled.tolist()):
+        visible = q * c + q * (q + 1) // 2                 # sum over j of (c + j + 1)
+        flops = 4 * d.num_q_heads * d.head_dim * visible
+        if q * g <= 8:  # decode-like: bound by reading the request's K/V once per kv head
+            L = c + q
+            dec_bytes += L * 2 * d.num_kv_heads * d.head_dim * 2 \
+                + 2 * q * d.num_q_heads * d.head_dim * 2 + -(-L // d.block_size) * 4
+            dec_flops += flops
+        else:
+            pre_flops += flops
+    N, Np, R = spec.num_tokens, spec.num_tokens_padded, spec.num_reqs
+    row = d.num_kv_heads * d.head_dim * 2
+    return dict(
+        attn_flops=pre_flops + dec_flops, prefill_flops=pre_flops, decode_flops=dec_flops,
+        decode_bytes=dec_bytes,
+        kv_write_bytes=2 * 2 * Np * row,                       # K and V, read + write
+        meta_bytes=Np * (4 + 4 + 3 * 4) + R * (2 * 4 + 3 * 4),
+        gather_bytes=2 * spec.num_reqs_padded * spec.hidden_size * 2)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            return json.load(f), "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def attention_sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "ragged_mixed_paged_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.startswith("attn") or f in ("attention.cu", "rb_internal.cuh"):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        try:
+            import torch
+
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.ident = uuid if uuid.startswith("GPU-") else f"GPU-{uuid}"
+        except Exception:
+            self.ident = str(device_index)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.ident, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        for line in out.strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[3:7]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- ranks
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws <= 1:
+        return 0, 1, 0
+    import torch
+    import torch.distributed as dist
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend == "nccl":
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend)
+    return dist.get_rank(), dist.get_world_size(), local
+
+
+def reduce_over_ranks(value: float, op: str, world: int, device=None) -> float:
+    """max / sum of a float over all ranks (timing bookkeeping only, never step data)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX if op == "max" else dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_step_sample(spec, tens, rows):
+    """The CPU oracle on a row sample of the step: metadata, KV write, attention for `rows`,
+    gather.  Returns seconds."""
+    import numpy as np
+    import torch
+
+    import oracle
+
+    d = spec.dims
+    f64 = lambda t: t.float().numpy().astype(np.float64)
+    u16 = lambda t: t.view(torch.int16).numpy()
+    t0 = time.perf_counter()
+    meta = oracle.prepare_inputs(block_size=d.block_size, null_block=d.null_block,
+                                 token_table=spec.token_table, block_table=spec.block_table,
+                                 num_computed=spec.num_computed,
+                                 num_scheduled=spec.num_scheduled,
+                                 num_reqs_padded=spec.num_reqs_padded,
+                                 num_tokens_padded=spec.num_tokens_padded)
+    oracle.kv_write(u16(tens.k_cache), u16(tens.v_cache), meta["slot_mapping"], u16(tens.k),
+                    u16(tens.v))
+    oracle.paged_attention(f64(tens.q), [f64(h) for h in tens.hist_k],
+                           [f64(h) for h in tens.hist_v], f64(tens.k), f64(tens.v),
+                           meta["query_start_loc"], meta["seq_lens"], spec.num_reqs, rows=rows)
+    oracle.gather_rows(u16(tens.hidden), meta["logits_indices"])
+    return time.perf_counter() - t0
+
+
+def row_sample(spec, stride, offset=0):
+    return list(range(offset % stride, spec.num_tokens, stride))
+
+
+def cpu_baseline(spec, target_s=12.0):
+    """Oracle timed on this host's cores on a bounded row sample of the same workload."""
+    import workloads as wl
+
+    tens = wl.make_tensors(spec, device="cpu")
+    probe = max(1, spec.num_tokens // 40)
+    t = oracle_step_sample(spec, tens, row_sample(spec, probe))
+    per_row = t / len(row_sample(spec, probe))
+    stride = max(1, math.ceil(spec.num_tokens * per_row / target_s))
+    rows = row_sample(spec, stride)
+    c0, w0 = time.process_time(), time.perf_counter()
+    t = oracle_step_sample(spec, tens, rows)
+    cores = (time.process_time() - c0) / max(time.perf_counter() - w0, 1e-9)
+    return {"value": len(rows) / t, "unit": UNIT, "cores": round(cores, 1),
+            "host_cores": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"every {stride}th of {spec.num_tokens} query rows (all heads) with the "
+                      f"full metadata, KV write and gather; {t:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    spec = make_spec(args.config)
+    import workloads as wl
+
+    tens = wl.make_tensors(spec, device="cpu")
+    budget = 150.0 / max(1, args.steps + args.warmup)      # seconds per step
+    probe = max(1, spec.num_tokens // 40)
+    t = oracle_step_sample(spec, tens, row_sample(spec, probe))
+    per_row = t / len(row_sample(spec, probe))
+    stride = max(1, math.ceil(spec.num_tokens * per_row / budget))
+    for w in range(max(0, args.warmup - 1)):
+        oracle_step_sample(spec, tens, row_sample(spec, stride, w))
+    times, nrows = [], 0
+    c0, w0 = time.process_time(), time.perf_counter()
+    for k in range(args.steps):
+        rows = row_sample(spec, stride, k)
+        times.append(oracle_step_sample(spec, tens, rows))
+        nrows += len(rows)
+    cores = (time.process_time() - c0) / max(time.perf_counter() - w0, 1e-9)
+    total = sum(times)
+    value = nrows / total
+    sample = (f"each step: the oracle's metadata, KV write and gather in full plus attention "
+              f"for every {stride}th query row (all heads), rotating the offset per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000 * total / max(1, args.steps), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_name(spec, args.config),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": round(cores, 1),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    import torch
+
+    import workloads as wl
+    import ragged_mixed_paged_gb300 as rb
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    spec = make_spec(args.config, rank)
+    d = spec.dims
+    tens = wl.make_tensors(spec, device=dev)
+    tables = wl.device_tables(spec, dev)
+    buf = rb.StepBuffers.allocate(rb.Dims.of(d), spec.num_reqs, spec.num_reqs_padded,
+                                  spec.num_tokens, spec.num_tokens_padded, tables, tens.q,
+                                  tens.k, tens.v, tens.hidden, tens.k_cache, tens.v_cache)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    E = lambda: torch.cuda.Event(enable_timing=True)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        rb.run_step(buf)
+    torch.cuda.synchronize()
+    if int(buf.meta["scalars"][3].item()) != 0:
+        raise SystemExit(f"device error word {int(buf.meta['scalars'][3].item()):#x}")
+
+    marks = [[E() for _ in range(5)] for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    launches0 = rb.launch_count()
+    w0 = time.perf_counter()
+    for k in range(args.steps):
+        flush.zero_()
+        rb.run_step(buf, marks=marks[k])
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - w0
+    launches = rb.launch_count() - launches0
+    clocks = sampler.stop()
+
+    def span(a, b):
+        return [m[a].elapsed_time(m[b]) for m in marks]
+
+    step_ms = statistics.mean(span(0, 4))
+    parts = {"prepare_inputs": span(0, 1), "kv_write": span(1, 2),
+             "paged_attention": span(2, 3), "gather_rows": span(3, 4)}
+    parts_ms = {k: statistics.mean(v) for k, v in parts.items()}
+    step_ms_max = reduce_over_ranks(step_ms, "max", world, dev)
+    total_tokens = reduce_over_ranks(float(spec.num_tokens), "sum", world, dev)
+    value = total_tokens / (step_ms_max / 1000.0)
+
+    w = work_counts(spec)
+    pk, pk_kind = peaks()
+    attn_s = parts_ms["paged_attention"] / 1000.0
+    # the attention call dominates the step; whether it is tensor- or HBM-bound depends on the mix
+    t_tensor = w["attn_flops"] / (pk["bf16_tflops"] * 1e12)
+    t_hbm = w["decode_bytes"] / (pk["hbm_gbs"] * 1e9)
+    src_hash = attention_sources_hash()
+    traffic = KNOWN_TRAFFIC.get((args.config, src_hash))
+    if t_tensor >= t_hbm:
+        achieved = w["attn_flops"] / attn_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
+                "kernel": "rb_paged_attention (plan + decode + prefill + combine launches)",
+                "peak_kind": f"bf16 dense burst, {pk_kind}"}
+    else:
+        achieved = w["decode_bytes"] / attn_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
+                "kernel": "rb_paged_attention (plan + decode + prefill + combine launches)",
+                "peak_kind": f"HBM copy, {pk_kind}"}
+
+    e2e = measure_e2e(spec, tens, buf, dev, args, flush, world)
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 Q/K/V/hidden, random page ids; no weights)",
+            "config": workload_name(spec, args.config), "roofline": roof,
+            "components_ms": parts_ms,
+            "work": {"attention_tflop": w["attn_flops"] / 1e12,
+                     "decode_kv_gb": w["decode_bytes"] / 1e9,
+                     "attention_tflops": w["attn_flops"] / attn_s / 1e12,
+                     "decode_part_gbs_if_alone": w["decode_bytes"] / attn_s / 1e9},
+            "gpu_launches": launches, "wall_s": wall, "clocks": clocks, "e2e": e2e,
+            "attention_source_hash": src_hash}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(spec)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def measure_e2e(spec, tens, buf, dev, args, flush, world):
+    """Same step through the public API with inputs copied from pinned host memory and the
+    results read back, copies inside the timed region."""
+    import torch
+
+    import ragged_mixed_paged_gb300 as rb
+
+    host_in = {
+        "token_table": buf.token_table.cpu().pin_memory(),
+        "block_table": buf.block_table.cpu().pin_memory(),
+        "num_computed": buf.num_computed.cpu().pin_memory(),
+        "num_scheduled": buf.num_scheduled.cpu().pin_memory(),
+        "q": buf.q.cpu().pin_memory(), "k": buf.k.cpu().pin_memory(),
+        "v": buf.v.cpu().pin_memory(), "hidden": buf.hidden.cpu().pin_memory(),
+    }
+    dst = {"token_table": buf.token_table, "block_table": buf.block_table,
+           "num_computed": buf.num_computed, "num_scheduled": buf.num_scheduled,
+           "q": buf.q, "k": buf.k, "v": buf.v, "hidden": buf.hidden}
+    host_out = {"attn_out": torch.empty_like(buf.attn_out, device="cpu").pin_memory(),
+                "rows_out": torch.empty_like(buf.rows_out, device="cpu").pin_memory(),
+                "scalars": torch.empty(4, dtype=torch.int32).pin_memory()}
+    src_out = {"attn_out": buf.attn_out, "rows_out": buf.rows_out,
+               "scalars": buf.meta["scalars"]}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def step():
+        for k, t in host_in.items():
+            dst[k].copy_(t, non_blocking=True)
+        rb.run_step(buf)
+        for k, t in host_out.items():
+            t.copy_(src_out[k], non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    n = max(3, min(args.steps, 50))
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n)]
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        step()
+        b.record()
+    torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms = reduce_over_ranks(ms, "max", world, dev)
+    return {"value": world * spec.num_tokens / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    rank, world, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

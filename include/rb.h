@@ -1,0 +1,206 @@
+/*
+ * rb.h — C ABI of the ragged mixed-batch step library (librb.so), NVIDIA GB300 / sm_103a.
+ *
+ * One flattened, unpadded forward step over a mixed batch of full prefills, chunked-prefill
+ * segments and decodes, for ONE attention layer:
+ *
+ *   rb_prepare_inputs   persistent batch arrays -> flat step inputs + attention metadata
+ *   rb_kv_write         this step's new K/V rows -> paged KV cache (by slot_mapping)
+ *   rb_paged_attention  varlen causal GQA attention through the page table
+ *   rb_gather_rows      hidden rows at logits_indices (the rows the LM head needs)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Every pointer named d_* is DEVICE memory on the current CUDA device; the caller owns it,
+ *    allocates it and keeps it alive until the work queued on `stream` has finished.  The
+ *    library allocates no device memory and never synchronises: each call only enqueues
+ *    kernels (and, for rb_prepare_inputs, one 4-byte memset) on `stream`, a cudaStream_t passed
+ *    as void* (NULL = the legacy default stream).
+ *  - All index arrays are int32.  bf16 tensors are passed as void* holding IEEE bfloat16 bits.
+ *  - Host-side checks (null pointers, sizes, alignment, unsupported shapes) run before anything
+ *    is enqueued and return a status other than RB_OK; nothing is enqueued then.
+ *  - Device-side checks never trap and never spin without limit: a violated precondition sets a
+ *    bit (RB_EBIT_*) in a caller-owned int32 error word with atomicOr, the offending access is
+ *    skipped or redirected to the null page, and the kernel carries on.  The caller zeroes the
+ *    word when it wants a fresh reading (rb_prepare_inputs zeroes its own) and reads it after
+ *    the step.  Results are unspecified where a bit was set.
+ *  - RB_ERR_CUDA means a CUDA runtime call failed (for example a launch error); the failing
+ *    call's cudaError_t can be read with cudaGetLastError().
+ *
+ * Page layout (per layer, K and V separate tensors): [num_blocks * block_size, nkv, head_dim]
+ * bf16, i.e. row `slot` holds the K (or V) of one token for all kv heads; slot =
+ * page_id * block_size + offset ("vLLM 源码完全拆解（五）…", "Block table 是逐请求的页表";
+ * nano-vLLM's per-layer cache [num_blocks, block_size, kv_heads, head_dim]).
+ */
+#ifndef RB_H_
+#define RB_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rb_status {
+  RB_OK = 0,
+  RB_ERR_INVALID_ARG = 1, /* null pointer, negative or inconsistent size, misaligned buffer */
+  RB_ERR_CAPACITY = 2,    /* a size exceeds a capacity given in rb_dims or the workspace */
+  RB_ERR_CUDA = 4,        /* a CUDA runtime call failed */
+  RB_ERR_UNSUPPORTED = 5  /* a shape this build has no kernel for */
+} rb_status;
+
+/* Device error-word bits (atomicOr'ed; see the conventions above). */
+#define RB_EBIT_NUM_SCHEDULED 0x001 /* a real request has num_scheduled < 1 */
+#define RB_EBIT_NUM_COMPUTED 0x002  /* a real request has num_computed < 0 */
+#define RB_EBIT_SEQ_LEN 0x004       /* num_computed + num_scheduled > max_model_len, or it
+                                       needs more pages than max_blocks_per_req */
+#define RB_EBIT_TOKEN_SUM 0x008     /* sum of num_scheduled != num_tokens */
+#define RB_EBIT_BLOCK_ID 0x010      /* a page id read for a real token is outside
+                                       [0, num_blocks) or is the null page */
+#define RB_EBIT_SLOT 0x020          /* rb_kv_write: slot >= num_blocks * block_size */
+#define RB_EBIT_ROW_INDEX 0x040     /* rb_gather_rows: index outside [0, num_hidden_rows) */
+#define RB_EBIT_ATTN_META 0x080     /* rb_paged_attention: query_start_loc not monotone, last
+                                       entry != num_tokens, seq_len < query length, or seq_len
+                                       beyond max_blocks_per_req pages */
+#define RB_EBIT_TIMEOUT 0x100       /* a bounded wait on an asynchronous copy gave up */
+
+/* Static sizes of the persistent batch and of one layer's paged KV pool. */
+typedef struct rb_dims {
+  int32_t block_size;         /* B: tokens per KV page */
+  int32_t num_q_heads;        /* nh */
+  int32_t num_kv_heads;       /* nkv; nh % nkv == 0, query head h reads kv head h / (nh/nkv) */
+  int32_t head_dim;           /* hd */
+  int32_t max_num_reqs;       /* rows of the token table and of the page table */
+  int32_t max_model_len;      /* M: columns of the token table */
+  int32_t max_blocks_per_req; /* MB: columns of the page table */
+  int32_t num_blocks;         /* physical pages in the pool, the null page included */
+  int32_t null_block;         /* reserved page id that receives every padding token */
+} rb_dims;
+
+/* Human-readable name of a status code (static string). */
+const char* rb_status_string(int32_t status);
+
+/* Number of kernels this library has enqueued since it was loaded (all devices, all calls). */
+uint64_t rb_kernel_launch_count(void);
+
+/*
+ * rb_pad_for_graph — host function; smallest entry of `capture_sizes` (sorted ascending,
+ * `num_sizes` entries) that is >= num_tokens; num_tokens itself when it exceeds the largest size
+ * (the step then runs unpadded), and -1 for invalid arguments (null sizes with num_sizes > 0,
+ * num_sizes < 0, num_tokens < 0, unsorted sizes).
+ * Source: "第8章 ModelRunner：从 SchedulerOutput 到 GPU Kernel", "8.5 pad_for_cudagraph" and
+ * "8.5.0.5 pad_for_cudagraph 的实现" (bisect_left over sorted sizes); "04 · 模型执行与 CUDA Graph",
+ * "4.4 派发" (beyond the largest captured size the step runs eager).
+ */
+int32_t rb_pad_for_graph(const int32_t* capture_sizes, int32_t num_sizes, int32_t num_tokens);
+
+/*
+ * rb_prepare_inputs — flatten one step of the persistent batch.
+ * Source: "vLLM 源码完全拆解（五）：GPUModelRunner 如何把动态请求拼成一次 GPU 前向", sections
+ * "第一步" (query_start_loc = exclusive prefix sum of num_scheduled), "第二步" (positions =
+ * num_computed + offset in the request; seq_lens = num_computed + num_scheduled), "第三步"
+ * (input ids gathered from row i, columns c_i .. c_i+q_i-1 of the token table), "第四步"
+ * (logits_indices = query_start_loc[1:] - 1), "Block table 是逐请求的页表" (slot_mapping) and
+ * "固定地址与动态有效长度如何共存" (padding to a captured size); "04 · 模型执行与 CUDA Graph",
+ * "5. 关键细节与坑" (padding tokens use the null page).
+ *
+ * Inputs (device, int32):
+ *   d_token_table   [max_num_reqs, max_model_len]       row i = token history of batch row i
+ *   d_num_computed  [num_reqs]                          tokens already in the cache (c_i)
+ *   d_num_scheduled [num_reqs]                          tokens scheduled this step (q_i >= 1)
+ *   d_block_table   [max_num_reqs, max_blocks_per_req]  physical page ids of each row
+ * Sizes: 0 <= num_reqs <= num_reqs_padded <= max_num_reqs; num_tokens = sum(q_i) (checked on the
+ *   device); num_tokens <= num_tokens_padded; num_tokens_padded >= 1 when num_reqs_padded >= 1.
+ * Outputs (device, int32, written in full):
+ *   d_input_ids, d_positions, d_slot_mapping  [num_tokens_padded]
+ *   d_query_start_loc                          [num_reqs_padded + 1]
+ *   d_seq_lens, d_logits_indices               [num_reqs_padded]
+ *   d_scalars [4] = {max_query_len, max_seq_len, num_actual_tokens (= num_tokens), error word}
+ * Padding: request i >= num_reqs gets the empty interval at the end (query_start_loc = N),
+ *   seq_len 0 and logits index max(N-1, 0); token t >= N gets input id 0, position 0 and slot
+ *   null_block * B + (t - N) % B, so padding only ever touches the null page.
+ * Errors: host -> RB_ERR_INVALID_ARG / RB_ERR_CAPACITY / RB_ERR_UNSUPPORTED (num_reqs > 16384);
+ *   device -> bits NUM_SCHEDULED, NUM_COMPUTED, SEQ_LEN, TOKEN_SUM, BLOCK_ID in d_scalars[3]
+ *   (zeroed by this call); a token whose page id is invalid gets a null-page slot.
+ */
+rb_status rb_prepare_inputs(const rb_dims* dims, int32_t num_reqs, int32_t num_reqs_padded,
+                            int32_t num_tokens, int32_t num_tokens_padded,
+                            const int32_t* d_token_table, const int32_t* d_num_computed,
+                            const int32_t* d_num_scheduled, const int32_t* d_block_table,
+                            int32_t* d_input_ids, int32_t* d_positions,
+                            int32_t* d_query_start_loc, int32_t* d_seq_lens,
+                            int32_t* d_slot_mapping, int32_t* d_logits_indices,
+                            int32_t* d_scalars, void* stream);
+
+/*
+ * rb_kv_write — scatter this step's K and V rows into the paged cache.
+ * Source: "vLLM 源码完全拆解（五）…", "3. 物理 KV 槽位" (row t goes to slot_mapping[t]);
+ * "变长批处理与一次混合前向", runner.py (the write happens before attention reads the context);
+ * "Nano-VLLM全代码解析笔记(4)-model_runner" (a slot of -1 is skipped).
+ *
+ *   d_k, d_v        [num_tokens_padded, nkv, hd] bf16, rows contiguous, 16-byte aligned
+ *   d_slot_mapping  [num_tokens_padded] int32; slot < 0 -> row skipped
+ *   d_k_cache, d_v_cache  [num_blocks * B, nkv, hd] bf16, 16-byte aligned (updated in place)
+ *   d_error_word    int32 or NULL; bit SLOT for slot >= num_blocks * B (row skipped)
+ * Two real tokens must not share a slot (then the surviving row is unspecified).
+ */
+rb_status rb_kv_write(const rb_dims* dims, int32_t num_tokens_padded, const void* d_k,
+                      const void* d_v, const int32_t* d_slot_mapping, void* d_k_cache,
+                      void* d_v_cache, int32_t* d_error_word, void* stream);
+
+/*
+ * Workspace bytes rb_paged_attention needs for batches of at most max_num_reqs requests and
+ * max_num_tokens real tokens (0 on invalid arguments).  The workspace is caller-owned device
+ * memory, at least 256-byte aligned; its contents need no initialisation and are scratch.
+ */
+size_t rb_paged_attention_workspace_size(const rb_dims* dims, int32_t max_num_reqs,
+                                         int32_t max_num_tokens);
+
+/*
+ * rb_paged_attention — varlen causal GQA attention of a mixed batch through the page table.
+ * Source: "vLLM 源码完全拆解（五）…", "4. 注意力读取边界" (query j of request i reads only its
+ * own request, keys 0 .. c_i + j, c_i = seq_len - query length) and "为什么不显式构造巨大
+ * Attention Mask" (bounds from query_start_loc, seq_lens, causal=True); "变长批处理与一次混合前向",
+ * runner.py (scale 1/sqrt(hd); new K/V written first, then the whole context is read);
+ * "Nano-VLLM全代码解析笔记(4)-model_runner" (cu_seqlens_q / seq lens / block tables).
+ *
+ *   d_q               [num_tokens_padded, nh, hd] bf16 (this step's queries, flat order)
+ *   d_k_cache/v_cache [num_blocks * B, nkv, hd] bf16 — must already hold this step's rows
+ *   d_block_table     [max_num_reqs, max_blocks_per_req] int32
+ *   d_query_start_loc [num_reqs + 1] int32, d_seq_lens [num_reqs] int32
+ *   softmax_scale     multiplier of q.k (normally 1/sqrt(hd))
+ *   d_out             [num_tokens_padded, nh, hd] bf16; rows >= num_tokens are written as 0
+ *   d_workspace       rb_paged_attention_workspace_size(dims, >= num_reqs, >= num_tokens) bytes
+ *   d_error_word      int32 or NULL; bits ATTN_META, BLOCK_ID, TIMEOUT
+ * Supported: block_size 16, head_dim 64 or 128, nh/nkv <= 16; base pointers 16-byte aligned.
+ * Decodes and short queries (query length x nh/nkv <= 8) run a split-KV streaming kernel; longer
+ * queries run a tensor-core tile kernel; all requests of the batch are handled by one call.
+ */
+rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
+                             int32_t num_tokens_padded, const void* d_q, const void* d_k_cache,
+                             const void* d_v_cache, const int32_t* d_block_table,
+                             const int32_t* d_query_start_loc, const int32_t* d_seq_lens,
+                             float softmax_scale, void* d_out, void* d_workspace,
+                             size_t workspace_bytes, int32_t* d_error_word, void* stream);
+
+/*
+ * rb_gather_rows — out[i, :] = hidden[indices[i], :] for i < num_rows.
+ * Source: "vLLM 源码完全拆解（五）…", "第四步：只在必要位置计算 logits"; "04 · 模型执行与
+ * CUDA Graph", step ⑤ (hidden_states[logits_indices]).
+ *
+ *   d_hidden  [num_hidden_rows, hidden_size] bf16;  d_indices [num_rows] int32
+ *   d_out     [num_rows, hidden_size] bf16
+ *   d_error_word int32 or NULL; bit ROW_INDEX for an index outside [0, num_hidden_rows), whose
+ *   output row is written as zeros.
+ * hidden_size * 2 must be a multiple of 16 bytes and both base pointers 16-byte aligned.
+ */
+rb_status rb_gather_rows(int32_t num_rows, int32_t hidden_size, int32_t num_hidden_rows,
+                         const void* d_hidden, const int32_t* d_indices, void* d_out,
+                         int32_t* d_error_word, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RB_H_ */

@@ -1,0 +1,267 @@
+// rb_paged_attention: varlen causal GQA attention of a mixed batch through the page table.
+//
+// What it computes ("vLLM 源码完全拆解（五）…", "4. 注意力读取边界"; "变长批处理与一次混合前向",
+// runner.py): for request i with c_i = seq_len_i - q_i cached tokens, query j (position c_i + j)
+// and query head h reading kv head h / (nh/nkv):
+//     o = softmax(scale * q . K[0 .. c_i + j]) . V[0 .. c_i + j]
+// over the request's own pages only.
+//
+// One call enqueues four kernels on the caller's stream, with no host round trip (the host
+// only knows num_reqs and the token counts):
+//   1. plan     (1 CTA)  validates the metadata, classifies requests (decode-like when
+//                        query_len * group <= 8), sizes KV splits so the decode work fills the
+//                        GPU, writes per-request unit offsets, zeroes padding rows;
+//   2. decode   (persistent, split-KV, TMA-staged) one warp per (request, kv head, split);
+//   3. prefill  (persistent, tensor-core tiles) one CTA per (request, kv head, 64-row tile);
+//   4. combine  merges the split partials of decode requests with more than one split.
+#include "attn_common.cuh"
+
+namespace rb {
+namespace attn {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+// Block-wide exclusive scan of two int32 values per thread; returns totals via *tot.
+__device__ void block_scan2(int v0, int v1, int* ex0, int* ex1, int* tot0, int* tot1) {
+  __shared__ int s0[32], s1[32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int i0 = v0, i1 = v1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int a = __shfl_up_sync(0xffffffffu, i0, o);
+    const int b = __shfl_up_sync(0xffffffffu, i1, o);
+    if (lane >= o) { i0 += a; i1 += b; }
+  }
+  if (lane == 31) { s0[warp] = i0; s1[warp] = i1; }
+  __syncthreads();
+  if (warp == 0) {
+    int w0 = lane < nw ? s0[lane] : 0, w1 = lane < nw ? s1[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int a = __shfl_up_sync(0xffffffffu, w0, o);
+      const int b = __shfl_up_sync(0xffffffffu, w1, o);
+      if (lane >= o) { w0 += a; w1 += b; }
+    }
+    s0[lane] = w0;
+    s1[lane] = w1;
+  }
+  __syncthreads();
+  *ex0 = i0 - v0 + (warp > 0 ? s0[warp - 1] : 0);
+  *ex1 = i1 - v1 + (warp > 0 ? s1[warp - 1] : 0);
+  *tot0 = s0[nw - 1];
+  *tot1 = s1[nw - 1];
+  __syncthreads();
+}
+
+struct ReqInfo {
+  bool ok;
+  int q, L, pages;
+};
+
+__device__ __forceinline__ ReqInfo req_info(const AttnArgs& a, int r) {
+  ReqInfo x;
+  const int s = a.qsl[r], e = a.qsl[r + 1];
+  x.q = e - s;
+  x.L = a.seq_lens[r];
+  x.pages = (x.L + kPage - 1) / kPage;
+  x.ok = s >= 0 && x.q >= 0 && e <= a.N && x.L >= x.q && x.pages <= a.MB;
+  return x;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(AttnArgs a, int head_dim) {
+  __shared__ unsigned long long s_pages;
+  const int tid = threadIdx.x;
+  const int per = (a.R + kPlanThreads - 1) / kPlanThreads;
+  const int lo = min(tid * per, a.R), hi = min(lo + per, a.R);
+  int bits = 0;
+  if (tid == 0) {
+    s_pages = 0;
+    if (a.qsl[0] != 0 || a.qsl[a.R] != a.N) bits |= RB_EBIT_ATTN_META;
+  }
+  __syncthreads();
+  unsigned long long my_pages = 0;
+  for (int r = lo; r < hi; ++r) {
+    const ReqInfo x = req_info(a, r);
+    if (!x.ok) { bits |= RB_EBIT_ATTN_META; continue; }
+    if (is_decode_class(x.q, a.group)) my_pages += static_cast<unsigned long long>(x.pages);
+  }
+  if (my_pages) atomicAdd(&s_pages, my_pages);
+  __syncthreads();
+  const long long page_heads = static_cast<long long>(s_pages) * a.nkv;
+  const int sp = static_cast<int>(max(static_cast<long long>(kMinSplitPages),
+                                      (page_heads + a.target_units - 1) / a.target_units));
+  int my_d = 0, my_p = 0;
+  for (int r = lo; r < hi; ++r) {
+    const ReqInfo x = req_info(a, r);
+    if (!x.ok || x.q == 0) continue;
+    if (is_decode_class(x.q, a.group)) my_d += (x.pages + sp - 1) / sp * a.nkv;
+    else my_p += (x.q * a.group + kPrefillTileM - 1) / kPrefillTileM * a.nkv;
+  }
+  int ex_d, ex_p, tot_d, tot_p;
+  block_scan2(my_d, my_p, &ex_d, &ex_p, &tot_d, &tot_p);
+  for (int r = lo; r < hi; ++r) {
+    const ReqInfo x = req_info(a, r);
+    a.dec_off[r] = ex_d;
+    a.pre_off[r] = ex_p;
+    if (!x.ok || x.q == 0) continue;
+    if (is_decode_class(x.q, a.group)) ex_d += (x.pages + sp - 1) / sp * a.nkv;
+    else ex_p += (x.q * a.group + kPrefillTileM - 1) / kPrefillTileM * a.nkv;
+  }
+  if (tid == 0) {
+    a.dec_off[a.R] = tot_d;
+    a.pre_off[a.R] = tot_p;
+    a.header[kHNumDecodeUnits] = tot_d;
+    a.header[kHNumPrefillUnits] = tot_p;
+    a.header[kHDecodeNext] = 0;
+    a.header[kHPrefillNext] = 0;
+    a.header[kHSplitPages] = sp;
+  }
+  // rows of padding tokens are written as zeros
+  const long long row16 = static_cast<long long>(a.nh) * head_dim * 2 / 16;
+  int4* out = reinterpret_cast<int4*>(a.out);
+  const long long first = static_cast<long long>(a.N) * row16;
+  const long long last = static_cast<long long>(a.N_pad) * row16;
+  for (long long i = first + tid; i < last; i += kPlanThreads) out[i] = make_int4(0, 0, 0, 0);
+  if (bits) raise_error(a.err, bits);
+}
+
+// Merges the split partials (m, l, o) of one (decode request, kv head): one warp per column.
+template <int HD>
+__global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
+  const int r = blockIdx.x, h = blockIdx.y;
+  const int col = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int base = a.dec_off[r];
+  const int nsplit = (a.dec_off[r + 1] - base) / a.nkv;
+  if (nsplit <= 1) return;
+  const int t0 = a.qsl[r];
+  const int cols = (a.qsl[r + 1] - t0) * a.group;
+  if (col >= cols) return;
+  constexpr int kPer = HD / 32;
+  float mx = -INFINITY;
+  for (int s = 0; s < nsplit; ++s)
+    mx = fmaxf(mx, a.part_ml[static_cast<size_t>(base + s * a.nkv + h) * kMaxCols + col].x);
+  if (mx == -INFINITY) mx = 0.f;
+  float acc[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+  float lsum = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const size_t u = static_cast<size_t>(base + s * a.nkv + h);
+    const float2 ml = a.part_ml[u * kMaxCols + col];
+    const float w = fast_exp2(ml.x - mx);
+    lsum += w * ml.y;
+    const float* o = a.part_o + (u * kMaxCols + col) * HD + lane * kPer;
+    if constexpr (kPer == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(o);
+      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(o);
+      acc[0] += w * v.x; acc[1] += w * v.y;
+    }
+  }
+  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  const int j = col / a.group, hh = col - j * a.group;
+  __nv_bfloat16* dst =
+      a.out + (static_cast<size_t>(t0 + j) * a.nh + h * a.group + hh) * HD + lane * kPer;
+  uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
+#pragma unroll
+  for (int k = 0; k < kPer; k += 2) d32[k / 2] = pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
+}
+
+}  // namespace
+}  // namespace attn
+}  // namespace rb
+
+extern "C" size_t rb_paged_attention_workspace_size(const rb_dims* dims, int32_t max_num_reqs,
+                                                    int32_t max_num_tokens) {
+  if (dims == nullptr || max_num_reqs < 0 || max_num_tokens < 0 || dims->num_kv_heads < 1 ||
+      dims->head_dim < 1)
+    return 0;
+  return rb::attn::ws_layout(dims->head_dim, dims->num_kv_heads, max_num_reqs).total;
+}
+
+extern "C" rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
+                                        int32_t num_tokens_padded, const void* d_q,
+                                        const void* d_k_cache, const void* d_v_cache,
+                                        const int32_t* d_block_table,
+                                        const int32_t* d_query_start_loc,
+                                        const int32_t* d_seq_lens, float softmax_scale,
+                                        void* d_out, void* d_workspace, size_t workspace_bytes,
+                                        int32_t* d_error_word, void* stream) {
+  using namespace rb;
+  using namespace rb::attn;
+  if (dims == nullptr) return RB_ERR_INVALID_ARG;
+  const rb_dims& d = *dims;
+  if (d.block_size != kPage) return RB_ERR_UNSUPPORTED;
+  if (d.head_dim != 64 && d.head_dim != 128) return RB_ERR_UNSUPPORTED;
+  if (d.num_kv_heads < 1 || d.num_q_heads < 1 || d.num_q_heads % d.num_kv_heads != 0)
+    return RB_ERR_INVALID_ARG;
+  if (d.num_q_heads / d.num_kv_heads > 16) return RB_ERR_UNSUPPORTED;
+  if (d.num_blocks < 1 || d.null_block < 0 || d.null_block >= d.num_blocks ||
+      d.max_blocks_per_req < 1 || d.max_num_reqs < 0)
+    return RB_ERR_INVALID_ARG;
+  if (static_cast<long long>(d.num_blocks) * kPage > 0x7fffffffLL) return RB_ERR_CAPACITY;
+  if (num_reqs < 0 || num_tokens < 0 || num_tokens_padded < num_tokens) return RB_ERR_INVALID_ARG;
+  if (num_reqs > d.max_num_reqs) return RB_ERR_CAPACITY;
+  if (!std::isfinite(softmax_scale)) return RB_ERR_INVALID_ARG;
+  if (d_q == nullptr || d_k_cache == nullptr || d_v_cache == nullptr || d_block_table == nullptr ||
+      d_query_start_loc == nullptr || d_seq_lens == nullptr || d_out == nullptr ||
+      d_workspace == nullptr)
+    return RB_ERR_INVALID_ARG;
+  if (!aligned16(d_q) || !aligned16(d_k_cache) || !aligned16(d_v_cache) || !aligned16(d_out) ||
+      (reinterpret_cast<uintptr_t>(d_workspace) & 255u) != 0)
+    return RB_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(d.head_dim, d.num_kv_heads, num_reqs);
+  if (workspace_bytes < w.total) return RB_ERR_CAPACITY;
+
+  CUtensorMap kmap, vmap;
+  const long long num_slots = static_cast<long long>(d.num_blocks) * kPage;
+  if (!encode_kv_tensor_map(&kmap, d_k_cache, d.head_dim, d.num_kv_heads, num_slots) ||
+      !encode_kv_tensor_map(&vmap, d_v_cache, d.head_dim, d.num_kv_heads, num_slots))
+    return RB_ERR_CUDA;
+
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
+  AttnArgs a{};
+  a.q = static_cast<const __nv_bfloat16*>(d_q);
+  a.out = static_cast<__nv_bfloat16*>(d_out);
+  a.block_table = d_block_table;
+  a.qsl = d_query_start_loc;
+  a.seq_lens = d_seq_lens;
+  a.header = reinterpret_cast<int32_t*>(ws + w.header);
+  a.dec_off = reinterpret_cast<int32_t*>(ws + w.dec_off);
+  a.pre_off = reinterpret_cast<int32_t*>(ws + w.pre_off);
+  a.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
+  a.part_o = reinterpret_cast<float*>(ws + w.part_o);
+  a.R = num_reqs;
+  a.N = num_tokens;
+  a.N_pad = num_tokens_padded;
+  a.nh = d.num_q_heads;
+  a.nkv = d.num_kv_heads;
+  a.group = d.num_q_heads / d.num_kv_heads;
+  a.MB = d.max_blocks_per_req;
+  a.num_blocks = d.num_blocks;
+  a.null_block = d.null_block;
+  const int sms = max(1, device_sm_count());
+  a.target_units = min(kMaxTargetUnits, 32 * sms);
+  a.scale_log2 = softmax_scale * 1.4426950408889634f;
+  a.err = d_error_word;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  attn_plan_kernel<<<1, kPlanThreads, 0, s>>>(a, d.head_dim);
+  if (last_launch_status() != RB_OK) return RB_ERR_CUDA;
+  note_launches(1);
+  if (num_reqs == 0) return RB_OK;
+  rb_status st = launch_decode(a, d.head_dim, kmap, vmap, s);
+  if (st != RB_OK) return st;
+  st = launch_prefill(a, d.head_dim, kmap, vmap, s);
+  if (st != RB_OK) return st;
+  const dim3 cgrid(static_cast<unsigned>(num_reqs), static_cast<unsigned>(d.num_kv_heads));
+  if (d.head_dim == 128)
+    attn_combine_kernel<128><<<cgrid, 256, 0, s>>>(a);
+  else
+    attn_combine_kernel<64><<<cgrid, 256, 0, s>>>(a);
+  if (last_launch_status() != RB_OK) return RB_ERR_CUDA;
+  note_launches(1);
+  return RB_OK;
+}

@@ -1,0 +1,96 @@
+"""One pass of the hot path over a batch: prepare_inputs -> kv_write -> paged_attention ->
+gather_rows, on one stream, with no host synchronisation inside.
+
+``StepBuffers`` holds fixed-address device buffers sized once (as a CUDA-graph runner keeps
+them); ``run_step`` only enqueues the four library calls.  The step's error word is the fourth
+scalar written by ``prepare_inputs``; the KV write and the attention OR their bits into it.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Optional
+
+from . import _binding as rb
+
+
+@dataclass
+class StepBuffers:
+    dims: rb.Dims
+    num_reqs: int
+    num_reqs_padded: int
+    num_tokens: int
+    num_tokens_padded: int
+    token_table: object
+    block_table: object
+    num_computed: object
+    num_scheduled: object
+    q: object
+    k: object
+    v: object
+    hidden: object
+    k_cache: object
+    v_cache: object
+    meta: dict
+    attn_out: object
+    workspace: object
+    rows_out: object
+
+    @classmethod
+    def allocate(cls, dims: rb.Dims, num_reqs: int, num_reqs_padded: int, num_tokens: int,
+                 num_tokens_padded: int, tables: dict, q, k, v, hidden, k_cache, v_cache):
+        import torch
+
+        dev = q.device
+        i32 = torch.int32
+        meta = dict(
+            input_ids=torch.empty(num_tokens_padded, dtype=i32, device=dev),
+            positions=torch.empty(num_tokens_padded, dtype=i32, device=dev),
+            query_start_loc=torch.empty(num_reqs_padded + 1, dtype=i32, device=dev),
+            seq_lens=torch.empty(num_reqs_padded, dtype=i32, device=dev),
+            slot_mapping=torch.empty(num_tokens_padded, dtype=i32, device=dev),
+            logits_indices=torch.empty(num_reqs_padded, dtype=i32, device=dev),
+            scalars=torch.zeros(4, dtype=i32, device=dev))
+        ws = torch.empty(rb.workspace_size(dims, max(num_reqs, 1), max(num_tokens, 1)),
+                         dtype=torch.uint8, device=dev)
+        return cls(dims=dims, num_reqs=num_reqs, num_reqs_padded=num_reqs_padded,
+                   num_tokens=num_tokens, num_tokens_padded=num_tokens_padded,
+                   token_table=tables["token_table"], block_table=tables["block_table"],
+                   num_computed=tables["num_computed"], num_scheduled=tables["num_scheduled"],
+                   q=q, k=k, v=v, hidden=hidden, k_cache=k_cache, v_cache=v_cache, meta=meta,
+                   attn_out=torch.empty_like(q), workspace=ws,
+                   rows_out=torch.empty((num_reqs_padded, hidden.shape[1]), dtype=hidden.dtype,
+                                        device=dev))
+
+    @property
+    def error_word(self):
+        return self.meta["scalars"][3:4]
+
+
+def run_step(b: StepBuffers, stream=None, softmax_scale: Optional[float] = None,
+             marks=None) -> None:
+    """Enqueue one whole step (all four library calls) on ``stream``.
+
+    ``marks``: optional five CUDA events, recorded on the same stream before the first call
+    and after each of the four calls (for per-call timing).
+    """
+    def mark(i):
+        if marks is not None:
+            marks[i].record(stream)
+
+    m = b.meta
+    mark(0)
+    rb.prepare_inputs(b.dims, b.num_reqs, b.num_reqs_padded, b.num_tokens, b.num_tokens_padded,
+                      b.token_table, b.num_computed, b.num_scheduled, b.block_table, out=m,
+                      stream=stream)
+    mark(1)
+    rb.kv_write(b.dims, b.k, b.v, m["slot_mapping"], b.k_cache, b.v_cache,
+                error_word=b.error_word, num_tokens_padded=b.num_tokens_padded, stream=stream)
+    mark(2)
+    rb.paged_attention(b.dims, b.num_reqs, b.num_tokens, b.q, b.k_cache, b.v_cache,
+                       b.block_table, m["query_start_loc"], m["seq_lens"], out=b.attn_out,
+                       workspace=b.workspace, softmax_scale=softmax_scale,
+                       error_word=b.error_word, stream=stream)
+    mark(3)
+    rb.gather_rows(b.hidden, m["logits_indices"], num_rows=b.num_reqs_padded, out=b.rows_out,
+                   error_word=b.error_word, stream=stream)
+    mark(4)

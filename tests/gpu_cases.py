@@ -1,0 +1,109 @@
+"""Shared helpers of the GPU parity tests: seeded cases, oracle evaluation, comparisons."""
+import functools
+
+import numpy as np
+import torch
+
+import oracle
+import workloads as wl
+
+ATTN_MAX_ABS = 2e-2   # bf16 output vs the float64 oracle
+ATTN_MEAN_ABS = 2e-3
+
+
+def dims_of(spec):
+    from ragged_mixed_paged_gb300 import Dims
+
+    return Dims.of(spec.dims)
+
+
+def oracle_meta(spec):
+    d = spec.dims
+    return oracle.prepare_inputs(block_size=d.block_size, null_block=d.null_block,
+                                 token_table=spec.token_table, block_table=spec.block_table,
+                                 num_computed=spec.num_computed, num_scheduled=spec.num_scheduled,
+                                 num_reqs_padded=spec.num_reqs_padded,
+                                 num_tokens_padded=spec.num_tokens_padded)
+
+
+def i32(a, device="cuda"):
+    return torch.as_tensor(np.ascontiguousarray(a, dtype=np.int32), device=device)
+
+
+def to64(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+class _Lazy:
+    """A history tensor converted to float64 only when the oracle reads it."""
+
+    def __init__(self, t):
+        self.t = t
+        self.shape = tuple(t.shape)
+
+    def __array__(self, dtype=None, copy=None):
+        a = to64(self.t)
+        return a if dtype is None else a.astype(dtype)
+
+
+@functools.lru_cache(maxsize=1)
+def config4_specs(steps=(0, 1, 57, 99)):
+    out = {}
+    sim = wl.MixedChunkSimulator()
+    for s in range(max(steps) + 1):
+        spec = sim.next_step()
+        if s in steps:
+            out[s] = spec
+    return out
+
+
+def sample_rows(spec, n_random=64, seed=0):
+    """Every decode row, plus the first/last rows, page-boundary rows and random rows of longer
+    queries."""
+    rng = np.random.default_rng(seed)
+    rows, s = [], 0
+    for c, q in zip(spec.num_computed, spec.num_scheduled):
+        c, q = int(c), int(q)
+        if q <= 8:
+            rows.extend(range(s, s + q))
+        else:
+            cand = {s, s + q - 1}
+            edges = [s + j for j in range(q) if (c + j) % 16 in (0, 15)]
+            cand.update(edges[:: max(1, len(edges) // 32)])
+            cand.update(int(x) for x in rng.integers(s, s + q, size=n_random))
+            rows.extend(sorted(cand))
+        s += q
+    return sorted(set(rows))
+
+
+def run_attention(rb, spec, tens, meta, error_word=None):
+    """KV write of this step's rows (oracle slots), then the library's attention."""
+    dims = dims_of(spec)
+    R, N = spec.num_reqs, spec.num_tokens
+    rb.kv_write(dims, tens.k, tens.v, i32(meta["slot_mapping"]), tens.k_cache, tens.v_cache,
+                error_word=error_word)
+    out = rb.paged_attention(dims, R, N, tens.q, tens.k_cache, tens.v_cache,
+                             i32(spec.block_table), i32(meta["query_start_loc"][:R + 1]),
+                             i32(meta["seq_lens"][:R]), error_word=error_word)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle_attention(spec, tens, meta, rows=None):
+    R = spec.num_reqs
+    return oracle.paged_attention(to64(tens.q), [_Lazy(h) for h in tens.hist_k],
+                                  [_Lazy(h) for h in tens.hist_v], to64(tens.k), to64(tens.v),
+                                  meta["query_start_loc"][:R + 1], meta["seq_lens"][:R], R,
+                                  rows=rows)
+
+
+def compare_attention(got, ref, N, rows=None):
+    g = got.float().cpu().numpy().astype(np.float64)
+    sel = np.arange(N) if rows is None else np.asarray(rows)
+    diff = np.abs(g[sel] - ref[sel])
+    assert np.isfinite(g[sel]).all()
+    max_abs, mean_abs = float(diff.max(initial=0.0)), float(diff.mean()) if diff.size else 0.0
+    assert max_abs <= ATTN_MAX_ABS, f"max abs {max_abs}"
+    assert mean_abs <= ATTN_MEAN_ABS, f"mean abs {mean_abs}"
+    assert np.all(g[N:] == 0.0), "padding rows must be zero"
+    return max_abs, mean_abs

@@ -1,0 +1,129 @@
+"""The C ABI loads without a GPU, exports every symbol rb.h declares, and rejects bad
+arguments on the host before anything is enqueued (no compute calls here)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT, load_golden
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from ragged_mixed_paged_gb300 import build
+
+    if not os.path.exists(build.LIB):
+        build.build()
+    import ragged_mixed_paged_gb300._binding as b
+
+    return b
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "rb.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    names = set(re.findall(r"\b(rb_[a-z0-9_]+)\s*\(", src))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"rb_prepare_inputs", "rb_kv_write", "rb_paged_attention", "rb_gather_rows",
+            "rb_pad_for_graph", "rb_paged_attention_workspace_size"} <= set(names)
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings(lib):
+    assert lib.status_string(0) == "ok"
+    assert lib.status_string(5) == "unsupported shape"
+
+
+def test_pad_for_graph_matches_the_pages(lib):
+    g = load_golden("padding_waste.json")
+    sizes = g["inputs"]["capture_sizes"]
+    for n, padded, _ in g["expected"]["graph_padding"]:
+        assert lib.pad_for_graph(sizes, n) == padded
+    assert lib.pad_for_graph(sizes, 1) == 1
+    assert lib.pad_for_graph(sizes, 256) == 256
+    assert lib.pad_for_graph(sizes, 257) == 257        # eager beyond the largest size
+    assert lib.pad_for_graph([], 5) == 5
+    assert lib.pad_for_graph([4, 2], 3) == -1          # unsorted sizes are rejected
+    assert lib.pad_for_graph(sizes, -1) == -1
+    import oracle
+    for n in range(0, 300):
+        assert lib.pad_for_graph(sizes, n) == oracle.pad_for_graph(sizes, n)
+
+
+def _dims(lib, **kw):
+    base = dict(block_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128, max_num_reqs=8,
+                max_model_len=4096, max_blocks_per_req=256, num_blocks=1000, null_block=0)
+    base.update(kw)
+    return lib.rb_dims(*[base[f] for f, _ in lib.rb_dims._fields_])
+
+
+FAKE = ctypes.c_void_p(0x100000)  # never dereferenced: every call below fails its host checks
+MISALIGNED = ctypes.c_void_p(0x100008)
+
+
+def test_prepare_inputs_host_checks(lib):
+    L = lib.lib
+    d = _dims(lib)
+    args = [FAKE] * 11  # token_table .. scalars; the stream follows
+    assert L.rb_prepare_inputs(None, 1, 1, 1, 1, *args, None) == 1
+    assert L.rb_prepare_inputs(ctypes.byref(d), 9, 9, 9, 9, *args, None) == 2   # > max_num_reqs
+    assert L.rb_prepare_inputs(ctypes.byref(d), 2, 1, 2, 2, *args, None) == 1   # R_pad < R
+    assert L.rb_prepare_inputs(ctypes.byref(d), 1, 1, 3, 2, *args, None) == 1   # N_pad < N
+    assert L.rb_prepare_inputs(ctypes.byref(d), 1, 2, 1, 0, *args, None) == 1   # N_pad = 0
+    bad = _dims(lib, null_block=1000)
+    assert L.rb_prepare_inputs(ctypes.byref(bad), 1, 1, 1, 1, *args, None) == 1
+    nul = [FAKE] * 6 + [None] + [FAKE] * 4  # query_start_loc missing
+    assert L.rb_prepare_inputs(ctypes.byref(d), 1, 1, 1, 1, *nul, None) == 1
+
+
+def test_kv_write_host_checks(lib):
+    L = lib.lib
+    d = _dims(lib)
+    assert L.rb_kv_write(ctypes.byref(d), 4, None, FAKE, FAKE, FAKE, FAKE, None, None) == 1
+    assert L.rb_kv_write(ctypes.byref(d), 4, MISALIGNED, FAKE, FAKE, FAKE, FAKE, None, None) == 1
+    assert L.rb_kv_write(ctypes.byref(d), -1, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == 1
+    odd = _dims(lib, num_kv_heads=1, head_dim=3)
+    assert L.rb_kv_write(ctypes.byref(odd), 4, FAKE, FAKE, FAKE, FAKE, FAKE, None, None) == 5
+    assert L.rb_kv_write(ctypes.byref(d), 0, None, None, None, None, None, None, None) == 0
+
+
+def _attn(lib, d, R=2, N=4, Np=4, ws=FAKE, ws_bytes=1 << 30, q=FAKE):
+    return lib.lib.rb_paged_attention(ctypes.byref(d), R, N, Np, q, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                      ctypes.c_float(0.1), FAKE, ws, ws_bytes, None, None)
+
+
+def test_paged_attention_host_checks(lib):
+    assert _attn(lib, _dims(lib, block_size=8)) == 5
+    assert _attn(lib, _dims(lib, head_dim=96)) == 5
+    assert _attn(lib, _dims(lib, num_q_heads=30)) == 1
+    assert _attn(lib, _dims(lib, num_q_heads=64, num_kv_heads=2)) == 5       # group 32
+    assert _attn(lib, _dims(lib), R=9) == 2
+    assert _attn(lib, _dims(lib), N=5, Np=4) == 1
+    assert _attn(lib, _dims(lib), q=MISALIGNED) == 1
+    assert _attn(lib, _dims(lib), ws=ctypes.c_void_p(0x100010)) == 1          # not 256-aligned
+    assert _attn(lib, _dims(lib), ws_bytes=16) == 2
+    d = _dims(lib)
+    need = lib.lib.rb_paged_attention_workspace_size(ctypes.byref(d), 2, 4)
+    assert need > 0
+    assert _attn(lib, d, ws_bytes=need - 1) == 2
+    more = lib.lib.rb_paged_attention_workspace_size(ctypes.byref(d), 200, 4)
+    assert more > need
+    assert lib.lib.rb_paged_attention_workspace_size(None, 2, 4) == 0
+    assert lib.lib.rb_paged_attention_workspace_size(ctypes.byref(d), -1, 4) == 0
+
+
+def test_gather_rows_host_checks(lib):
+    L = lib.lib
+    assert L.rb_gather_rows(2, 4095, 8, FAKE, FAKE, FAKE, None, None) == 5
+    assert L.rb_gather_rows(2, 4096, 8, None, FAKE, FAKE, None, None) == 1
+    assert L.rb_gather_rows(2, 4096, 8, MISALIGNED, FAKE, FAKE, None, None) == 1
+    assert L.rb_gather_rows(0, 4096, 8, None, None, None, None, None) == 0
+    assert L.rb_gather_rows(-1, 4096, 8, FAKE, FAKE, FAKE, None, None) == 1
