@@ -11,10 +11,9 @@ from conftest import ROOT, load_golden
 
 @pytest.fixture(scope="module")
 def lib():
-    from ragged_mixed_paged_gb300 import build
+    import __graft_entry__
 
-    if not os.path.exists(build.LIB):
-        build.build()
+    __graft_entry__._build_module().build()
     import ragged_mixed_paged_gb300._binding as b
 
     return b
