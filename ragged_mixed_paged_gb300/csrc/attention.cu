@@ -96,7 +96,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(AttnArgs a, int
     const ReqInfo x = req_info(a, r);
     if (!x.ok || x.q == 0) continue;
     if (is_decode_class(x.q, a.group)) my_d += (x.pages + sp - 1) / sp * a.nkv;
-    else my_p += (x.q * a.group + kPrefillTileM - 1) / kPrefillTileM * a.nkv;
+    else my_p += (x.q * a.group + a.tile_m - 1) / a.tile_m * a.nkv;
   }
   int ex_d, ex_p, tot_d, tot_p;
   block_scan2(my_d, my_p, &ex_d, &ex_p, &tot_d, &tot_p);
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(AttnArgs a, int
     a.pre_off[r] = ex_p;
     if (!x.ok || x.q == 0) continue;
     if (is_decode_class(x.q, a.group)) ex_d += (x.pages + sp - 1) / sp * a.nkv;
-    else ex_p += (x.q * a.group + kPrefillTileM - 1) / kPrefillTileM * a.nkv;
+    else ex_p += (x.q * a.group + a.tile_m - 1) / a.tile_m * a.nkv;
   }
   if (tid == 0) {
     a.dec_off[a.R] = tot_d;
@@ -221,6 +221,13 @@ extern "C" rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, i
       !encode_kv_tensor_map(&vmap, d_v_cache, d.head_dim, d.num_kv_heads, num_slots))
     return RB_ERR_CUDA;
 
+  const int group = d.num_q_heads / d.num_kv_heads;
+  const bool use_tc = prefill_tc_supported(d.head_dim, group);
+  CUtensorMap qmap;
+  if (use_tc && num_tokens_padded > 0 &&
+      !encode_q_tensor_map(&qmap, d_q, d.head_dim, d.num_q_heads, num_tokens_padded, group))
+    return RB_ERR_CUDA;
+
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
   AttnArgs a{};
   a.q = static_cast<const __nv_bfloat16*>(d_q);
@@ -244,6 +251,7 @@ extern "C" rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, i
   a.null_block = d.null_block;
   const int sms = max(1, device_sm_count());
   a.target_units = min(kMaxTargetUnits, 32 * sms);
+  a.tile_m = use_tc ? 128 : kPrefillTileM;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.err = d_error_word;
 
@@ -254,7 +262,8 @@ extern "C" rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, i
   if (num_reqs == 0) return RB_OK;
   rb_status st = launch_decode(a, d.head_dim, kmap, vmap, s);
   if (st != RB_OK) return st;
-  st = launch_prefill(a, d.head_dim, kmap, vmap, s);
+  st = use_tc ? launch_prefill_tc(a, d.head_dim, qmap, kmap, vmap, s)
+              : launch_prefill(a, d.head_dim, kmap, vmap, s);
   if (st != RB_OK) return st;
   const dim3 cgrid(static_cast<unsigned>(num_reqs), static_cast<unsigned>(d.num_kv_heads));
   if (d.head_dim == 128)

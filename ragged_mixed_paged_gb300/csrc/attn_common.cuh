@@ -8,7 +8,7 @@ namespace rb {
 namespace attn {
 
 constexpr int kMaxCols = 8;          // decode columns: (query token, head of the group) pairs
-constexpr int kPrefillTileM = 64;    // query rows per prefill tile
+constexpr int kPrefillTileM = 64;    // query rows per mma.sync prefill tile
 constexpr int kMaxTargetUnits = 8192;
 constexpr int kMinSplitPages = 8;
 constexpr int kPage = 16;            // tokens per KV page (the only page size these kernels take)
@@ -59,6 +59,7 @@ struct AttnArgs {
   float* part_o;
   int R, N, N_pad, nh, nkv, group, MB, num_blocks, null_block;
   int target_units;
+  int tile_m;  // query rows per prefill unit (128 on the tcgen05 path, 64 on the mma.sync path)
   float scale_log2;
   int32_t* err;
 };
@@ -72,6 +73,9 @@ rb_status launch_decode(const AttnArgs& a, int head_dim, const CUtensorMap& kmap
                         const CUtensorMap& vmap, cudaStream_t s);
 rb_status launch_prefill(const AttnArgs& a, int head_dim, const CUtensorMap& kmap,
                          const CUtensorMap& vmap, cudaStream_t s);
+bool prefill_tc_supported(int head_dim, int group);
+rb_status launch_prefill_tc(const AttnArgs& a, int head_dim, const CUtensorMap& qmap,
+                            const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t s);
 
 }  // namespace attn
 }  // namespace rb

@@ -62,6 +62,24 @@ bool encode_kv_tensor_map(CUtensorMap* map, const void* base, int head_dim, int 
   return r == CUDA_SUCCESS;
 }
 
+bool encode_q_tensor_map(CUtensorMap* map, const void* base, int head_dim, int num_q_heads,
+                         long long num_tokens, int group) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (enc == nullptr || group < 1 || 128 % group != 0) return false;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim),
+                              static_cast<cuuint64_t>(num_q_heads),
+                              static_cast<cuuint64_t>(num_tokens)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(head_dim) * num_q_heads * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group),
+                             static_cast<cuuint32_t>(128 / group)};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                   strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace rb
 
 extern "C" {

@@ -43,9 +43,9 @@ def test_long_context_sampled(rb):
     _case(rb, spec, rows=sample_rows(spec, n_random=96, seed=5))
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", range(32))
 def test_fuzzed_mixes(rb, seed):
-    nh, nkv = [(4, 4), (4, 2), (8, 2), (16, 2), (32, 8), (16, 1)][seed % 6]
+    nh, nkv = [(4, 4), (4, 2), (8, 2), (16, 2), (32, 8), (16, 1), (6, 2), (12, 2)][seed % 8]
     hd = 64 if seed % 2 else 128
     spec = wl.random_batch(seed, num_q_heads=nh, num_kv_heads=nkv, head_dim=hd, max_reqs=7,
                            max_q=150, max_c=400, pad_tokens=seed % 4, decode_frac=0.5)
