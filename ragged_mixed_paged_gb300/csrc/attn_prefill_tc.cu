@@ -5,8 +5,9 @@
 // SM (persistent; units pulled from an atomic counter, the most expensive tile of each request
 // first), 6 warps with fixed roles:
 //   warp 4     TMA producer: fetches units into a 4-entry ring, loads the Q tile once per unit
-//              (3-D box {64 dims, group heads, 128/group tokens}) and each 128-key K/V tile
-//              (8 pages x 128-byte boxes, 128B swizzle) into a 2-stage ring;
+//              (3-D box {64 dims, group heads, 128/group tokens}) and each 128-key K and V
+//              tile (8 pages x 128-byte boxes, 128B swizzle, one page per lane) into separate
+//              3-stage rings, V one tile behind K (K is released as soon as S is done);
 //   warp 5     allocates 512 TMEM columns; one thread issues the MMAs:
 //              S_j = Q K_j^T  (M=128, N=128, K=hd; A, B K-major from shared memory) into one of
 //              two S buffers, then O += P_{j-1} V_{j-1}  (M=128, N=hd, K=128; A = P read from
@@ -35,13 +36,13 @@ struct TcCfg {
   static constexpr int kTileBytes = kHalves * kHalfBytes;
   static constexpr int kQHalfBytes = kM * 128;
   static constexpr int kQBytes = kHalves * kQHalfBytes;
-  static constexpr int kStages = 2;
-  static constexpr int kStageBytes = 2 * kTileBytes;      // K then V
-  static constexpr int kUsed = kStages * kStageBytes + kQBytes;
-  // slack after the buffers keeps every descriptor reading inside the allocation, and the
-  // total keeps one CTA per SM (each CTA holds all 512 TMEM columns)
-  static constexpr int kSmemBytes =
-      (kUsed + 32 * 1024 + 1024) > 120 * 1024 ? (kUsed + 32 * 1024 + 1024) : 120 * 1024;
+  static constexpr int kStagesK = 3;                      // K freed when S is done
+  static constexpr int kStagesV = 3;                      // V freed when P V is done
+  static constexpr int kVOffset = kStagesK * kTileBytes;
+  static constexpr int kQOffset = kVOffset + kStagesV * kTileBytes;
+  static constexpr int kUsed = kQOffset + kQBytes;
+  // at least 120 KB keeps one CTA per SM (each CTA holds all 512 TMEM columns)
+  static constexpr int kSmemBytes = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
   static constexpr int kThreads = 192;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColO = 256;                  // S0 at 0, S1 at 128, O at 256
@@ -55,7 +56,7 @@ struct TcUnit {
 struct TcShared {
   uint64_t unit_full[4], unit_empty[4];
   uint64_t q_full, q_empty;
-  uint64_t kv_full[2], kv_empty[2];
+  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
   uint64_t s_full[2], p_full[2];
   uint64_t o_done, o_free, drain;
   TcUnit units[4];
@@ -106,83 +107,126 @@ __device__ __forceinline__ TcUnit decode_unit(const AttnArgs& a, int u) {
 }
 
 template <int HD>
-__device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t k_base, uint32_t q_base,
+__device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
                          const CUtensorMap* qmap, const CUtensorMap* kmap,
                          const CUtensorMap* vmap) {
+  // The whole warp: page ids are held one per lane (a 32-page window, the next one prefetched)
+  // and lanes 0..7 each issue the boxes of one page of a tile.  V runs one tile behind K.
   using C = TcCfg<HD>;
   volatile int* abort = &sh.abort;
+  const int lane = threadIdx.x & 31;
   const int n_units = a.header[kHNumPrefillUnits];
-  uint32_t it = 0, q_armed = 0, kv_armed[2] = {0, 0};
+  uint32_t it = 0, q_armed = 0, k_armed[3] = {0, 0, 0}, v_armed[3] = {0, 0, 0};
+  auto lane0_wait = [&](uint64_t* bar, uint32_t phase) -> bool {
+    int ok = 1;
+    if (lane == 0) ok = tc_wait(bar, phase, abort, a.err) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
   for (int k = 0;; ++k) {
     const int slot = k % C::kRing;
-    if (!tc_wait(&sh.unit_empty[slot], ((k / C::kRing) & 1) ^ 1, abort, a.err)) break;
-    const int u = atomicAdd(a.header + kHPrefillNext, 1);
-    TcUnit un{};
-    if (u < n_units) un = decode_unit(a, u);
-    sh.units[slot] = un;
-    tc::mbar_arrive(&sh.unit_full[slot]);
+    if (!lane0_wait(&sh.unit_empty[slot], ((k / C::kRing) & 1) ^ 1)) break;
+    if (lane == 0) {
+      const int u = atomicAdd(a.header + kHPrefillNext, 1);
+      TcUnit un{};
+      if (u < n_units) un = decode_unit(a, u);
+      sh.units[slot] = un;
+      tc::mbar_arrive(&sh.unit_full[slot]);
+    }
+    __syncwarp();
+    const TcUnit un = sh.units[slot];
     if (!un.valid) break;
-    if (!tc_wait(&sh.q_empty, (k & 1) ^ 1, abort, a.err)) break;
-    mbar_arrive_expect_tx(&sh.q_full, C::kQBytes);
-    ++q_armed;
+    if (!lane0_wait(&sh.q_empty, (k & 1) ^ 1)) break;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&sh.q_full, C::kQBytes);
+      ++q_armed;
 #pragma unroll
-    for (int hf = 0; hf < C::kHalves; ++hf)
-      tma_load_3d(q_base + hf * C::kQHalfBytes, qmap, &sh.q_full, hf * 64, un.h * a.group,
-                  un.t0 + un.row0 / a.group);
+      for (int hf = 0; hf < C::kHalves; ++hf)
+        tma_load_3d(smem_base + C::kQOffset + hf * C::kQHalfBytes, qmap, &sh.q_full, hf * 64,
+                    un.h * a.group, un.t0 + un.row0 / a.group);
+    }
     const int32_t* bt_row = a.block_table + static_cast<size_t>(un.r) * a.MB;
+    int win = 0;
+    int bid = lane < un.pages ? __ldg(bt_row + lane) : a.null_block;
+    int bid_next = 32 + lane < un.pages ? __ldg(bt_row + 32 + lane) : a.null_block;
+    int ids[2] = {a.null_block, a.null_block};  // page id of this lane for tiles j and j-1
     bool ok = true;
-    for (int j = 0; j < un.n_kt; ++j, ++it) {
-      const int st = it % C::kStages;
-      if (!tc_wait(&sh.kv_empty[st], ((it / C::kStages) & 1) ^ 1, abort, a.err)) {
-        ok = false;
-        break;
-      }
-      mbar_arrive_expect_tx(&sh.kv_full[st], C::kStageBytes);
-      ++kv_armed[st];
-      const uint32_t kdst = k_base + st * C::kStageBytes, vdst = kdst + C::kTileBytes;
-#pragma unroll 1
-      for (int p = 0; p < C::kPagesPerTile; ++p) {
-        const int pg = j * C::kPagesPerTile + p;
-        int id = a.null_block;  // pages past the sequence: any valid page (masked, V zeroed)
-        if (pg < un.pages) {
-          id = __ldg(bt_row + pg);
-          if (id < 0 || id >= a.num_blocks || id == a.null_block) {
-            raise_error(a.err, RB_EBIT_BLOCK_ID);
-            id = a.null_block;
-          }
+    for (int j = 0; j <= un.n_kt; ++j) {
+      if (j < un.n_kt) {  // K of tile j
+        const int first = j * C::kPagesPerTile;
+        if (first - win >= 32) {
+          win += 32;
+          bid = bid_next;
+          bid_next = win + 32 + lane < un.pages ? __ldg(bt_row + win + 32 + lane) : a.null_block;
         }
+        int id = __shfl_sync(0xffffffffu, bid, first + (lane & 7) - win);
+        const int pg = first + (lane & 7);
+        if (pg >= un.pages) {
+          id = a.null_block;  // past the sequence: any valid page (masked, V zeroed)
+        } else if (id < 0 || id >= a.num_blocks || id == a.null_block) {
+          if (lane < C::kPagesPerTile) raise_error(a.err, RB_EBIT_BLOCK_ID);
+          id = a.null_block;
+        }
+        ids[j & 1] = id;
+        const uint32_t itk = it + j, st = itk % C::kStagesK;
+        if (!lane0_wait(&sh.k_empty[st], ((itk / C::kStagesK) & 1) ^ 1)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&sh.k_full[st], C::kTileBytes);
+          ++k_armed[st];
+        }
+        __syncwarp();
+        if (lane < C::kPagesPerTile) {
 #pragma unroll
-        for (int hf = 0; hf < C::kHalves; ++hf) {
-          const uint32_t off = hf * C::kHalfBytes + p * (kPage * 128);
-          tma_load_3d(kdst + off, kmap, &sh.kv_full[st], hf * 64, un.h, id * kPage);
-          tma_load_3d(vdst + off, vmap, &sh.kv_full[st], hf * 64, un.h, id * kPage);
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(smem_base + st * C::kTileBytes + hf * C::kHalfBytes + lane * (kPage * 128),
+                        kmap, &sh.k_full[st], hf * 64, un.h, id * kPage);
+        }
+      }
+      if (j >= 1) {  // V of tile j-1
+        const uint32_t itv = it + j - 1, st = itv % C::kStagesV;
+        if (!lane0_wait(&sh.v_empty[st], ((itv / C::kStagesV) & 1) ^ 1)) { ok = false; break; }
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&sh.v_full[st], C::kTileBytes);
+          ++v_armed[st];
+        }
+        __syncwarp();
+        if (lane < C::kPagesPerTile) {
+          const int id = ids[(j - 1) & 1];
+#pragma unroll
+          for (int hf = 0; hf < C::kHalves; ++hf)
+            tma_load_3d(smem_base + C::kVOffset + st * C::kTileBytes + hf * C::kHalfBytes +
+                            lane * (kPage * 128),
+                        vmap, &sh.v_full[st], hf * 64, un.h, id * kPage);
         }
       }
     }
     if (!ok) break;
+    it += un.n_kt;
   }
-  if (*abort) {  // let every copy already issued land before the CTA can exit
+  if (lane == 0 && *abort) {  // let every copy already issued land before the CTA can exit
     if (q_armed) mbar_wait_bounded(&sh.q_full, (q_armed - 1) & 1, 100000000ull);
-    for (int st = 0; st < 2; ++st)
-      if (kv_armed[st]) mbar_wait_bounded(&sh.kv_full[st], (kv_armed[st] - 1) & 1, 100000000ull);
+    for (int b = 0; b < 3; ++b) {
+      if (k_armed[b]) mbar_wait_bounded(&sh.k_full[b], (k_armed[b] - 1) & 1, 100000000ull);
+      if (v_armed[b]) mbar_wait_bounded(&sh.v_full[b], (v_armed[b] - 1) & 1, 100000000ull);
+    }
   }
 }
 
 template <int HD>
-__device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint32_t k_base,
-                           uint32_t q_base) {
+__device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint32_t smem_base) {
   using C = TcCfg<HD>;
   volatile int* abort = &sh.abort;
   constexpr uint32_t idesc_s = tc::make_idesc(128, 128, false);
   constexpr uint32_t idesc_o = tc::make_idesc(128, HD, true);
+  const uint32_t qs = smem_base + C::kQOffset;
   uint32_t it = 0;
   bool issued = false;
   auto issue_pv = [&](uint32_t itp, bool first_of_unit, int k) -> bool {
-    const uint32_t sb = itp & 1u, st = itp % C::kStages;
+    const uint32_t sb = itp & 1u, st = itp % C::kStagesV;
     if (!tc_wait(&sh.p_full[sb], (itp >> 1) & 1, abort, a.err)) return false;
+    if (!tc_wait(&sh.v_full[st], (itp / C::kStagesV) & 1, abort, a.err)) return false;
     if (first_of_unit && k > 0 && !tc_wait(&sh.o_free, (k - 1) & 1, abort, a.err)) return false;
     tc::fence_after_sync();
-    const uint32_t vb = k_base + st * C::kStageBytes + C::kTileBytes;
+    const uint32_t vb = smem_base + C::kVOffset + st * C::kTileBytes;
 #pragma unroll
     for (int kk = 0; kk < C::kN / 16; ++kk) {
       const uint64_t bdesc = tc::sdesc_sw128(vb + kk * (16 * 128), C::kHalfBytes, 1024);
@@ -190,7 +234,7 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
                  (first_of_unit && kk == 0) ? 0u : 1u);
     }
     tc::commit(&sh.o_done);
-    tc::commit(&sh.kv_empty[st]);
+    tc::commit(&sh.v_empty[st]);
     return true;
   };
   for (int k = 0;; ++k) {
@@ -202,20 +246,21 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
     tc::fence_after_sync();
     bool ok = true;
     for (int j = 0; j < un.n_kt && ok; ++j) {
-      const uint32_t itg = it + j, st = itg % C::kStages, sb = itg & 1u;
-      if (!tc_wait(&sh.kv_full[st], (itg / C::kStages) & 1, abort, a.err)) { ok = false; break; }
+      const uint32_t itg = it + j, st = itg % C::kStagesK, sb = itg & 1u;
+      if (!tc_wait(&sh.k_full[st], (itg / C::kStagesK) & 1, abort, a.err)) { ok = false; break; }
       tc::fence_after_sync();
-      const uint32_t kb = k_base + st * C::kStageBytes;
+      const uint32_t kb = smem_base + st * C::kTileBytes;
 #pragma unroll
       for (int ks = 0; ks < HD / 16; ++ks) {
         const uint32_t off = (ks >> 2) * C::kQHalfBytes + (ks & 3) * 32;
-        const uint64_t adesc = tc::sdesc_sw128(q_base + off, 16, 1024);
+        const uint64_t adesc = tc::sdesc_sw128(qs + off, 16, 1024);
         const uint64_t bdesc = tc::sdesc_sw128(kb + (ks >> 2) * C::kHalfBytes + (ks & 3) * 32,
                                                16, 1024);
         tc::mma_ss(tmem + sb * 128, adesc, bdesc, idesc_s, ks > 0 ? 1u : 0u);
       }
       issued = true;
       tc::commit(&sh.s_full[sb]);
+      tc::commit(&sh.k_empty[st]);
       if (j == un.n_kt - 1) tc::commit(&sh.q_empty);
       if (j > 0) ok = issue_pv(itg - 1, j == 1, k);
     }
@@ -231,8 +276,7 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
 }
 
 template <int HD>
-__device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint32_t k_base,
-                           uint8_t* k_ptr) {
+__device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8_t* smem_ptr) {
   using C = TcCfg<HD>;
   volatile int* abort = &sh.abort;
   const int t = threadIdx.x;  // 0..127: query row within the tile and TMEM lane
@@ -263,18 +307,23 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < un.n_kt; ++j) {
-      const uint32_t itg = it + j, sb = itg & 1u, st = itg % C::kStages;
+      const uint32_t itg = it + j, sb = itg & 1u, sv = itg % C::kStagesV;
       if (!wait_all(&sh.s_full[sb], (itg >> 1) & 1)) { ok = false; break; }
       tc::fence_after_sync();
       float s[128];
       {
-        uint32_t r[32];
+        uint32_t r0[32], r1[32], r2[32], r3[32];
+        tc::ld32(tmem + lane_off + sb * 128 + 0, r0);
+        tc::ld32(tmem + lane_off + sb * 128 + 32, r1);
+        tc::ld32(tmem + lane_off + sb * 128 + 64, r2);
+        tc::ld32(tmem + lane_off + sb * 128 + 96, r3);
+        tc::wait_ld();
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          tc::ld32(tmem + lane_off + sb * 128 + c * 32, r);
-          tc::wait_ld();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[c * 32 + i] = __uint_as_float(r[i]) * a.scale_log2;
+        for (int i = 0; i < 32; ++i) {
+          s[i] = __uint_as_float(r0[i]) * a.scale_log2;
+          s[32 + i] = __uint_as_float(r1[i]) * a.scale_log2;
+          s[64 + i] = __uint_as_float(r2[i]) * a.scale_log2;
+          s[96 + i] = __uint_as_float(r3[i]) * a.scale_log2;
         }
       }
       const int kv_base = j * C::kN;
@@ -282,9 +331,13 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = (kv_base + i <= lim) ? s[i] : -INFINITY;
       }
-      float m_tile = s[0];
+      float mx[8];
 #pragma unroll
-      for (int i = 1; i < 128; ++i) m_tile = fmaxf(m_tile, s[i]);
+      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+      const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
       const bool need = m_tile > m_ref + 8.f;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? m_tile : m_ref;
@@ -308,9 +361,10 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
       }
       // keys at or past the end of the sequence may hold anything: zero their V rows
       if (kv_base + C::kN > un.L) {
+        if (!wait_all(&sh.v_full[sv], (itg / C::kStagesV) & 1)) { ok = false; break; }
         const int kmin = max(un.L - kv_base, 0);
         if (t >= kmin) {
-          uint8_t* vrow = k_ptr + st * C::kStageBytes + C::kTileBytes + t * 128;
+          uint8_t* vrow = smem_ptr + C::kVOffset + sv * C::kTileBytes + t * 128;
 #pragma unroll
           for (int hf = 0; hf < C::kHalves; ++hf)
 #pragma unroll
@@ -321,7 +375,7 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
         }
       }
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      float rs = 0.f;
+      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
         uint32_t pk[32];
@@ -329,13 +383,13 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
         for (int i = 0; i < 32; ++i) {
           const float p0 = fast_exp2(s[c * 64 + 2 * i] - mu);
           const float p1 = fast_exp2(s[c * 64 + 2 * i + 1] - mu);
-          rs += p0 + p1;
+          rs[i & 7] += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
         tc::st32(tmem + lane_off + sb * 128 + c * 32, pk);
       }
       tc::wait_st();
-      l += rs;
+      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       // observe P_{j-1} V_{j-1} before P_j lets the next one start: o_done then never runs more
       // than one phase ahead of pv_seen, so its parity waits stay unambiguous
       if (!catch_up(itg)) { ok = false; break; }
@@ -384,7 +438,7 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-  const uint32_t q_base = base + C::kStages * C::kStageBytes;
+
   if (tid == 0) {
     for (int i = 0; i < C::kRing; ++i) {
       mbar_init(&sh.unit_full[i], 1);
@@ -392,9 +446,13 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
     }
     mbar_init(&sh.q_full, 1);
     mbar_init(&sh.q_empty, 1);
+    for (int i = 0; i < 3; ++i) {
+      mbar_init(&sh.k_full[i], 1);
+      mbar_init(&sh.k_empty[i], 1);
+      mbar_init(&sh.v_full[i], 1);
+      mbar_init(&sh.v_empty[i], 1);
+    }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sh.kv_full[i], 1);
-      mbar_init(&sh.kv_empty[i], 1);
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.p_full[i], 128);
     }
@@ -414,11 +472,11 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
   const uint32_t tmem = sh.tmem_base;
 
   if (warp == 4) {
-    if ((tid & 31) == 0) producer<HD>(a, sh, base, q_base, &qmap, &kmap, &vmap);
+    producer<HD>(a, sh, base, &qmap, &kmap, &vmap);
   } else if (warp == 5) {
-    if ((tid & 31) == 0) mma_issuer<HD>(a, sh, tmem, base, q_base);
+    if ((tid & 31) == 0) mma_issuer<HD>(a, sh, tmem, base);
   } else {
-    softmax_wg<HD>(a, sh, tmem, base, base_ptr);
+    softmax_wg<HD>(a, sh, tmem, base_ptr);
   }
 
   tc::fence_before_sync();
