@@ -171,7 +171,7 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- ranks
-def dist_setup():
+def dist_setup(backend=None):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws <= 1:
         return 0, 1, 0
@@ -179,7 +179,8 @@ def dist_setup():
     import torch.distributed as dist
 
     local = int(os.environ.get("LOCAL_RANK", "0"))
-    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if backend is None:
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
     if backend == "nccl":
         torch.cuda.set_device(local)
     dist.init_process_group(backend)
