@@ -185,6 +185,30 @@ rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, int32_t num_
                              size_t workspace_bytes, int32_t* d_error_word, void* stream);
 
 /*
+ * rb_paged_attention_static_ws — rb_paged_attention without a caller-provided workspace.
+ * The pages have no counterpart: this entry point exists for callers that cannot allocate
+ * device memory, such as code whose host framework owns every device byte (a raw cudaMalloc
+ * would escape its accounting) or a step loop where cudaMalloc/cudaFree would synchronise the
+ * device.  It allocates nothing.  Its scratch is a fixed 64 MiB array compiled into the library,
+ * held by every GPU that loads it until the process exits.
+ *
+ * Arguments, layouts, results and device error bits are those of rb_paged_attention.
+ * Errors: RB_ERR_CAPACITY when rb_paged_attention_workspace_size(dims, num_reqs, num_tokens)
+ * exceeds 64 MiB (at 8 kv heads and head_dim 128: more than 992 requests); RB_ERR_CUDA if the
+ * array's device address cannot be obtained.  The first call on a device looks that address
+ * up with the device current; make it before any stream capture.  All calls on a device share
+ * the array: calls whose work overlaps on the GPU (e.g. two streams at once) race on it, so
+ * serialise them.  Nothing in the array needs clearing between calls.
+ */
+rb_status rb_paged_attention_static_ws(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
+                                       int32_t num_tokens_padded, const void* d_q,
+                                       const void* d_k_cache, const void* d_v_cache,
+                                       const int32_t* d_block_table,
+                                       const int32_t* d_query_start_loc,
+                                       const int32_t* d_seq_lens, float softmax_scale,
+                                       void* d_out, int32_t* d_error_word, void* stream);
+
+/*
  * rb_gather_rows — out[i, :] = hidden[indices[i], :] for i < num_rows.
  * Source: "vLLM 源码完全拆解（五）…", "第四步：只在必要位置计算 logits"; "04 · 模型执行与
  * CUDA Graph", step ⑤ (hidden_states[logits_indices]).
