@@ -194,7 +194,7 @@ rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, int32_t num_
  *
  * Arguments, layouts, results and device error bits are those of rb_paged_attention.
  * Errors: RB_ERR_CAPACITY when rb_paged_attention_workspace_size(dims, num_reqs, num_tokens)
- * exceeds 64 MiB (at 8 kv heads and head_dim 128: more than 992 requests); RB_ERR_CUDA if the
+ * exceeds 64 MiB (at 8 kv heads and head_dim 128: more than 991 requests); RB_ERR_CUDA if the
  * array's device address cannot be obtained.  The first call on a device looks that address
  * up with the device current; make it before any stream capture.  All calls on a device share
  * the array: calls whose work overlaps on the GPU (e.g. two streams at once) race on it, so

@@ -6,14 +6,14 @@
 //     o = softmax(scale * q . K[0 .. c_i + j]) . V[0 .. c_i + j]
 // over the request's own pages only.
 //
-// One call enqueues four kernels on the caller's stream, with no host round trip (the host
+// One call enqueues three kernels on the caller's stream, with no host round trip (the host
 // only knows num_reqs and the token counts):
 //   1. plan     (1 CTA)  validates the metadata, classifies requests (decode-like when
 //                        query_len * group <= 8), sizes KV splits so the decode work fills the
 //                        GPU, writes per-request unit offsets, zeroes padding rows;
-//   2. decode   (persistent, split-KV, TMA-staged) one warp per (request, kv head, split);
-//   3. prefill  (persistent, tensor-core tiles) one CTA per (request, kv head, 64-row tile);
-//   4. combine  merges the split partials of decode requests with more than one split.
+//   2. decode   (persistent, split-KV, TMA-staged) one warp per (request, kv head, split); the
+//               last split of a (request, kv head) to finish merges the partials;
+//   3. prefill  (persistent, tensor-core tiles) one CTA per (request, kv head, row tile).
 #include "attn_common.cuh"
 
 namespace rb {
@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(AttnArgs a, int
     a.header[kHPrefillNext] = 0;
     a.header[kHSplitPages] = sp;
   }
+  for (int i = tid; i < a.R * a.nkv; i += kPlanThreads) a.done[i] = 0;
   // rows of padding tokens are written as zeros
   const long long row16 = static_cast<long long>(a.nh) * head_dim * 2 / 16;
   int4* out = reinterpret_cast<int4*>(a.out);
@@ -124,49 +125,6 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(AttnArgs a, int
   const long long last = static_cast<long long>(a.N_pad) * row16;
   for (long long i = first + tid; i < last; i += kPlanThreads) out[i] = make_int4(0, 0, 0, 0);
   if (bits) raise_error(a.err, bits);
-}
-
-// Merges the split partials (m, l, o) of one (decode request, kv head): one warp per column.
-template <int HD>
-__global__ void __launch_bounds__(256) attn_combine_kernel(AttnArgs a) {
-  const int r = blockIdx.x, h = blockIdx.y;
-  const int col = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int base = a.dec_off[r];
-  const int nsplit = (a.dec_off[r + 1] - base) / a.nkv;
-  if (nsplit <= 1) return;
-  const int t0 = a.qsl[r];
-  const int cols = (a.qsl[r + 1] - t0) * a.group;
-  if (col >= cols) return;
-  constexpr int kPer = HD / 32;
-  float mx = -INFINITY;
-  for (int s = 0; s < nsplit; ++s)
-    mx = fmaxf(mx, a.part_ml[static_cast<size_t>(base + s * a.nkv + h) * kMaxCols + col].x);
-  if (mx == -INFINITY) mx = 0.f;
-  float acc[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
-  float lsum = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
-    const size_t u = static_cast<size_t>(base + s * a.nkv + h);
-    const float2 ml = a.part_ml[u * kMaxCols + col];
-    const float w = fast_exp2(ml.x - mx);
-    lsum += w * ml.y;
-    const float* o = a.part_o + (u * kMaxCols + col) * HD + lane * kPer;
-    if constexpr (kPer == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(o);
-      acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(o);
-      acc[0] += w * v.x; acc[1] += w * v.y;
-    }
-  }
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-  const int j = col / a.group, hh = col - j * a.group;
-  __nv_bfloat16* dst =
-      a.out + (static_cast<size_t>(t0 + j) * a.nh + h * a.group + hh) * HD + lane * kPer;
-  uint32_t* d32 = reinterpret_cast<uint32_t*>(dst);
-#pragma unroll
-  for (int k = 0; k < kPer; k += 2) d32[k / 2] = pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
 }
 
 }  // namespace
@@ -238,6 +196,7 @@ extern "C" rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, i
   a.header = reinterpret_cast<int32_t*>(ws + w.header);
   a.dec_off = reinterpret_cast<int32_t*>(ws + w.dec_off);
   a.pre_off = reinterpret_cast<int32_t*>(ws + w.pre_off);
+  a.done = reinterpret_cast<int32_t*>(ws + w.done);
   a.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
   a.part_o = reinterpret_cast<float*>(ws + w.part_o);
   a.R = num_reqs;
@@ -262,15 +221,6 @@ extern "C" rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, i
   if (num_reqs == 0) return RB_OK;
   rb_status st = launch_decode(a, d.head_dim, kmap, vmap, s);
   if (st != RB_OK) return st;
-  st = use_tc ? launch_prefill_tc(a, d.head_dim, qmap, kmap, vmap, s)
-              : launch_prefill(a, d.head_dim, kmap, vmap, s);
-  if (st != RB_OK) return st;
-  const dim3 cgrid(static_cast<unsigned>(num_reqs), static_cast<unsigned>(d.num_kv_heads));
-  if (d.head_dim == 128)
-    attn_combine_kernel<128><<<cgrid, 256, 0, s>>>(a);
-  else
-    attn_combine_kernel<64><<<cgrid, 256, 0, s>>>(a);
-  if (last_launch_status() != RB_OK) return RB_ERR_CUDA;
-  note_launches(1);
-  return RB_OK;
+  return use_tc ? launch_prefill_tc(a, d.head_dim, qmap, kmap, vmap, s)
+                : launch_prefill(a, d.head_dim, kmap, vmap, s);
 }

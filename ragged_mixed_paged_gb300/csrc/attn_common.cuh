@@ -22,9 +22,10 @@ enum HeaderField : int {
   kHeaderInts = 32
 };
 
-// Workspace: [header][decode unit offsets R+1][prefill unit offsets R+1][partial (m, l)][partial o]
+// Workspace: [header][decode unit offsets R+1][prefill unit offsets R+1]
+//            [finished-split counters R x nkv][partial (m, l)][partial o]
 struct WsLayout {
-  size_t header, dec_off, pre_off, part_ml, part_o, total;
+  size_t header, dec_off, pre_off, done, part_ml, part_o, total;
   long long max_units;
 };
 
@@ -40,6 +41,7 @@ inline WsLayout ws_layout(int head_dim, int num_kv_heads, int num_reqs) {
   w.header = take(kHeaderInts * sizeof(int32_t));
   w.dec_off = take(static_cast<size_t>(num_reqs + 1) * sizeof(int32_t));
   w.pre_off = take(static_cast<size_t>(num_reqs + 1) * sizeof(int32_t));
+  w.done = take(static_cast<size_t>(num_reqs) * num_kv_heads * sizeof(int32_t));
   w.part_ml = take(static_cast<size_t>(w.max_units) * kMaxCols * sizeof(float2));
   w.part_o = take(static_cast<size_t>(w.max_units) * kMaxCols * head_dim * sizeof(float));
   w.total = off;
@@ -55,6 +57,7 @@ struct AttnArgs {
   int32_t* header;
   int32_t* dec_off;
   int32_t* pre_off;
+  int32_t* done;  // per (request, kv head): decode splits finished so far
   float2* part_ml;
   float* part_o;
   int R, N, N_pad, nh, nkv, group, MB, num_blocks, null_block;

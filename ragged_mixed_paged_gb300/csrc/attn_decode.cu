@@ -11,8 +11,9 @@
 // with mma.sync m16n8k16 (bf16 in, fp32 accumulate).  P^T's fragments come from S^T's with a
 // register transpose (movmatrix), so each page costs 2 x hd/16 MMAs and every K/V byte is read
 // once per kv head, shared by the whole query-head group.  Softmax statistics are per column,
-// reduced with warp shuffles; a unit with several splits leaves (m, l, o) partials for the
-// combine kernel, a single-split unit writes the normalised bf16 output directly.
+// reduced with warp shuffles; a unit with several splits leaves (m, l, o) partials and the last
+// split of its (request, kv head) to finish merges them; a single-split unit writes the
+// normalised bf16 output directly.
 #include "attn_common.cuh"
 
 namespace rb {
@@ -30,6 +31,50 @@ struct DecCfg {
   static constexpr int kSmemBytes = kWarps * kStages * kStageBytes + 1024;
   static constexpr int kKS = HD / 16;
 };
+
+// Log-sum-exp merge of the split partials of one (request, kv head) by one warp: lanes over
+// splits for the maxima, lanes over head_dim for the weighted sum.  Partials written by other
+// SMs are read through L2 (ld.global.cg).
+template <int HD>
+__device__ void combine_splits(const AttnArgs& a, int h, int first, int nsplit, int t0,
+                               int cols) {
+  const int lane = threadIdx.x & 31;
+  constexpr int kPer = HD / 32;
+  for (int col = 0; col < cols; ++col) {
+    float mx = -INFINITY;
+    for (int sp = lane; sp < nsplit; sp += 32)
+      mx = fmaxf(mx, __ldcg(&a.part_ml[static_cast<size_t>(first + sp * a.nkv + h) * kMaxCols +
+                                       col].x));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (mx == -INFINITY) mx = 0.f;
+    float acc[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) acc[k] = 0.f;
+    float lsum = 0.f;
+#pragma unroll 4
+    for (int sp = 0; sp < nsplit; ++sp) {
+      const size_t u = static_cast<size_t>(first + sp * a.nkv + h);
+      const float2 ml = __ldcg(a.part_ml + u * kMaxCols + col);
+      const float w = fast_exp2(ml.x - mx);
+      lsum += w * ml.y;
+      const float* o = a.part_o + (u * kMaxCols + col) * HD + lane * kPer;
+      if constexpr (kPer == 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(o));
+        acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+      } else {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(o));
+        acc[0] += w * v.x; acc[1] += w * v.y;
+      }
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const int j = col / a.group, hh = col - j * a.group;
+    uint32_t* d32 = reinterpret_cast<uint32_t*>(
+        a.out + (static_cast<size_t>(t0 + j) * a.nh + h * a.group + hh) * HD + lane * kPer);
+#pragma unroll
+    for (int k = 0; k < kPer; k += 2) d32[k / 2] = pack_bf16x2(acc[k] * inv, acc[k + 1] * inv);
+  }
+}
 
 template <int HD>
 __global__ void __launch_bounds__(DecCfg<HD>::kWarps * 32)
@@ -253,6 +298,16 @@ __global__ void __launch_bounds__(DecCfg<HD>::kWarps * 32)
       if (lane < 4) {
         a.part_ml[static_cast<size_t>(u) * kMaxCols + c0] = make_float2(m0, l0);
         a.part_ml[static_cast<size_t>(u) * kMaxCols + c1] = make_float2(m1, l1);
+      }
+      // the last split of this (request, kv head) to finish merges all partials
+      __threadfence();
+      __syncwarp();
+      int prev = 0;
+      if (lane == 0) prev = atomicAdd(a.done + r * a.nkv + h, 1);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev == nsplit - 1) {
+        __threadfence();
+        combine_splits<HD>(a, h, first, nsplit, t0, cols);
       }
     }
   }
