@@ -210,7 +210,7 @@ extern "C" rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, i
   a.null_block = d.null_block;
   const int sms = max(1, device_sm_count());
   a.target_units = min(kMaxTargetUnits, 32 * sms);
-  a.tile_m = use_tc ? 128 : kPrefillTileM;
+  a.tile_m = use_tc ? 256 : kPrefillTileM;  // tcgen05 units are pairs of 128-row tiles
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.err = d_error_word;
 

@@ -62,7 +62,7 @@ struct AttnArgs {
   float* part_o;
   int R, N, N_pad, nh, nkv, group, MB, num_blocks, null_block;
   int target_units;
-  int tile_m;  // query rows per prefill unit (128 on the tcgen05 path, 64 on the mma.sync path)
+  int tile_m;  // query rows per prefill unit (256 on the tcgen05 path, 64 on the mma.sync path)
   float scale_log2;
   int32_t* err;
 };

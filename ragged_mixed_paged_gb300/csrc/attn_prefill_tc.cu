@@ -1,22 +1,23 @@
-// Prefill / chunk attention tiles on the 5th-generation tensor cores (tcgen05 + TMEM).
+// Prefill / chunk attention on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
-// Work unit = (request, kv head, tile of 128 query rows); rows are (query token, head of the
-// group) pairs, token-major, so every K/V tile serves the whole query-head group.  One CTA per
-// SM (persistent; units pulled from an atomic counter, the most expensive tile of each request
-// first), 6 warps with fixed roles:
-//   warp 4     TMA producer: fetches units into a 4-entry ring, loads the Q tile once per unit
-//              (3-D box {64 dims, group heads, 128/group tokens}) and each 128-key K and V
-//              tile (8 pages x 128-byte boxes, 128B swizzle, one page per lane) into separate
-//              3-stage rings, V one tile behind K (K is released as soon as S is done);
-//   warp 5     allocates 512 TMEM columns; one thread issues the MMAs:
-//              S_j = Q K_j^T  (M=128, N=128, K=hd; A, B K-major from shared memory) into one of
-//              two S buffers, then O += P_{j-1} V_{j-1}  (M=128, N=hd, K=128; A = P read from
-//              TMEM, B = V MN-major from shared memory), so S_{j+1} runs while P_j is made;
-//   warps 0-3  softmax, thread t = query row t: reads its S row from TMEM, masks causally,
-//              keeps a running max and sum in the log2 domain, writes P (bf16) back over the
-//              S columns, and rescales the O row in TMEM only when the max grows by more than
-//              2^8 (exact either way: P and the sum share the same reference).  The epilogue
-//              reads O, divides by the sum and stores bf16 rows.
+// Work unit = (request, kv head, pair of 128-row query tiles A and B); rows are (query token,
+// head of the group) pairs, token-major, so every K/V tile serves the whole query-head group
+// and both tiles of the pair.  One CTA per SM (persistent; units pulled from an atomic
+// counter, the most expensive pair of each request first), 12 warps with fixed roles:
+//   warp 8     TMA producer: fetches units into a 4-entry ring, loads Q_A and Q_B once per unit
+//              (3-D boxes {64 dims, group heads, 128/group tokens}) and each 128-key K and V
+//              tile (8 pages x 128-byte boxes, 128B swizzle, one page per lane) into a 3-stage
+//              K ring and a 2-stage V ring, V one tile behind K (K is freed once S is done);
+//   warp 9     allocates all 512 TMEM columns (S_A, S_B, O_A, O_B); one thread issues the MMAs
+//              in the order S_A(0) S_B(0) | PV_A(0) S_A(1) | PV_B(0) S_B(1) | PV_A(1) ...
+//              S = Q K^T: M=128, N=128, K=hd, both operands K-major in shared memory;
+//              O += P V:  M=128, N=hd,  K=128, P read from TMEM, V MN-major in shared memory;
+//              so one tile's softmax runs while the tensor core works on the other tile;
+//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B; thread t = query row t: reads its
+//              S row from TMEM, masks causally, keeps a running max and sum in the log2
+//              domain, writes P (bf16) back over the S columns, and rescales its O row in TMEM
+//              only when the max grows by more than 2^8 (exact either way: P and the sum share
+//              the same reference).  The epilogue reads O, divides by the sum, stores bf16 rows.
 // All mbarrier waits are bounded; a timeout sets RB_EBIT_TIMEOUT, every role stops, in-flight
 // copies and MMAs are drained with bounded waits and TMEM is freed before the CTA exits.
 #include "attn_common.cuh"
@@ -28,37 +29,50 @@ namespace {
 
 template <int HD>
 struct TcCfg {
-  static constexpr int kM = 128;                          // query rows per tile
+  static constexpr int kM = 128;                          // query rows per tile (2 per unit)
   static constexpr int kN = 128;                          // keys per K/V tile
   static constexpr int kPagesPerTile = kN / kPage;        // 8
   static constexpr int kHalves = HD / 64;                 // 128-byte swizzle atoms per row
   static constexpr int kHalfBytes = kN * 128;             // one 64-dim half of a K or V tile
   static constexpr int kTileBytes = kHalves * kHalfBytes;
   static constexpr int kQHalfBytes = kM * 128;
-  static constexpr int kQBytes = kHalves * kQHalfBytes;
-  static constexpr int kStagesK = 3;                      // K freed when S is done
-  static constexpr int kStagesV = 3;                      // V freed when P V is done
+  static constexpr int kQBytes = kHalves * kQHalfBytes;   // one Q tile
+  static constexpr int kStagesK = 3;
+  static constexpr int kStagesV = 2;
   static constexpr int kVOffset = kStagesK * kTileBytes;
-  static constexpr int kQOffset = kVOffset + kStagesV * kTileBytes;
-  static constexpr int kUsed = kQOffset + kQBytes;
+  static constexpr int kQOffset = kVOffset + kStagesV * kTileBytes;  // Q_A then Q_B
+  static constexpr int kUsed = kQOffset + 2 * kQBytes;
   // at least 120 KB keeps one CTA per SM (each CTA holds all 512 TMEM columns)
   static constexpr int kSmemBytes = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
-  static constexpr int kThreads = 192;
+  // 3 warpgroups launched at 168 registers per thread (the 64-bit-register pool of one SM for
+  // 384 threads); the softmax warpgroups then take 216 and the producer/MMA warpgroup keeps 72:
+  // 2 x 128 x 216 + 128 x 72 = 384 x 168.
+  static constexpr int kThreads = 384;
+  static constexpr int kLaunchRegs = 168;
+  static constexpr int kSoftmaxRegs = 216;
+  static constexpr int kControlRegs = 72;
+  static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
+                "register split exceeds the launch allocation");
+  static constexpr int kProducerWarp = 8;
+  static constexpr int kMmaWarp = 9;  // warps 10 and 11 only complete the third warpgroup
   static constexpr uint32_t kTmemCols = 512;
-  static constexpr uint32_t kColO = 256;                  // S0 at 0, S1 at 128, O at 256
+  static constexpr uint32_t kColS0 = 0;                   // S_A at 0, S_B at 128
+  static constexpr uint32_t kColO0 = 256;                 // O_A at 256, O_B at 256 + HD
   static constexpr int kRing = 4;
+  __device__ static constexpr uint32_t col_s(int x) { return kColS0 + 128u * x; }
+  __device__ static constexpr uint32_t col_o(int x) { return kColO0 + static_cast<uint32_t>(HD) * x; }
 };
 
 struct TcUnit {
-  int r, h, row0, t0, q, L, c, rows_total, n_kt, pages, valid;
+  int r, h, row0, t0, q, L, c, rows_total, n[2], n_kt, pages, valid;
 };
 
 struct TcShared {
   uint64_t unit_full[4], unit_empty[4];
   uint64_t q_full, q_empty;
-  uint64_t k_full[3], k_empty[3], v_full[3], v_empty[3];
-  uint64_t s_full[2], p_full[2];
-  uint64_t o_done, o_free, drain;
+  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
+  uint64_t drain;
   TcUnit units[4];
   uint32_t tmem_base;
   int abort;
@@ -84,23 +98,28 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t phase, volatile 
   }
 }
 
+__device__ __forceinline__ int tiles_for(int c, int jmax) { return (c + jmax + 1 + 127) / 128; }
+
 __device__ __forceinline__ TcUnit decode_unit(const AttnArgs& a, int u) {
   TcUnit un{};
   const int r = upper_bound_i32(a.pre_off, a.R + 1, u) - 1;
   const int first = a.pre_off[r];
-  const int tiles_r = (a.pre_off[r + 1] - first) / a.nkv;
+  const int pairs_r = (a.pre_off[r + 1] - first) / a.nkv;
   const int local = u - first;
   un.r = r;
   un.h = local % a.nkv;
-  const int tile = tiles_r - 1 - local / a.nkv;
+  const int pair = pairs_r - 1 - local / a.nkv;
   un.t0 = a.qsl[r];
   un.q = a.qsl[r + 1] - un.t0;
   un.L = a.seq_lens[r];
   un.c = un.L - un.q;
   un.rows_total = un.q * a.group;
-  un.row0 = tile * 128;
-  const int jmax = (min(un.row0 + 128, un.rows_total) - 1) / a.group;
-  un.n_kt = (un.c + jmax + 1 + 127) / 128;
+  un.row0 = pair * 256;
+  un.n[0] = tiles_for(un.c, (min(un.row0 + 128, un.rows_total) - 1) / a.group);
+  un.n[1] = un.row0 + 128 < un.rows_total
+                ? tiles_for(un.c, (min(un.row0 + 256, un.rows_total) - 1) / a.group)
+                : 0;
+  un.n_kt = max(un.n[0], un.n[1]);
   un.pages = (un.L + kPage - 1) / kPage;
   un.valid = 1;
   return un;
@@ -116,7 +135,7 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
   volatile int* abort = &sh.abort;
   const int lane = threadIdx.x & 31;
   const int n_units = a.header[kHNumPrefillUnits];
-  uint32_t it = 0, q_armed = 0, k_armed[3] = {0, 0, 0}, v_armed[3] = {0, 0, 0};
+  uint32_t it = 0, q_armed = 0, k_armed[3] = {0, 0, 0}, v_armed[2] = {0, 0};
   auto lane0_wait = [&](uint64_t* bar, uint32_t phase) -> bool {
     int ok = 1;
     if (lane == 0) ok = tc_wait(bar, phase, abort, a.err) ? 1 : 0;
@@ -137,12 +156,14 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
     if (!un.valid) break;
     if (!lane0_wait(&sh.q_empty, (k & 1) ^ 1)) break;
     if (lane == 0) {
-      mbar_arrive_expect_tx(&sh.q_full, C::kQBytes);
+      const int nq = un.n[1] > 0 ? 2 : 1;
+      mbar_arrive_expect_tx(&sh.q_full, nq * C::kQBytes);
       ++q_armed;
+      for (int x = 0; x < nq; ++x)
 #pragma unroll
-      for (int hf = 0; hf < C::kHalves; ++hf)
-        tma_load_3d(smem_base + C::kQOffset + hf * C::kQHalfBytes, qmap, &sh.q_full, hf * 64,
-                    un.h * a.group, un.t0 + un.row0 / a.group);
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem_base + C::kQOffset + x * C::kQBytes + hf * C::kQHalfBytes, qmap,
+                      &sh.q_full, hf * 64, un.h * a.group, un.t0 + (un.row0 + 128 * x) / a.group);
     }
     const int32_t* bt_row = a.block_table + static_cast<size_t>(un.r) * a.MB;
     int win = 0;
@@ -204,10 +225,10 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
   }
   if (lane == 0 && *abort) {  // let every copy already issued land before the CTA can exit
     if (q_armed) mbar_wait_bounded(&sh.q_full, (q_armed - 1) & 1, 100000000ull);
-    for (int b = 0; b < 3; ++b) {
+    for (int b = 0; b < 3; ++b)
       if (k_armed[b]) mbar_wait_bounded(&sh.k_full[b], (k_armed[b] - 1) & 1, 100000000ull);
+    for (int b = 0; b < 2; ++b)
       if (v_armed[b]) mbar_wait_bounded(&sh.v_full[b], (v_armed[b] - 1) & 1, 100000000ull);
-    }
   }
 }
 
@@ -217,57 +238,85 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
   volatile int* abort = &sh.abort;
   constexpr uint32_t idesc_s = tc::make_idesc(128, 128, false);
   constexpr uint32_t idesc_o = tc::make_idesc(128, HD, true);
-  const uint32_t qs = smem_base + C::kQOffset;
-  uint32_t it = 0;
+  uint32_t itk = 0;                       // K/V tiles consumed
+  uint32_t tcount[2] = {0, 0};            // S (= P V) tiles per side
+  uint32_t ucount[2] = {0, 0};            // units per side that used O
   bool issued = false;
-  auto issue_pv = [&](uint32_t itp, bool first_of_unit, int k) -> bool {
-    const uint32_t sb = itp & 1u, st = itp % C::kStagesV;
-    if (!tc_wait(&sh.p_full[sb], (itp >> 1) & 1, abort, a.err)) return false;
-    if (!tc_wait(&sh.v_full[st], (itp / C::kStagesV) & 1, abort, a.err)) return false;
-    if (first_of_unit && k > 0 && !tc_wait(&sh.o_free, (k - 1) & 1, abort, a.err)) return false;
-    tc::fence_after_sync();
-    const uint32_t vb = smem_base + C::kVOffset + st * C::kTileBytes;
+  auto wait = [&](uint64_t* bar, uint32_t phase) { return tc_wait(bar, phase, abort, a.err); };
+  auto issue_s = [&](int x, uint32_t kt) {  // S_x = Q_x K^T into S_x
+    const uint32_t kb = smem_base + (kt % C::kStagesK) * C::kTileBytes;
+    const uint32_t qs = smem_base + C::kQOffset + x * C::kQBytes;
+#pragma unroll
+    for (int ks = 0; ks < HD / 16; ++ks) {
+      const uint64_t adesc =
+          tc::sdesc_sw128(qs + (ks >> 2) * C::kQHalfBytes + (ks & 3) * 32, 16, 1024);
+      const uint64_t bdesc =
+          tc::sdesc_sw128(kb + (ks >> 2) * C::kHalfBytes + (ks & 3) * 32, 16, 1024);
+      tc::mma_ss(tmem + C::col_s(x), adesc, bdesc, idesc_s, ks > 0 ? 1u : 0u);
+    }
+    tc::commit(&sh.s_full[x]);
+    issued = true;
+  };
+  auto issue_pv = [&](int x, uint32_t kt, bool first) {  // O_x (+)= P_x V
+    const uint32_t vb = smem_base + C::kVOffset + (kt % C::kStagesV) * C::kTileBytes;
 #pragma unroll
     for (int kk = 0; kk < C::kN / 16; ++kk) {
       const uint64_t bdesc = tc::sdesc_sw128(vb + kk * (16 * 128), C::kHalfBytes, 1024);
-      tc::mma_ts(tmem + C::kColO, tmem + sb * 128 + kk * 8, bdesc, idesc_o,
-                 (first_of_unit && kk == 0) ? 0u : 1u);
+      tc::mma_ts(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, bdesc, idesc_o,
+                 (first && kk == 0) ? 0u : 1u);
     }
-    tc::commit(&sh.o_done);
-    tc::commit(&sh.v_empty[st]);
-    return true;
+    tc::commit(&sh.o_done[x]);
   };
   for (int k = 0;; ++k) {
     const int slot = k % C::kRing;
-    if (!tc_wait(&sh.unit_full[slot], (k / C::kRing) & 1, abort, a.err)) break;
+    if (!wait(&sh.unit_full[slot], (k / C::kRing) & 1)) break;
     const TcUnit un = sh.units[slot];
     if (!un.valid) break;
-    if (!tc_wait(&sh.q_full, k & 1, abort, a.err)) break;
+    if (!wait(&sh.q_full, k & 1)) break;
+    if (!wait(&sh.k_full[itk % C::kStagesK], (itk / C::kStagesK) & 1)) break;
     tc::fence_after_sync();
+    issue_s(0, itk);
+    if (un.n[1] > 0) issue_s(1, itk);
+    tc::commit(&sh.k_empty[itk % C::kStagesK]);
+    if (un.n_kt == 1) tc::commit(&sh.q_empty);
     bool ok = true;
     for (int j = 0; j < un.n_kt && ok; ++j) {
-      const uint32_t itg = it + j, st = itg % C::kStagesK, sb = itg & 1u;
-      if (!tc_wait(&sh.k_full[st], (itg / C::kStagesK) & 1, abort, a.err)) { ok = false; break; }
-      tc::fence_after_sync();
-      const uint32_t kb = smem_base + st * C::kTileBytes;
-#pragma unroll
-      for (int ks = 0; ks < HD / 16; ++ks) {
-        const uint32_t off = (ks >> 2) * C::kQHalfBytes + (ks & 3) * 32;
-        const uint64_t adesc = tc::sdesc_sw128(qs + off, 16, 1024);
-        const uint64_t bdesc = tc::sdesc_sw128(kb + (ks >> 2) * C::kHalfBytes + (ks & 3) * 32,
-                                               16, 1024);
-        tc::mma_ss(tmem + sb * 128, adesc, bdesc, idesc_s, ks > 0 ? 1u : 0u);
+      const uint32_t kt = itk + j;
+      bool k_ready = false;
+      for (int x = 0; x < 2; ++x) {
+        if (j >= un.n[x]) continue;
+        if (!wait(&sh.p_full[x], (tcount[x] + j) & 1) ||
+            !wait(&sh.v_full[kt % C::kStagesV], (kt / C::kStagesV) & 1) ||
+            (j == 0 && ucount[x] > 0 && !wait(&sh.o_free[x], (ucount[x] - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc::fence_after_sync();
+        issue_pv(x, kt, j == 0);
+        if (j + 1 < un.n[x]) {
+          if (!k_ready) {
+            if (!wait(&sh.k_full[(kt + 1) % C::kStagesK], ((kt + 1) / C::kStagesK) & 1)) {
+              ok = false;
+              break;
+            }
+            tc::fence_after_sync();
+            k_ready = true;
+          }
+          issue_s(x, kt + 1);
+        }
       }
-      issued = true;
-      tc::commit(&sh.s_full[sb]);
-      tc::commit(&sh.k_empty[st]);
-      if (j == un.n_kt - 1) tc::commit(&sh.q_empty);
-      if (j > 0) ok = issue_pv(itg - 1, j == 1, k);
+      if (!ok) break;
+      tc::commit(&sh.v_empty[kt % C::kStagesV]);                        // P V of tile j issued
+      if (j + 1 < un.n_kt) tc::commit(&sh.k_empty[(kt + 1) % C::kStagesK]);  // S of tile j+1
+      if (j + 2 == un.n_kt) tc::commit(&sh.q_empty);                      // unit's last S issued
     }
-    if (ok) ok = issue_pv(it + un.n_kt - 1, un.n_kt == 1, k);
     if (!ok) break;
     tc::mbar_arrive(&sh.unit_empty[slot]);
-    it += un.n_kt;
+    for (int x = 0; x < 2; ++x) {
+      tcount[x] += un.n[x];
+      if (un.n[x] > 0) ++ucount[x];
+    }
+    itk += un.n_kt;
   }
   if (issued) {  // every MMA and every commit-arrival lands before TMEM and smem are released
     tc::commit(&sh.drain);
@@ -275,20 +324,23 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
   }
 }
 
+// Softmax and epilogue of tile x (0 = A, 1 = B); thread t = row t of the tile = TMEM lane t.
 template <int HD>
-__device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8_t* smem_ptr) {
+__device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8_t* smem_ptr,
+                           int x) {
   using C = TcCfg<HD>;
   volatile int* abort = &sh.abort;
-  const int t = threadIdx.x;  // 0..127: query row within the tile and TMEM lane
+  const int t = threadIdx.x & 127;
   const uint32_t lane_off = static_cast<uint32_t>((t >> 5) * 32) << 16;
-  uint32_t it = 0, pv_seen = 0;
+  const uint32_t col_s = tmem + lane_off + C::col_s(x), col_o = tmem + lane_off + C::col_o(x);
+  uint32_t tc_x = 0, pv_seen = 0, itk = 0;
   auto wait_all = [&](uint64_t* bar, uint32_t phase) -> bool {
     const bool ok = tc_wait(bar, phase, abort, a.err);
     return !__any_sync(0xffffffffu, !ok);
   };
   auto catch_up = [&](uint32_t target) -> bool {  // consume o_done phases up to `target`
     while (pv_seen < target) {
-      if (!wait_all(&sh.o_done, pv_seen & 1)) return false;
+      if (!wait_all(&sh.o_done[x], pv_seen & 1)) return false;
       ++pv_seen;
     }
     return true;
@@ -298,32 +350,34 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
     if (!wait_all(&sh.unit_full[slot], (k / C::kRing) & 1)) break;
     const TcUnit un = sh.units[slot];
     if (!un.valid) break;
-    const int row = un.row0 + t;
+    const int n = un.n[x];
+    const int row0 = un.row0 + 128 * x;
+    const int row = row0 + t;
     const bool valid = row < un.rows_total;
     const int jt = valid ? row / a.group : 0;
     const int hh = valid ? row - jt * a.group : 0;
     const int lim = un.c + jt;
-    const int lim_min = un.c + un.row0 / a.group;
+    const int lim_min = un.c + row0 / a.group;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int j = 0; j < un.n_kt; ++j) {
-      const uint32_t itg = it + j, sb = itg & 1u, sv = itg % C::kStagesV;
-      if (!wait_all(&sh.s_full[sb], (itg >> 1) & 1)) { ok = false; break; }
+    for (int j = 0; j < n; ++j) {
+      const uint32_t tj = tc_x + j;
+      if (!wait_all(&sh.s_full[x], tj & 1)) { ok = false; break; }
       tc::fence_after_sync();
       float s[128];
       {
         uint32_t r0[32], r1[32], r2[32], r3[32];
-        tc::ld32(tmem + lane_off + sb * 128 + 0, r0);
-        tc::ld32(tmem + lane_off + sb * 128 + 32, r1);
-        tc::ld32(tmem + lane_off + sb * 128 + 64, r2);
-        tc::ld32(tmem + lane_off + sb * 128 + 96, r3);
+        tc::ld32(col_s + 0, r0);
+        tc::ld32(col_s + 32, r1);
+        tc::ld32(col_s + 64, r2);
+        tc::ld32(col_s + 96, r3);
         tc::wait_ld();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          s[i] = __uint_as_float(r0[i]) * a.scale_log2;
-          s[32 + i] = __uint_as_float(r1[i]) * a.scale_log2;
-          s[64 + i] = __uint_as_float(r2[i]) * a.scale_log2;
-          s[96 + i] = __uint_as_float(r3[i]) * a.scale_log2;
+          s[i] = __uint_as_float(r0[i]);
+          s[32 + i] = __uint_as_float(r1[i]);
+          s[64 + i] = __uint_as_float(r2[i]);
+          s[96 + i] = __uint_as_float(r3[i]);
         }
       }
       const int kv_base = j * C::kN;
@@ -336,32 +390,36 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
       for (int i = 0; i < 8; ++i) mx[i] = s[i];
 #pragma unroll
       for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+      // scores are scaled inside the exponent: max and mask commute with a positive scale
       const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+                           a.scale_log2;
       const bool need = m_tile > m_ref + 8.f;
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? m_tile : m_ref;
         const float alpha = fast_exp2(m_ref - m_new);
         if (j > 0) {
-          if (!catch_up(itg)) { ok = false; break; }  // O must hold P_{j-1} V_{j-1}
+          if (!catch_up(tj)) { ok = false; break; }  // O must hold P_{j-1} V_{j-1}
           tc::fence_after_sync();
           uint32_t r[32];
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
-            tc::ld32(tmem + lane_off + C::kColO + c * 32, r);
+            tc::ld32(col_o + c * 32, r);
             tc::wait_ld();
 #pragma unroll
             for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tc::st32(tmem + lane_off + C::kColO + c * 32, r);
+            tc::st32(col_o + c * 32, r);
           }
           tc::wait_st();
         }
         l *= alpha;
         m_ref = m_new;
       }
-      // keys at or past the end of the sequence may hold anything: zero their V rows
-      if (kv_base + C::kN > un.L) {
-        if (!wait_all(&sh.v_full[sv], (itg / C::kStagesV) & 1)) { ok = false; break; }
+      // keys at or past the end of the sequence may hold anything: zero their V rows (only the
+      // unit's last K/V tile can reach them; tile A zeroes it when it uses that tile)
+      if (kv_base + C::kN > un.L && (x == 0 || j >= un.n[0])) {
+        const uint32_t kt = itk + j, sv = kt % C::kStagesV;
+        if (!wait_all(&sh.v_full[sv], (kt / C::kStagesV) & 1)) { ok = false; break; }
         const int kmin = max(un.L - kv_base, 0);
         if (t >= kmin) {
           uint8_t* vrow = smem_ptr + C::kVOffset + sv * C::kTileBytes + t * 128;
@@ -375,53 +433,57 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
         }
       }
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+      const float sc = a.scale_log2;
       float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        uint32_t pk[32];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float p0 = fast_exp2(s[c * 64 + 2 * i] - mu);
-          const float p1 = fast_exp2(s[c * 64 + 2 * i + 1] - mu);
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = fast_exp2(fmaf(s[c * 32 + 2 * i], sc, -mu));
+          const float p1 = fast_exp2(fmaf(s[c * 32 + 2 * i + 1], sc, -mu));
           rs[i & 7] += p0 + p1;
           pk[i] = pack_bf16x2(p0, p1);
         }
-        tc::st32(tmem + lane_off + sb * 128 + c * 32, pk);
+        tc::st16(col_s + c * 16, pk);
       }
       tc::wait_st();
       l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       // observe P_{j-1} V_{j-1} before P_j lets the next one start: o_done then never runs more
       // than one phase ahead of pv_seen, so its parity waits stay unambiguous
-      if (!catch_up(itg)) { ok = false; break; }
+      if (!catch_up(tj)) { ok = false; break; }
       tc::fence_before_sync();
-      tc::mbar_arrive(&sh.p_full[sb]);
+      tc::mbar_arrive(&sh.p_full[x]);
     }
     if (!ok) break;
-    it += un.n_kt;
-    if (!catch_up(it)) break;  // every P V of this unit has landed in O
-    tc::fence_after_sync();
-    const float inv = l > 0.f ? 1.f / l : 0.f;
-    uint4* dst = reinterpret_cast<uint4*>(
-        a.out + (static_cast<size_t>(un.t0 + jt) * a.nh + un.h * a.group + hh) * HD);
+    itk += un.n_kt;
+    if (n > 0) {
+      tc_x += n;
+      if (!catch_up(tc_x)) break;  // every P V of this unit has landed in O
+      tc::fence_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(
+          a.out + (static_cast<size_t>(un.t0 + jt) * a.nh + un.h * a.group + hh) * HD);
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
-      uint32_t r[32];
-      tc::ld32(tmem + lane_off + C::kColO + c * 32, r);
-      tc::wait_ld();
-      if (valid) {
+      for (int c = 0; c < HD / 32; ++c) {
+        uint32_t r[32];
+        tc::ld32(col_o + c * 32, r);
+        tc::wait_ld();
+        if (valid) {
 #pragma unroll
-        for (int v = 0; v < 4; ++v) {
-          uint4 w;
-          w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
-          w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
-          w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
-          w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
-          dst[c * 4 + v] = w;
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
+            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
+            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
+            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
+            dst[c * 4 + v] = w;
+          }
         }
       }
+      tc::fence_before_sync();
+      tc::mbar_arrive(&sh.o_free[x]);
     }
-    tc::fence_before_sync();
-    tc::mbar_arrive(&sh.o_free);
     tc::mbar_arrive(&sh.unit_empty[slot]);
   }
 }
@@ -438,31 +500,30 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
-
   if (tid == 0) {
     for (int i = 0; i < C::kRing; ++i) {
       mbar_init(&sh.unit_full[i], 1);
-      mbar_init(&sh.unit_empty[i], 1 + 128);
+      mbar_init(&sh.unit_empty[i], 1 + 256);
     }
     mbar_init(&sh.q_full, 1);
     mbar_init(&sh.q_empty, 1);
     for (int i = 0; i < 3; ++i) {
       mbar_init(&sh.k_full[i], 1);
       mbar_init(&sh.k_empty[i], 1);
-      mbar_init(&sh.v_full[i], 1);
-      mbar_init(&sh.v_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh.v_full[i], 1);
+      mbar_init(&sh.v_empty[i], 1);
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.p_full[i], 128);
+      mbar_init(&sh.o_done[i], 1);
+      mbar_init(&sh.o_free[i], 128);
     }
-    mbar_init(&sh.o_done, 1);
-    mbar_init(&sh.o_free, 128);
     mbar_init(&sh.drain, 1);
     sh.abort = 0;
     fence_barrier_init();
   }
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     tc::tmem_alloc(&sh.tmem_base, C::kTmemCols);
     tc::tmem_relinquish();
   }
@@ -471,18 +532,22 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = sh.tmem_base;
 
-  if (warp == 4) {
-    producer<HD>(a, sh, base, &qmap, &kmap, &vmap);
-  } else if (warp == 5) {
-    if ((tid & 31) == 0) mma_issuer<HD>(a, sh, tmem, base);
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kControlRegs));
+    if (warp == C::kProducerWarp) {
+      producer<HD>(a, sh, base, &qmap, &kmap, &vmap);
+    } else if (warp == C::kMmaWarp) {
+      if ((tid & 31) == 0) mma_issuer<HD>(a, sh, tmem, base);
+    }
   } else {
-    softmax_wg<HD>(a, sh, tmem, base_ptr);
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kSoftmaxRegs));
+    softmax_wg<HD>(a, sh, tmem, base_ptr, warp >> 2);
   }
 
   tc::fence_before_sync();
   __syncthreads();
   tc::fence_after_sync();
-  if (warp == 5) {
+  if (warp == C::kMmaWarp) {
     __syncwarp();
     tc::tmem_dealloc(tmem, C::kTmemCols);
   }
