@@ -34,8 +34,9 @@ METRIC = "mixed-step tokens/s; decode-attn HBM GB/s & prefill TFLOPS vs peak"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# dram bytes (read + write) per attention call measured by ncu for the attention kernels as
-# they stand, keyed by the hash of their sources; null once the sources change.
+# DRAM bytes (read + write) per launch measured by ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum), keyed by (kernel, workload, hash of the kernel's sources): a figure is
+# reported only while the kernel's sources are the ones it was measured on (profiles/).
 KNOWN_TRAFFIC = {}
 
 
@@ -105,13 +106,21 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def attention_sources_hash():
+KERNEL_SOURCES = {
+    "fused": ("attn_prefill_tc.cu", "attn_decode_warp.cuh", "tc_ptx.cuh", "attn_common.cuh",
+              "rb_internal.cuh"),
+    "prefill": ("attn_prefill.cu", "attn_common.cuh", "rb_internal.cuh"),
+    "decode": ("attn_decode.cu", "attn_decode_warp.cuh", "attn_common.cuh", "rb_internal.cuh"),
+}
+
+
+def kernel_sources_hash(kind):
+    """Hash of the sources a kernel is built from (traffic figures are valid for one hash)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ragged_mixed_paged_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.startswith("attn") or f in ("attention.cu", "rb_internal.cuh"):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode() + fh.read())
+    for f in KERNEL_SOURCES[kind]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
 
 
@@ -323,7 +332,25 @@ def run_ours(args, rank, world, local):
     if int(buf.meta["scalars"][3].item()) != 0:
         raise SystemExit(f"device error word {int(buf.meta['scalars'][3].item()):#x}")
 
-    marks = [[E() for _ in range(5)] for _ in range(args.steps)]
+    # events recorded inside the step: 5 around the four calls, 3 inside the attention call
+    EX = lambda: torch.cuda.Event(enable_timing=True, external=True)
+    marks, attn_marks = [EX() for _ in range(5)], [EX() for _ in range(3)]
+    for ev in marks + attn_marks:
+        ev.record()  # torch creates the handle lazily; the library re-records it in the step
+    torch.cuda.synchronize()
+    graph = None
+    launches_per_step = None
+    if not args.eager:
+        # the step has only scalar host inputs and fixed-address buffers: capture it once and
+        # replay it, as a serving loop would, so host launch latency does not enter the step
+        launches0 = rb.launch_count()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            rb.run_step(buf, marks=marks, attn_marks=attn_marks)
+        launches_per_step = rb.launch_count() - launches0
+        graph.replay()
+        torch.cuda.synchronize()
+    samples = []  # per step: the 8 event timestamps
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
@@ -332,20 +359,37 @@ def run_ours(args, rank, world, local):
     w0 = time.perf_counter()
     for k in range(args.steps):
         flush.zero_()
-        rb.run_step(buf, marks=marks[k])
+        if graph is not None:
+            graph.replay()
+        else:
+            rb.run_step(buf, marks=marks, attn_marks=attn_marks)
+        torch.cuda.synchronize()
+        pts = [marks[0], marks[1], marks[2], attn_marks[0], attn_marks[1], attn_marks[2],
+               marks[3], marks[4]]
+        samples.append([pts[0].elapsed_time(p) for p in pts])
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - w0
-    launches = rb.launch_count() - launches0
+    launches = (launches_per_step * args.steps if graph is not None
+                else rb.launch_count() - launches0)
     clocks = sampler.stop()
 
+    # timestamps: 0 start | 1 after prepare | 2 after kv_write | 3 after plan | 4 after decode |
+    # 5 after prefill | 6 after attention | 7 after gather
     def span(a, b):
-        return [m[a].elapsed_time(m[b]) for m in marks]
+        idx = {0: 0, 1: 1, 2: 2, 3: 6, 4: 7}
+        return [s[idx[b]] - s[idx[a]] for s in samples]
+
+    def kspan(a, b):  # inside the attention call: planner | decode kernel | prefill kernel
+        return [s[2 + b] - s[2 + a] for s in samples]
 
     step_ms = statistics.mean(span(0, 4))
     parts = {"prepare_inputs": span(0, 1), "kv_write": span(1, 2),
              "paged_attention": span(2, 3), "gather_rows": span(3, 4)}
     parts_ms = {k: statistics.mean(v) for k, v in parts.items()}
+    kernels_ms = {"attn_plan": statistics.mean(kspan(0, 1)),
+                  "attn_decode": statistics.mean(kspan(1, 2)),
+                  "attn_prefill": statistics.mean(kspan(2, 3))}
     step_ms_max = reduce_over_ranks(step_ms, "max", world, dev)
     total_tokens = reduce_over_ranks(float(spec.num_tokens), "sum", world, dev)
     value = total_tokens / (step_ms_max / 1000.0)
@@ -353,22 +397,44 @@ def run_ours(args, rank, world, local):
     w = work_counts(spec)
     pk, pk_kind = peaks()
     attn_s = parts_ms["paged_attention"] / 1000.0
-    # the attention call dominates the step; whether it is tensor- or HBM-bound depends on the mix
-    t_tensor = w["attn_flops"] / (pk["bf16_tflops"] * 1e12)
+    dec_s = kernels_ms["attn_decode"] / 1000.0
+    pre_s = kernels_ms["attn_prefill"] / 1000.0
+    # decode and prefill units share one launch (timed as the prefill span) when the head group
+    # is a power of two and head_dim is 64 or 128 (the tcgen05 path)
+    fused = (d.num_q_heads // d.num_kv_heads) in (1, 2, 4, 8, 16) and d.head_dim in (64, 128)
+    t_tensor = w["prefill_flops"] / (pk["bf16_tflops"] * 1e12)
     t_hbm = w["decode_bytes"] / (pk["hbm_gbs"] * 1e9)
-    src_hash = attention_sources_hash()
-    traffic = KNOWN_TRAFFIC.get((args.config, src_hash))
-    if t_tensor >= t_hbm:
-        achieved = w["attn_flops"] / attn_s / 1e12
+    if fused:
+        kernels_ms = {"attn_plan": kernels_ms["attn_plan"],
+                      "attn_fused": kernels_ms["attn_prefill"]}
+        tensor_bound = t_tensor >= t_hbm
+        achieved = (w["prefill_flops"] / pre_s / 1e12 if tensor_bound
+                    else w["decode_bytes"] / pre_s / 1e9)
+        peak = pk["bf16_tflops"] if tensor_bound else pk["hbm_gbs"]
+        roof = {"bound": "tensor" if tensor_bound else "hbm", "achieved": achieved,
+                "peak": peak, "unit": "TFLOP/s" if tensor_bound else "GB/s",
+                "frac": achieved / peak,
+                "traffic": KNOWN_TRAFFIC.get(("fused", args.config, kernel_sources_hash("fused"))),
+                "kernel": "attn_fused (split-KV decode + tcgen05 prefill units, one launch)",
+                "launch_ms": pre_s * 1000.0,
+                "overlap_frac": max(t_tensor, t_hbm) / pre_s,
+                "tensor_frac": w["prefill_flops"] / pre_s / 1e12 / pk["bf16_tflops"],
+                "hbm_frac": w["decode_bytes"] / pre_s / 1e9 / pk["hbm_gbs"],
+                "peak_kind": f"{'bf16 dense burst' if tensor_bound else 'HBM copy'}, {pk_kind}"}
+    # otherwise the dominant kernel: the one with the larger measured share of the step
+    elif pre_s >= dec_s:
+        achieved = w["prefill_flops"] / pre_s / 1e12
         roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"], "traffic": traffic,
-                "kernel": "rb_paged_attention (plan + decode + prefill + combine launches)",
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
+                "traffic": KNOWN_TRAFFIC.get(("prefill", args.config, kernel_sources_hash("prefill"))),
+                "kernel": "attn_prefill (tcgen05 tiles)", "launch_ms": kernels_ms["attn_prefill"],
                 "peak_kind": f"bf16 dense burst, {pk_kind}"}
     else:
-        achieved = w["decode_bytes"] / attn_s / 1e9
+        achieved = w["decode_bytes"] / dec_s / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"], "traffic": traffic,
-                "kernel": "rb_paged_attention (plan + decode + prefill + combine launches)",
+                "frac": achieved / pk["hbm_gbs"],
+                "traffic": KNOWN_TRAFFIC.get(("decode", args.config, kernel_sources_hash("decode"))),
+                "kernel": "attn_decode (split-KV)", "launch_ms": kernels_ms["attn_decode"],
                 "peak_kind": f"HBM copy, {pk_kind}"}
 
     e2e = measure_e2e(spec, tens, buf, dev, args, flush, world)
@@ -377,13 +443,16 @@ def run_ours(args, rank, world, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded N(0,1) bf16 Q/K/V/hidden, random page ids; no weights)",
             "config": workload_name(spec, args.config), "roofline": roof,
-            "components_ms": parts_ms,
-            "work": {"attention_tflop": w["attn_flops"] / 1e12,
+            "components_ms": parts_ms, "attention_kernels_ms": kernels_ms,
+            "work": {"prefill_tflop": w["prefill_flops"] / 1e12,
                      "decode_kv_gb": w["decode_bytes"] / 1e9,
-                     "attention_tflops": w["attn_flops"] / attn_s / 1e12,
-                     "decode_part_gbs_if_alone": w["decode_bytes"] / attn_s / 1e9},
-            "gpu_launches": launches, "wall_s": wall, "clocks": clocks, "e2e": e2e,
-            "attention_source_hash": src_hash}
+                     "attention_call_tflops": w["attn_flops"] / attn_s / 1e12,
+                     "prefill_tflops_over_kernel": w["prefill_flops"] / pre_s / 1e12 if pre_s else None,
+                     "decode_gbs_over_kernel": (w["decode_bytes"] / (pre_s if fused else dec_s) / 1e9
+                                                if (pre_s if fused else dec_s) else None)},
+            "gpu_launches": launches, "launch": "eager" if args.eager else "cuda_graph_replay",
+            "wall_s": wall, "clocks": clocks, "e2e": e2e,
+            "kernel_source_hashes": {k: kernel_sources_hash(k) for k in KERNEL_SOURCES}}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(spec)
     if rank == 0:
@@ -450,6 +519,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch every step from Python instead of replaying a captured graph")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -185,6 +185,26 @@ rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, int32_t num_
                              size_t workspace_bytes, int32_t* d_error_word, void* stream);
 
 /*
+ * rb_paged_attention_profiled — rb_paged_attention that also records caller-created CUDA events
+ * (cudaEvent_t passed as void*) on `stream` between its launches, for per-kernel timing:
+ * events[0] after the planner, events[1] after the decode kernel, events[2] after the prefill
+ * kernel; only the first num_events (<= 3) are used and NULL entries are skipped.  While
+ * `stream` is being captured into a CUDA graph the records are made as external event nodes, so
+ * they are recorded on every replay.  Same
+ * arguments, results and errors as rb_paged_attention otherwise; RB_ERR_INVALID_ARG if
+ * num_events < 0 or events is NULL with num_events > 0.
+ */
+rb_status rb_paged_attention_profiled(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
+                                      int32_t num_tokens_padded, const void* d_q,
+                                      const void* d_k_cache, const void* d_v_cache,
+                                      const int32_t* d_block_table,
+                                      const int32_t* d_query_start_loc,
+                                      const int32_t* d_seq_lens, float softmax_scale, void* d_out,
+                                      void* d_workspace, size_t workspace_bytes,
+                                      int32_t* d_error_word, void* stream, void* const* events,
+                                      int32_t num_events);
+
+/*
  * rb_paged_attention_static_ws — rb_paged_attention without a caller-provided workspace.
  * The pages have no counterpart: this entry point exists for callers that cannot allocate
  * device memory, such as code whose host framework owns every device byte (a raw cudaMalloc

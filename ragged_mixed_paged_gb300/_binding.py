@@ -47,7 +47,7 @@ class rb_dims(ctypes.Structure):
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
-            f"{LIB_PATH} is missing: build it with `python -m ragged_mixed_paged_gb300.build` "
+            f"{LIB_PATH} is missing: build it with `python ragged_mixed_paged_gb300/build.py` "
             "(there is no CPU fallback)")
     lib = ctypes.CDLL(LIB_PATH)
     P = ctypes.c_void_p
@@ -62,6 +62,9 @@ def _load():
         "rb_paged_attention_workspace_size": (ctypes.c_size_t, [PD, I32, I32]),
         "rb_paged_attention": (I32, [PD, I32, I32, I32, P, P, P, P, P, P, ctypes.c_float, P, P,
                                      ctypes.c_size_t, P, P]),
+        "rb_paged_attention_profiled": (I32, [PD, I32, I32, I32, P, P, P, P, P, P,
+                                              ctypes.c_float, P, P, ctypes.c_size_t, P, P,
+                                              ctypes.POINTER(ctypes.c_void_p), I32]),
         "rb_gather_rows": (I32, [I32, I32, I32, P, P, P, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -190,7 +193,10 @@ def kv_write(dims: Dims, k, v, slot_mapping, k_cache, v_cache, error_word=None,
 
 def paged_attention(dims: Dims, num_reqs: int, num_tokens: int, q, k_cache, v_cache,
                     block_table, query_start_loc, seq_lens, out=None, workspace=None,
-                    softmax_scale: Optional[float] = None, error_word=None, stream=None):
+                    softmax_scale: Optional[float] = None, error_word=None, stream=None,
+                    events=None):
+    """``events``: optional up to three recorded-once torch.cuda.Event objects that the library
+    re-records after its planner, decode and prefill launches (per-kernel timing)."""
     import torch
 
     bf = torch.bfloat16
@@ -201,15 +207,22 @@ def paged_attention(dims: Dims, num_reqs: int, num_tokens: int, q, k_cache, v_ca
                                 device=q.device)
     scale = 1.0 / math.sqrt(dims.head_dim) if softmax_scale is None else softmax_scale
     d = dims.c()
-    st = lib.rb_paged_attention(
-        ctypes.byref(d), num_reqs, num_tokens, q.shape[0], _ptr(q, bf, "q"),
-        _ptr(k_cache, bf, "k_cache"), _ptr(v_cache, bf, "v_cache"),
-        _ptr(block_table, torch.int32, "block_table"),
-        _ptr(query_start_loc, torch.int32, "query_start_loc"),
-        _ptr(seq_lens, torch.int32, "seq_lens"), ctypes.c_float(scale), _ptr(out, bf, "out"),
-        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
-        _ptr(error_word, torch.int32, "error_word"), _stream(stream))
-    _check("rb_paged_attention", st)
+    args = (ctypes.byref(d), num_reqs, num_tokens, q.shape[0], _ptr(q, bf, "q"),
+            _ptr(k_cache, bf, "k_cache"), _ptr(v_cache, bf, "v_cache"),
+            _ptr(block_table, torch.int32, "block_table"),
+            _ptr(query_start_loc, torch.int32, "query_start_loc"),
+            _ptr(seq_lens, torch.int32, "seq_lens"), ctypes.c_float(scale), _ptr(out, bf, "out"),
+            _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+            _ptr(error_word, torch.int32, "error_word"), _stream(stream))
+    if events is None:
+        _check("rb_paged_attention", lib.rb_paged_attention(*args))
+    else:
+        handles = [e.cuda_event for e in events]
+        if not all(handles):
+            raise ValueError("record each event once before passing it (torch creates them lazily)")
+        arr = (ctypes.c_void_p * len(handles))(*handles)
+        _check("rb_paged_attention_profiled",
+               lib.rb_paged_attention_profiled(*args, arr, len(handles)))
     return out
 
 

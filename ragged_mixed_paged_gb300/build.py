@@ -1,6 +1,7 @@
 """Builds librb.so in-tree for sm_103a (nvcc only; translation units compiled in parallel).
 
-Usage: ``python -m ragged_mixed_paged_gb300.build`` or ``build()`` from Python.
+Usage: ``python ragged_mixed_paged_gb300/build.py`` (run it as a script: importing the
+package first would load the library it is about to rebuild) or ``__graft_entry__.build()``.
 """
 from __future__ import annotations
 

@@ -6,14 +6,16 @@
 //     o = softmax(scale * q . K[0 .. c_i + j]) . V[0 .. c_i + j]
 // over the request's own pages only.
 //
-// One call enqueues three kernels on the caller's stream, with no host round trip (the host
+// One call enqueues its kernels on the caller's stream, with no host round trip (the host
 // only knows num_reqs and the token counts):
 //   1. plan     (1 CTA)  validates the metadata, classifies requests (decode-like when
-//                        query_len * group <= 8), sizes KV splits so the decode work fills the
-//                        GPU, writes per-request unit offsets, zeroes padding rows;
-//   2. decode   (persistent, split-KV, TMA-staged) one warp per (request, kv head, split); the
-//               last split of a (request, kv head) to finish merges the partials;
-//   3. prefill  (persistent, tensor-core tiles) one CTA per (request, kv head, row tile).
+//                        query_len * group <= 8), splits the CTAs between decode and prefill
+//                        work, sizes KV splits, writes per-request unit offsets, zeroes padding;
+//   2. one persistent launch (head groups that are powers of two): every CTA runs decode units
+//      (split-KV, one warp per (request, kv head, split); the last split of a (request, kv head)
+//      merges the partials) and prefill units (tcgen05 tiles), starting with the kind the
+//      planner assigned it and then helping with the other, so HBM-bound and tensor-bound work
+//      overlap; other groups run a decode launch and an mma.sync prefill launch instead.
 #include "attn_common.cuh"
 
 namespace rb {
@@ -71,26 +73,52 @@ __device__ __forceinline__ ReqInfo req_info(const AttnArgs& a, int r) {
 
 __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(AttnArgs a, int head_dim) {
   __shared__ unsigned long long s_pages;
+  __shared__ float s_flops;
   const int tid = threadIdx.x;
   const int per = (a.R + kPlanThreads - 1) / kPlanThreads;
   const int lo = min(tid * per, a.R), hi = min(lo + per, a.R);
   int bits = 0;
   if (tid == 0) {
     s_pages = 0;
+    s_flops = 0.f;
     if (a.qsl[0] != 0 || a.qsl[a.R] != a.N) bits |= RB_EBIT_ATTN_META;
   }
   __syncthreads();
   unsigned long long my_pages = 0;
+  float my_flops = 0.f;  // prefill work: 4 * nh * hd * visible keys
   for (int r = lo; r < hi; ++r) {
     const ReqInfo x = req_info(a, r);
     if (!x.ok) { bits |= RB_EBIT_ATTN_META; continue; }
-    if (is_decode_class(x.q, a.group)) my_pages += static_cast<unsigned long long>(x.pages);
+    if (is_decode_class(x.q, a.group)) {
+      my_pages += static_cast<unsigned long long>(x.pages);
+    } else {
+      const float c = static_cast<float>(x.L - x.q), q = static_cast<float>(x.q);
+      my_flops += 4.f * a.nh * head_dim * (q * c + 0.5f * q * (q + 1.f));
+    }
   }
   if (my_pages) atomicAdd(&s_pages, my_pages);
+  if (my_flops > 0.f) atomicAdd(&s_flops, my_flops);
   __syncthreads();
   const long long page_heads = static_cast<long long>(s_pages) * a.nkv;
+  // Fused launch: split the CTAs between decode (HBM-bound) and prefill (tensor-bound) so both
+  // finish together; CTAs that run out of their own work then help with the other kind.
+  // Rates per SM: ~80 GB/s of paged K/V for decode, ~7 TFLOP/s for prefill tiles.  Splits are
+  // sized for every CTA of the launch (all of them may end up helping with decode), so the
+  // decode tail stays short.
+  int decode_ctas = 0;
+  int target = a.target_units;
+  if (a.fused_ctas > 0) {
+    const float dec_bytes = static_cast<float>(page_heads) * (2.f * kPage * head_dim * 2.f);
+    const float t_dec = dec_bytes / 80e3f;   // microseconds on one SM
+    const float t_pre = s_flops / 7e6f;
+    if (t_dec > 0.f) {
+      const float share = t_pre > 0.f ? t_dec / (t_dec + t_pre) : 1.f;
+      decode_ctas = max(1, min(a.fused_ctas, static_cast<int>(share * a.fused_ctas + 0.5f)));
+    }
+    target = min(kMaxTargetUnits, 4 * a.decode_warps_per_cta * a.fused_ctas);
+  }
   const int sp = static_cast<int>(max(static_cast<long long>(kMinSplitPages),
-                                      (page_heads + a.target_units - 1) / a.target_units));
+                                      (page_heads + target - 1) / target));
   int my_d = 0, my_p = 0;
   for (int r = lo; r < hi; ++r) {
     const ReqInfo x = req_info(a, r);
@@ -116,6 +144,8 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(AttnArgs a, int
     a.header[kHDecodeNext] = 0;
     a.header[kHPrefillNext] = 0;
     a.header[kHSplitPages] = sp;
+    a.header[kHDecodeCtas] = decode_ctas;
+    a.header[kHRoleNext] = 0;
   }
   for (int i = tid; i < a.R * a.nkv; i += kPlanThreads) a.done[i] = 0;
   // rows of padding tokens are written as zeros
@@ -139,14 +169,15 @@ extern "C" size_t rb_paged_attention_workspace_size(const rb_dims* dims, int32_t
   return rb::attn::ws_layout(dims->head_dim, dims->num_kv_heads, max_num_reqs).total;
 }
 
-extern "C" rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
-                                        int32_t num_tokens_padded, const void* d_q,
-                                        const void* d_k_cache, const void* d_v_cache,
-                                        const int32_t* d_block_table,
-                                        const int32_t* d_query_start_loc,
-                                        const int32_t* d_seq_lens, float softmax_scale,
-                                        void* d_out, void* d_workspace, size_t workspace_bytes,
-                                        int32_t* d_error_word, void* stream) {
+namespace {
+
+rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
+                               int32_t num_tokens_padded, const void* d_q, const void* d_k_cache,
+                               const void* d_v_cache, const int32_t* d_block_table,
+                               const int32_t* d_query_start_loc, const int32_t* d_seq_lens,
+                               float softmax_scale, void* d_out, void* d_workspace,
+                               size_t workspace_bytes, int32_t* d_error_word, void* stream,
+                               void* const* events, int32_t num_events) {
   using namespace rb;
   using namespace rb::attn;
   if (dims == nullptr) return RB_ERR_INVALID_ARG;
@@ -211,16 +242,67 @@ extern "C" rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, i
   const int sms = max(1, device_sm_count());
   a.target_units = min(kMaxTargetUnits, 32 * sms);
   a.tile_m = use_tc ? 256 : kPrefillTileM;  // tcgen05 units are pairs of 128-row tiles
+  a.fused_ctas = use_tc ? sms : 0;
+  a.decode_warps_per_cta = 8;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.err = d_error_word;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
+  if (num_events > 0 && cudaStreamIsCapturing(s, &capturing) != cudaSuccess) return RB_ERR_CUDA;
+  auto mark = [&](int i) -> bool {  // inside a stream capture the records become graph nodes
+    return i >= num_events || events[i] == nullptr ||
+           cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), s,
+                                    capturing == cudaStreamCaptureStatusActive
+                                        ? cudaEventRecordExternal
+                                        : cudaEventRecordDefault) == cudaSuccess;
+  };
   attn_plan_kernel<<<1, kPlanThreads, 0, s>>>(a, d.head_dim);
   if (last_launch_status() != RB_OK) return RB_ERR_CUDA;
   note_launches(1);
-  if (num_reqs == 0) return RB_OK;
-  rb_status st = launch_decode(a, d.head_dim, kmap, vmap, s);
+  if (!mark(0)) return RB_ERR_CUDA;
+  rb_status st = RB_OK;
+  if (use_tc) {  // one launch runs decode and prefill units side by side
+    if (!mark(1)) return RB_ERR_CUDA;
+    if (num_reqs > 0) st = launch_prefill_tc(a, d.head_dim, qmap, kmap, vmap, s);
+    if (st != RB_OK) return st;
+    if (!mark(2)) return RB_ERR_CUDA;
+    return RB_OK;
+  }
+  if (num_reqs > 0) st = launch_decode(a, d.head_dim, kmap, vmap, s);
   if (st != RB_OK) return st;
-  return use_tc ? launch_prefill_tc(a, d.head_dim, qmap, kmap, vmap, s)
-                : launch_prefill(a, d.head_dim, kmap, vmap, s);
+  if (!mark(1)) return RB_ERR_CUDA;
+  if (num_reqs > 0) st = launch_prefill(a, d.head_dim, kmap, vmap, s);
+  if (st != RB_OK) return st;
+  if (!mark(2)) return RB_ERR_CUDA;
+  return RB_OK;
+}
+
+}  // namespace
+
+extern "C" rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
+                                        int32_t num_tokens_padded, const void* d_q,
+                                        const void* d_k_cache, const void* d_v_cache,
+                                        const int32_t* d_block_table,
+                                        const int32_t* d_query_start_loc,
+                                        const int32_t* d_seq_lens, float softmax_scale,
+                                        void* d_out, void* d_workspace, size_t workspace_bytes,
+                                        int32_t* d_error_word, void* stream) {
+  return paged_attention_impl(dims, num_reqs, num_tokens, num_tokens_padded, d_q, d_k_cache,
+                              d_v_cache, d_block_table, d_query_start_loc, d_seq_lens,
+                              softmax_scale, d_out, d_workspace, workspace_bytes, d_error_word,
+                              stream, nullptr, 0);
+}
+
+extern "C" rb_status rb_paged_attention_profiled(
+    const rb_dims* dims, int32_t num_reqs, int32_t num_tokens, int32_t num_tokens_padded,
+    const void* d_q, const void* d_k_cache, const void* d_v_cache, const int32_t* d_block_table,
+    const int32_t* d_query_start_loc, const int32_t* d_seq_lens, float softmax_scale, void* d_out,
+    void* d_workspace, size_t workspace_bytes, int32_t* d_error_word, void* stream,
+    void* const* events, int32_t num_events) {
+  if (num_events < 0 || (num_events > 0 && events == nullptr)) return RB_ERR_INVALID_ARG;
+  return paged_attention_impl(dims, num_reqs, num_tokens, num_tokens_padded, d_q, d_k_cache,
+                              d_v_cache, d_block_table, d_query_start_loc, d_seq_lens,
+                              softmax_scale, d_out, d_workspace, workspace_bytes, d_error_word,
+                              stream, events, num_events);
 }

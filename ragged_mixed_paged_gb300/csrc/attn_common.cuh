@@ -19,6 +19,8 @@ enum HeaderField : int {
   kHDecodeNext = 2,
   kHPrefillNext = 3,
   kHSplitPages = 4,
+  kHDecodeCtas = 5,  // fused kernel: CTAs that start on decode units
+  kHRoleNext = 6,    // fused kernel: role ticket counter
   kHeaderInts = 32
 };
 
@@ -63,6 +65,8 @@ struct AttnArgs {
   int R, N, N_pad, nh, nkv, group, MB, num_blocks, null_block;
   int target_units;
   int tile_m;  // query rows per prefill unit (256 on the tcgen05 path, 64 on the mma.sync path)
+  int fused_ctas;  // > 0: decode and prefill share one launch of this many CTAs (one per SM)
+  int decode_warps_per_cta;  // decode warps per CTA in the launch that runs decode units
   float scale_log2;
   int32_t* err;
 };

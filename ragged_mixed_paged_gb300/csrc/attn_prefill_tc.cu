@@ -1,6 +1,10 @@
 // Prefill / chunk attention on the 5th-generation tensor cores (tcgen05 + TMEM).
 //
-// Work unit = (request, kv head, pair of 128-row query tiles A and B); rows are (query token,
+// The same persistent launch also runs the split-KV decode units (attn_decode_warp.cuh): the
+// planner assigns each CTA a first kind of work (decode or prefill) so HBM-bound and
+// tensor-bound units run side by side; a CTA whose queue empties helps with the other one.
+//
+// Prefill unit = (request, kv head, pair of 128-row query tiles A and B); rows are (query token,
 // head of the group) pairs, token-major, so every K/V tile serves the whole query-head group
 // and both tiles of the pair.  One CTA per SM (persistent; units pulled from an atomic
 // counter, the most expensive pair of each request first), 12 warps with fixed roles:
@@ -21,6 +25,7 @@
 // All mbarrier waits are bounded; a timeout sets RB_EBIT_TIMEOUT, every role stops, in-flight
 // copies and MMAs are drained with bounded waits and TMEM is freed before the CTA exits.
 #include "attn_common.cuh"
+#include "attn_decode_warp.cuh"
 #include "tc_ptx.cuh"
 
 namespace rb {
@@ -42,6 +47,8 @@ struct TcCfg {
   static constexpr int kVOffset = kStagesK * kTileBytes;
   static constexpr int kQOffset = kVOffset + kStagesV * kTileBytes;  // Q_A then Q_B
   static constexpr int kUsed = kQOffset + 2 * kQBytes;
+  static_assert(8 * DecCfg<HD>::kStages * DecCfg<HD>::kStageBytes <= kUsed,
+                "the decode phase's stages must fit in the prefill phase's shared memory");
   // at least 120 KB keeps one CTA per SM (each CTA holds all 512 TMEM columns)
   static constexpr int kSmemBytes = (kUsed + 1024) > 120 * 1024 ? (kUsed + 1024) : 120 * 1024;
   // 3 warpgroups launched at 168 registers per thread (the 64-bit-register pool of one SM for
@@ -73,9 +80,11 @@ struct TcShared {
   uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint64_t drain;
+  uint64_t dec_bars[8][DecCfg<128>::kStages];  // decode phase: one ring per warp 0..7
   TcUnit units[4];
   uint32_t tmem_base;
   int abort;
+  int decode_first;
 };
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -520,7 +529,10 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
       mbar_init(&sh.o_free[i], 128);
     }
     mbar_init(&sh.drain, 1);
+    for (int w = 0; w < 8; ++w)
+      for (int st = 0; st < DecCfg<128>::kStages; ++st) mbar_init(&sh.dec_bars[w][st], 1);
     sh.abort = 0;
+    sh.decode_first = atomicAdd(a.header + kHRoleNext, 1) < a.header[kHDecodeCtas];
     fence_barrier_init();
   }
   if (warp == C::kMmaWarp) {
@@ -532,21 +544,43 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
   tc::fence_after_sync();
   const uint32_t tmem = sh.tmem_base;
 
+  // Two phases: the kind of work the planner assigned this CTA first, then the other kind
+  // until its queue is empty too.  The decode phase runs on warps 0-7, each with its own ring of
+  // decode stages in the same shared memory the prefill phase uses.  Each register class keeps
+  // its own loop so the code after setmaxnreg stays within that class's budget.
+  const bool decode_first = sh.decode_first != 0;
+  auto phase_end = [] {
+    fence_proxy_async_smem();  // generic smem traffic of this phase before the next one's TMA
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+  };
   if (warp >= 8) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kControlRegs));
-    if (warp == C::kProducerWarp) {
-      producer<HD>(a, sh, base, &qmap, &kmap, &vmap);
-    } else if (warp == C::kMmaWarp) {
-      if ((tid & 31) == 0) mma_issuer<HD>(a, sh, tmem, base);
+    for (int phase = 0; phase < 2; ++phase) {
+      if ((phase == 0) != decode_first) {
+        if (warp == C::kProducerWarp) {
+          producer<HD>(a, sh, base, &qmap, &kmap, &vmap);
+        } else if (warp == C::kMmaWarp) {
+          if ((tid & 31) == 0) mma_issuer<HD>(a, sh, tmem, base);
+        }
+      }
+      phase_end();
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(C::kSoftmaxRegs));
-    softmax_wg<HD>(a, sh, tmem, base_ptr, warp >> 2);
+    for (int phase = 0; phase < 2; ++phase) {
+      if ((phase == 0) == decode_first) {
+        using D = DecCfg<HD>;
+        decode_warp<HD>(&kmap, &vmap, a, sh.dec_bars[warp],
+                        base + warp * D::kStages * D::kStageBytes,
+                        base_ptr + warp * D::kStages * D::kStageBytes);
+      } else {
+        softmax_wg<HD>(a, sh, tmem, base_ptr, warp >> 2);
+      }
+      phase_end();
+    }
   }
-
-  tc::fence_before_sync();
-  __syncthreads();
-  tc::fence_after_sync();
   if (warp == C::kMmaWarp) {
     __syncwarp();
     tc::tmem_dealloc(tmem, C::kTmemCols);

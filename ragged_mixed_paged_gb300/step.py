@@ -67,11 +67,13 @@ class StepBuffers:
 
 
 def run_step(b: StepBuffers, stream=None, softmax_scale: Optional[float] = None,
-             marks=None) -> None:
+             marks=None, attn_marks=None) -> None:
     """Enqueue one whole step (all four library calls) on ``stream``.
 
     ``marks``: optional five CUDA events, recorded on the same stream before the first call
-    and after each of the four calls (for per-call timing).
+    and after each of the four calls (for per-call timing).  ``attn_marks``: optional three
+    recorded-once events the attention call re-records after its planner, decode and prefill
+    launches (per-kernel timing).
     """
     def mark(i):
         if marks is not None:
@@ -89,7 +91,7 @@ def run_step(b: StepBuffers, stream=None, softmax_scale: Optional[float] = None,
     rb.paged_attention(b.dims, b.num_reqs, b.num_tokens, b.q, b.k_cache, b.v_cache,
                        b.block_table, m["query_start_loc"], m["seq_lens"], out=b.attn_out,
                        workspace=b.workspace, softmax_scale=softmax_scale,
-                       error_word=b.error_word, stream=stream)
+                       error_word=b.error_word, stream=stream, events=attn_marks)
     mark(3)
     rb.gather_rows(b.hidden, m["logits_indices"], num_rows=b.num_reqs_padded, out=b.rows_out,
                    error_word=b.error_word, stream=stream)

@@ -113,8 +113,16 @@ def test_whole_step(rb, name, make):
     compare_attention(buf.attn_out, ref, spec.num_tokens)
     assert np.array_equal(_u16(buf.rows_out),
                           oracle.gather_rows(_u16(tens.hidden), meta["logits_indices"]))
-    # a second step on the same buffers gives the same answer (fixed addresses, no state)
+    # a second step on the same buffers gives the same answer (fixed addresses, no state), also
+    # through the profiled attention entry point that records events between its launches
     first = buf.attn_out.clone()
-    run_step(buf)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    attn_marks = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    for e in attn_marks:
+        e.record()
+    run_step(buf, marks=marks, attn_marks=attn_marks)
     torch.cuda.synchronize()
     assert torch.equal(buf.attn_out, first)
+    times = [marks[2].elapsed_time(attn_marks[0]), attn_marks[0].elapsed_time(attn_marks[1]),
+             attn_marks[1].elapsed_time(attn_marks[2]), attn_marks[2].elapsed_time(marks[3])]
+    assert all(t >= 0 for t in times)
