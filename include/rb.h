@@ -117,6 +117,13 @@ int32_t rb_pad_for_graph(const int32_t* capture_sizes, int32_t num_sizes, int32_
  *   d_query_start_loc                          [num_reqs_padded + 1]
  *   d_seq_lens, d_logits_indices               [num_reqs_padded]
  *   d_scalars [4] = {max_query_len, max_seq_len, num_actual_tokens (= num_tokens), error word}
+ * Optional phase flags ("Chunked Prefill：query 很长，但仍只是一段区间", "第四步"): when
+ *   d_is_prefilling and d_discard_request_mask [num_reqs_padded] (int32 0/1) are given (both,
+ *   with d_num_prompt [num_reqs] = prompt lengths whenever num_reqs > 0) they receive
+ *   is_prefilling = num_computed < num_prompt (not "query length 1 means decode") and
+ *   discard_request_mask = num_computed + num_scheduled < num_prompt (the chunk ends inside the
+ *   prompt, so the token sampled from its last position is not an output); padded requests get
+ *   0 and 1.  With both flag pointers NULL nothing is written and d_num_prompt is ignored.
  * Padding: request i >= num_reqs gets the empty interval at the end (query_start_loc = N),
  *   seq_len 0 and logits index max(N-1, 0); token t >= N gets input id 0, position 0 and slot
  *   null_block * B + (t - N) % B, so padding only ever touches the null page.
@@ -131,7 +138,9 @@ rb_status rb_prepare_inputs(const rb_dims* dims, int32_t num_reqs, int32_t num_r
                             int32_t* d_input_ids, int32_t* d_positions,
                             int32_t* d_query_start_loc, int32_t* d_seq_lens,
                             int32_t* d_slot_mapping, int32_t* d_logits_indices,
-                            int32_t* d_scalars, void* stream);
+                            int32_t* d_scalars, const int32_t* d_num_prompt,
+                            int32_t* d_is_prefilling, int32_t* d_discard_request_mask,
+                            void* stream);
 
 /*
  * rb_kv_write — scatter this step's K and V rows into the paged cache.

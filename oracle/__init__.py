@@ -20,10 +20,11 @@ Every function is pinned by ``tests/test_oracle_*.py`` against values the pages
 print, closed forms, special cases that reduce to library routines, and brute
 force over tiny inputs.
 """
-from .metadata import prepare_inputs, pad_for_graph, padded_layout_tokens, req_indices_and_query_pos
+from .metadata import (prepare_inputs, pad_for_graph, padded_layout_tokens,
+                       req_indices_and_query_pos, request_flags)
 from .kv_cache import kv_write
 from .attention import paged_attention
 from .gather import gather_rows
 
-__all__ = ["prepare_inputs", "pad_for_graph", "padded_layout_tokens", "req_indices_and_query_pos",
+__all__ = ["prepare_inputs", "request_flags", "pad_for_graph", "padded_layout_tokens", "req_indices_and_query_pos",
            "kv_write", "paged_attention", "gather_rows"]

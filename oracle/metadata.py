@@ -48,13 +48,15 @@ def req_indices_and_query_pos(num_scheduled: Sequence[int]):
 def prepare_inputs(*, block_size: int, null_block: int, token_table: np.ndarray,
                    block_table: np.ndarray, num_computed: Sequence[int],
                    num_scheduled: Sequence[int], num_reqs_padded: int | None = None,
-                   num_tokens_padded: int | None = None) -> Dict[str, np.ndarray]:
+                   num_tokens_padded: int | None = None,
+                   num_prompt: Sequence[int] | None = None) -> Dict[str, np.ndarray]:
     """Flat step inputs and attention metadata of one batch, as plain loops.
 
     Returns int64 arrays ``query_start_loc [R_pad+1]``, ``seq_lens [R_pad]``,
     ``positions [N_pad]``, ``input_ids [N_pad]``, ``slot_mapping [N_pad]``,
     ``logits_indices [R_pad]``, ``visible_keys [N]`` (keys each query may read, "4. 注意力读取边界")
-    and ints ``max_query_len``, ``max_seq_len``, ``num_actual_tokens``.
+    and ints ``max_query_len``, ``max_seq_len``, ``num_actual_tokens``.  With ``num_prompt``
+    also ``is_prefilling [R_pad]`` and ``discard_request_mask [R_pad]`` (see request_flags).
     """
     B = int(block_size)
     R = len(num_scheduled)
@@ -92,7 +94,10 @@ def prepare_inputs(*, block_size: int, null_block: int, token_table: np.ndarray,
     # 第四步: last flat token of every request
     logits = [qsl[i + 1] - 1 for i in range(R)] + [max(N - 1, 0)] * (R_pad - R)
 
+    flags = {} if num_prompt is None else request_flags(num_computed, num_scheduled, num_prompt,
+                                                        R_pad)
     return dict(
+        **flags,
         query_start_loc=np.array(qsl, np.int64),
         seq_lens=np.array(seq_lens, np.int64),
         positions=np.array(positions, np.int64),
@@ -104,6 +109,30 @@ def prepare_inputs(*, block_size: int, null_block: int, token_table: np.ndarray,
         max_seq_len=max(seq_lens[:R] + [0]),
         num_actual_tokens=N,
     )
+
+
+def request_flags(num_computed: Sequence[int], num_scheduled: Sequence[int],
+                  num_prompt: Sequence[int], num_reqs_padded: int | None = None):
+    """Phase flags of each request ("Chunked Prefill：query 很长，但仍只是一段区间" and
+    "第四步：只在必要位置计算 logits" on the GPUModelRunner page).
+
+    is_prefilling[i]: the request has not yet computed its whole prompt before this step
+    (num_computed < num_prompt) — the page's rule, not "query length 1 means decode".
+    discard_request_mask[i]: this step's chunk still stops inside the prompt
+    (num_computed + num_scheduled < num_prompt), so the token sampled from its last position is
+    not an output.  Reading: a padded request is not prefilling and its logits are discarded.
+    """
+    R = len(num_scheduled)
+    R_pad = R if num_reqs_padded is None else int(num_reqs_padded)
+    prefilling, discard = [], []
+    for i in range(R):
+        c, q, p = int(num_computed[i]), int(num_scheduled[i]), int(num_prompt[i])
+        prefilling.append(1 if c < p else 0)
+        discard.append(1 if c + q < p else 0)
+    prefilling += [0] * (R_pad - R)
+    discard += [1] * (R_pad - R)
+    return dict(is_prefilling=np.array(prefilling, np.int64),
+                discard_request_mask=np.array(discard, np.int64))
 
 
 def pad_for_graph(capture_sizes: Sequence[int], num_tokens: int) -> int:

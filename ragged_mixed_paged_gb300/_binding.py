@@ -57,7 +57,8 @@ def _load():
         "rb_status_string": (ctypes.c_char_p, [I32]),
         "rb_kernel_launch_count": (ctypes.c_uint64, []),
         "rb_pad_for_graph": (I32, [P, I32, I32]),
-        "rb_prepare_inputs": (I32, [PD, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P]),
+        "rb_prepare_inputs": (I32, [PD, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P,
+                                    P, P, P]),
         "rb_kv_write": (I32, [PD, I32, P, P, P, P, P, P, P]),
         "rb_paged_attention_workspace_size": (ctypes.c_size_t, [PD, I32, I32]),
         "rb_paged_attention": (I32, [PD, I32, I32, I32, P, P, P, P, P, P, ctypes.c_float, P, P,
@@ -149,8 +150,11 @@ def workspace_size(dims: Dims, max_num_reqs: int, max_num_tokens: int) -> int:
 
 def prepare_inputs(dims: Dims, num_reqs: int, num_reqs_padded: int, num_tokens: int,
                    num_tokens_padded: int, token_table, num_computed, num_scheduled, block_table,
-                   out: Optional[dict] = None, stream=None) -> dict:
-    """Flat step inputs + metadata; returns the output tensors (allocated unless given)."""
+                   out: Optional[dict] = None, stream=None, num_prompt=None) -> dict:
+    """Flat step inputs + metadata; returns the output tensors (allocated unless given).
+
+    With ``num_prompt`` (int32 prompt lengths) the output also holds ``is_prefilling`` and
+    ``discard_request_mask`` ([num_reqs_padded] int32)."""
     import torch
 
     i32 = torch.int32
@@ -164,6 +168,10 @@ def prepare_inputs(dims: Dims, num_reqs: int, num_reqs_padded: int, num_tokens: 
             slot_mapping=torch.empty(num_tokens_padded, dtype=i32, device=dev),
             logits_indices=torch.empty(num_reqs_padded, dtype=i32, device=dev),
             scalars=torch.empty(4, dtype=i32, device=dev))
+    if num_prompt is not None and "is_prefilling" not in out:
+        out["is_prefilling"] = torch.empty(num_reqs_padded, dtype=i32, device=dev)
+        out["discard_request_mask"] = torch.empty(num_reqs_padded, dtype=i32, device=dev)
+    with_flags = num_prompt is not None
     d = dims.c()
     st = lib.rb_prepare_inputs(
         ctypes.byref(d), num_reqs, num_reqs_padded, num_tokens, num_tokens_padded,
@@ -172,7 +180,10 @@ def prepare_inputs(dims: Dims, num_reqs: int, num_reqs_padded: int, num_tokens: 
         _ptr(out["input_ids"], i32), _ptr(out["positions"], i32),
         _ptr(out["query_start_loc"], i32), _ptr(out["seq_lens"], i32),
         _ptr(out["slot_mapping"], i32), _ptr(out["logits_indices"], i32),
-        _ptr(out["scalars"], i32), _stream(stream))
+        _ptr(out["scalars"], i32),
+        _ptr(num_prompt, i32, "num_prompt") if with_flags and num_prompt.numel() else None,
+        _ptr(out["is_prefilling"], i32) if with_flags else None,
+        _ptr(out["discard_request_mask"], i32) if with_flags else None, _stream(stream))
     _check("rb_prepare_inputs", st)
     return out
 

@@ -8,6 +8,8 @@
 //   input_ids[t]    = token_table[r, positions[t]]
 //   slot_mapping[t] = block_table[r, pos / B] * B + pos % B         (padding -> null page)
 //   logits_indices  = query_start_loc[1:] - 1
+//   is_prefilling   = num_computed < num_prompt, discard_request_mask = seq_len < num_prompt
+//                     (optional; "Chunked Prefill：query 很长，但仍只是一段区间")
 //
 // Design: the per-request arrays are tiny, so every CTA recomputes the prefix sum of
 // num_scheduled in shared memory (warp-shuffle scan) instead of waiting on a second launch;
@@ -37,6 +39,9 @@ struct PrepArgs {
   int32_t* slots;
   int32_t* logits;
   int32_t* scalars;
+  const int32_t* __restrict__ num_prompt;  // optional: phase flags below
+  int32_t* is_prefilling;
+  int32_t* discard;
 };
 
 // Exclusive prefix sum of num_scheduled[0..R) into s_qsl[0..R] (s_qsl[R] = total).
@@ -99,9 +104,18 @@ __global__ void __launch_bounds__(kThreads) prepare_inputs_kernel(PrepArgs a) {
         a.logits[i] = s_qsl[i + 1] - 1;
         my_q = max(my_q, q);
         my_len = max(my_len, static_cast<int>(len));
+        if (a.is_prefilling != nullptr) {  // "Chunked Prefill": phase from computed vs prompt
+          const int p = a.num_prompt[i];
+          a.is_prefilling[i] = c < p ? 1 : 0;
+          a.discard[i] = len < p ? 1 : 0;
+        }
       } else {
         a.seq_lens[i] = 0;
         a.logits[i] = max(a.N - 1, 0);
+        if (a.is_prefilling != nullptr) {
+          a.is_prefilling[i] = 0;
+          a.discard[i] = 1;
+        }
       }
     }
     if (tid == 0 && total != a.N) bits |= RB_EBIT_TOKEN_SUM;
@@ -192,7 +206,8 @@ extern "C" rb_status rb_prepare_inputs(const rb_dims* dims, int32_t num_reqs,
                                        int32_t* d_positions, int32_t* d_query_start_loc,
                                        int32_t* d_seq_lens, int32_t* d_slot_mapping,
                                        int32_t* d_logits_indices, int32_t* d_scalars,
-                                       void* stream) {
+                                       const int32_t* d_num_prompt, int32_t* d_is_prefilling,
+                                       int32_t* d_discard_request_mask, void* stream) {
   using namespace rb;
   if (dims == nullptr || d_query_start_loc == nullptr || d_scalars == nullptr)
     return RB_ERR_INVALID_ARG;
@@ -217,13 +232,19 @@ extern "C" rb_status rb_prepare_inputs(const rb_dims* dims, int32_t num_reqs,
       (d_input_ids == nullptr || d_positions == nullptr || d_slot_mapping == nullptr))
     return RB_ERR_INVALID_ARG;
 
+  // phase flags are written when both flag outputs are given (prompt lengths then needed)
+  const bool flags = d_is_prefilling != nullptr || d_discard_request_mask != nullptr;
+  if (flags && (d_is_prefilling == nullptr || d_discard_request_mask == nullptr ||
+                (num_reqs > 0 && d_num_prompt == nullptr)))
+    return RB_ERR_INVALID_ARG;
+
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(d_scalars + 3, 0, sizeof(int32_t), s) != cudaSuccess) return RB_ERR_CUDA;
   PrepArgs a{num_reqs, num_reqs_padded, num_tokens, num_tokens_padded, d.block_size,
              d.max_model_len, d.max_blocks_per_req, d.num_blocks, d.null_block,
              d_token_table, d_num_computed, d_num_scheduled, d_block_table, d_input_ids,
              d_positions, d_query_start_loc, d_seq_lens, d_slot_mapping, d_logits_indices,
-             d_scalars};
+             d_scalars, d_num_prompt, d_is_prefilling, d_discard_request_mask};
   const size_t smem = static_cast<size_t>(num_reqs + 1) * sizeof(int32_t);
   if (smem > 48 * 1024) {
     if (cudaFuncSetAttribute(prepare_inputs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,

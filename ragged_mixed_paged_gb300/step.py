@@ -34,6 +34,7 @@ class StepBuffers:
     attn_out: object
     workspace: object
     rows_out: object
+    num_prompt: object = None  # int32 prompt lengths: enables is_prefilling / discard mask
 
     @classmethod
     def allocate(cls, dims: rb.Dims, num_reqs: int, num_reqs_padded: int, num_tokens: int,
@@ -50,6 +51,9 @@ class StepBuffers:
             slot_mapping=torch.empty(num_tokens_padded, dtype=i32, device=dev),
             logits_indices=torch.empty(num_reqs_padded, dtype=i32, device=dev),
             scalars=torch.zeros(4, dtype=i32, device=dev))
+        if tables.get("num_prompt") is not None:
+            meta["is_prefilling"] = torch.empty(num_reqs_padded, dtype=i32, device=dev)
+            meta["discard_request_mask"] = torch.empty(num_reqs_padded, dtype=i32, device=dev)
         ws = torch.empty(rb.workspace_size(dims, max(num_reqs, 1), max(num_tokens, 1)),
                          dtype=torch.uint8, device=dev)
         return cls(dims=dims, num_reqs=num_reqs, num_reqs_padded=num_reqs_padded,
@@ -59,7 +63,8 @@ class StepBuffers:
                    q=q, k=k, v=v, hidden=hidden, k_cache=k_cache, v_cache=v_cache, meta=meta,
                    attn_out=torch.empty_like(q), workspace=ws,
                    rows_out=torch.empty((num_reqs_padded, hidden.shape[1]), dtype=hidden.dtype,
-                                        device=dev))
+                                        device=dev),
+                   num_prompt=tables.get("num_prompt"))
 
     @property
     def error_word(self):
@@ -83,7 +88,7 @@ def run_step(b: StepBuffers, stream=None, softmax_scale: Optional[float] = None,
     mark(0)
     rb.prepare_inputs(b.dims, b.num_reqs, b.num_reqs_padded, b.num_tokens, b.num_tokens_padded,
                       b.token_table, b.num_computed, b.num_scheduled, b.block_table, out=m,
-                      stream=stream)
+                      stream=stream, num_prompt=b.num_prompt)
     mark(1)
     rb.kv_write(b.dims, b.k, b.v, m["slot_mapping"], b.k_cache, b.v_cache,
                 error_word=b.error_word, num_tokens_padded=b.num_tokens_padded, stream=stream)

@@ -23,7 +23,8 @@ def oracle_meta(spec):
                                  token_table=spec.token_table, block_table=spec.block_table,
                                  num_computed=spec.num_computed, num_scheduled=spec.num_scheduled,
                                  num_reqs_padded=spec.num_reqs_padded,
-                                 num_tokens_padded=spec.num_tokens_padded)
+                                 num_tokens_padded=spec.num_tokens_padded,
+                                 num_prompt=spec.num_prompt)
 
 
 def i32(a, device="cuda"):

@@ -71,7 +71,7 @@ MISALIGNED = ctypes.c_void_p(0x100008)
 def test_prepare_inputs_host_checks(lib):
     L = lib.lib
     d = _dims(lib)
-    args = [FAKE] * 11  # token_table .. scalars; the stream follows
+    args = [FAKE] * 11 + [None] * 3  # token_table .. scalars, no phase flags; stream follows
     assert L.rb_prepare_inputs(None, 1, 1, 1, 1, *args, None) == 1
     assert L.rb_prepare_inputs(ctypes.byref(d), 9, 9, 9, 9, *args, None) == 2   # > max_num_reqs
     assert L.rb_prepare_inputs(ctypes.byref(d), 2, 1, 2, 2, *args, None) == 1   # R_pad < R
@@ -79,8 +79,12 @@ def test_prepare_inputs_host_checks(lib):
     assert L.rb_prepare_inputs(ctypes.byref(d), 1, 2, 1, 0, *args, None) == 1   # N_pad = 0
     bad = _dims(lib, null_block=1000)
     assert L.rb_prepare_inputs(ctypes.byref(bad), 1, 1, 1, 1, *args, None) == 1
-    nul = [FAKE] * 6 + [None] + [FAKE] * 4  # query_start_loc missing
+    nul = [FAKE] * 6 + [None] + [FAKE] * 4 + [None] * 3  # query_start_loc missing
     assert L.rb_prepare_inputs(ctypes.byref(d), 1, 1, 1, 1, *nul, None) == 1
+    half = [FAKE] * 11 + [FAKE, FAKE, None]  # one flag output without the other
+    assert L.rb_prepare_inputs(ctypes.byref(d), 1, 1, 1, 1, *half, None) == 1
+    noprompt = [FAKE] * 11 + [None, FAKE, FAKE]  # flags requested without prompt lengths
+    assert L.rb_prepare_inputs(ctypes.byref(d), 1, 1, 1, 1, *noprompt, None) == 1
 
 
 def test_kv_write_host_checks(lib):

@@ -16,7 +16,7 @@ def _run(rb, spec, num_tokens=None):
     out = rb.prepare_inputs(dims_of(spec), spec.num_reqs, spec.num_reqs_padded,
                             spec.num_tokens if num_tokens is None else num_tokens,
                             spec.num_tokens_padded, t["token_table"], t["num_computed"],
-                            t["num_scheduled"], t["block_table"])
+                            t["num_scheduled"], t["block_table"], num_prompt=t.get("num_prompt"))
     torch.cuda.synchronize()
     return {k: v.cpu().numpy() for k, v in out.items()}
 
@@ -25,6 +25,9 @@ def _assert_exact(got, spec):
     ref = oracle_meta(spec)
     for k in KEYS:
         assert np.array_equal(got[k], ref[k]), k
+    if spec.num_prompt is not None:
+        for k in ("is_prefilling", "discard_request_mask"):
+            assert np.array_equal(got[k], ref[k]), k
     assert got["scalars"].tolist() == [ref["max_query_len"], ref["max_seq_len"],
                                        ref["num_actual_tokens"], 0]
 
@@ -61,6 +64,20 @@ def test_fuzzed_mixes_bit_exact(rb, seed):
     spec = wl.random_batch(seed, block_size=B, max_reqs=12, max_q=70, max_c=200,
                            pad_tokens=seed % 5, pad_reqs=seed % 3)
     _assert_exact(_run(rb, spec), spec)
+
+
+def test_phase_flags_page_examples(rb):
+    """The debug example prints discard=[False, True]; the exercise drops request 3's logits."""
+    from conftest import load_golden
+
+    for name in ("runner_debug_example.json", "batch_layout_exercise.json"):
+        g = load_golden(name)
+        spec = wl.batch_from_lists(g["inputs"]["num_computed"], g["inputs"]["num_scheduled"])
+        spec.num_prompt = np.array(g["inputs"]["num_prompt"], np.int32)
+        got = _run(rb, spec)
+        assert got["discard_request_mask"].astype(bool).tolist() == \
+            g["expected"]["discard_request_mask"]
+        _assert_exact(got, spec)
 
 
 def test_empty_batch(rb):

@@ -203,3 +203,31 @@ def test_random_three_request_batches():
         out = oracle.prepare_inputs(block_size=B, null_block=0, token_table=tok, block_table=bt,
                                     num_computed=c, num_scheduled=q)
         _check_invariants(c, q, B, out, bt)
+
+
+def test_request_flags_debug_example():
+    """'最小可复现实验': the page prints discard=[False, True] for A (decode) and B (chunk)."""
+    g = load_golden("runner_debug_example.json")
+    i, e = g["inputs"], g["expected"]
+    out = _run(i["num_computed"], i["num_scheduled"], num_prompt=i["num_prompt"])
+    assert out["discard_request_mask"].astype(bool).tolist() == e["discard_request_mask"]
+    assert out["is_prefilling"].astype(bool).tolist() == e["is_prefilling"]
+
+
+def test_request_flags_exercise_answer():
+    """'练习' 1: request 3 stops at 20 of its 40 prompt tokens, so its logits are not sampled; the
+    answer keeps logits only where the discard mask is clear."""
+    g = load_golden("batch_layout_exercise.json")
+    i, e = g["inputs"], g["expected"]
+    out = _run(i["num_computed"], i["num_scheduled"], num_prompt=i["num_prompt"])
+    assert out["discard_request_mask"].astype(bool).tolist() == e["discard_request_mask"]
+    kept = [int(x) for x, d in zip(out["logits_indices"], out["discard_request_mask"]) if not d]
+    assert kept == e["logits_indices_needed"]
+
+
+def test_one_token_query_can_still_be_prefilling():
+    """'Chunked Prefill' section: a short query does not mean decode; the phase comes from
+    num_computed against num_prompt."""
+    flags = oracle.request_flags([5, 9, 12, 0], [1, 1, 1, 4], [9, 9, 12, 2], num_reqs_padded=6)
+    assert flags["is_prefilling"].tolist() == [1, 0, 0, 1, 0, 0]
+    assert flags["discard_request_mask"].tolist() == [1, 0, 0, 0, 1, 1]

@@ -125,6 +125,8 @@ def _build_spec(name, dims, computed, scheduled, rng, hidden_size, seed,
         n = pages_for(total, dims.block_size)
         block_table[i, :n] = pool.take(n)
     n_tok = int(scheduled.sum(dtype=np.int64))
+    if num_prompt is None:  # decodes: prompt already computed; longer queries finish their prompt
+        num_prompt = [int(c) if int(q) == 1 else int(c) + int(q) for c, q in zip(computed, scheduled)]
     return BatchSpec(name=name, dims=dims, num_computed=computed, num_scheduled=scheduled,
                      num_reqs_padded=R if num_reqs_padded is None else num_reqs_padded,
                      num_tokens_padded=n_tok if num_tokens_padded is None else num_tokens_padded,
@@ -238,8 +240,13 @@ def random_batch(seed: int, *, max_reqs: int = 6, max_q: int = 40, max_c: int = 
                 max_blocks_per_req=M // block_size,
                 num_blocks=_pool_blocks_for(computed, scheduled, block_size) + 3)
     n = sum(scheduled)
-    return _build_spec(f"random mix seed={seed}", dims, computed, scheduled, rng, hidden_size, seed,
-                       num_reqs_padded=R + pad_reqs, num_tokens_padded=n + pad_tokens)
+    spec = _build_spec(f"random mix seed={seed}", dims, computed, scheduled, rng, hidden_size,
+                       seed, num_reqs_padded=R + pad_reqs, num_tokens_padded=n + pad_tokens)
+    # some chunks stop inside their prompt (drawn last so the other draws do not move)
+    extra = rng.integers(0, 2, size=R) * rng.integers(1, max_q + 1, size=R)
+    spec.num_prompt = np.where(spec.num_scheduled > 1, spec.num_prompt + extra,
+                               spec.num_prompt).astype(np.int32)
+    return spec
 
 
 def batch_from_lists(num_computed, num_scheduled, *, block_size=16, num_q_heads=4, num_kv_heads=2,
@@ -479,8 +486,11 @@ def device_tables(spec: BatchSpec, device):
     def t(a):
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(device)
 
-    return dict(token_table=t(spec.token_table), block_table=t(spec.block_table),
-                num_computed=t(spec.num_computed), num_scheduled=t(spec.num_scheduled))
+    out = dict(token_table=t(spec.token_table), block_table=t(spec.block_table),
+               num_computed=t(spec.num_computed), num_scheduled=t(spec.num_scheduled))
+    if spec.num_prompt is not None:
+        out["num_prompt"] = t(spec.num_prompt)
+    return out
 
 
 def with_padding(spec: BatchSpec, num_reqs_padded: int, num_tokens_padded: int) -> BatchSpec:
