@@ -44,7 +44,42 @@ KNOWN_TRAFFIC = {
 
 
 # ----------------------------------------------------------------------------- workloads
-def make_spec(config: int, rank: int = 0):
+def chunked_mix_step0(rank: int, oracle_layout: bool = False):
+    """Step 0 of the chunked-prefill request stream, laid out into batch rows by the library's
+    own device-side batch update (the oracle's InputBatch on the reference leg)."""
+    import workloads as wl
+
+    stream = wl.MixedChunkStream(seed=4000 + 7919 * rank)
+    step, d = stream.next_step(), stream.dims
+    if oracle_layout:
+        from oracle.persistent_batch import InputBatch
+
+        batch = InputBatch(d.max_num_reqs, d.max_model_len, d.max_blocks_per_req)
+        batch.apply(step)
+        cols = batch.columns(step.scheduled)
+        tok, blk = batch.tables()
+        computed, sched, prompt = cols["num_computed"], cols["num_scheduled"], cols["num_prompt"]
+    else:
+        import torch
+
+        import ragged_mixed_paged_gb300 as rb
+
+        batch = rb.PersistentBatch(d.max_num_reqs, d.max_model_len, d.max_blocks_per_req)
+        batch.apply(step)
+        torch.cuda.synchronize()
+        if int(batch.error_word.item()) != 0:
+            raise SystemExit(f"batch update error word {int(batch.error_word.item()):#x}")
+        R = batch.num_reqs
+        computed = batch.num_computed[:R].cpu().numpy()
+        sched = batch.num_scheduled[:R].cpu().numpy()
+        prompt = batch.num_prompt[:R].cpu().numpy()
+        tok, blk = batch.token_table.cpu().numpy(), batch.block_table.cpu().numpy()
+        del batch
+    return wl.spec_from_columns("chunked-prefill mix step 0", d, computed, sched, prompt, tok, blk,
+                                seed=(4000 + 7919 * rank) * 1000)
+
+
+def make_spec(config: int, rank: int = 0, oracle_layout: bool = False):
     import workloads as wl
 
     if config == 1:
@@ -54,7 +89,7 @@ def make_spec(config: int, rank: int = 0):
     if config == 3:
         return wl.config3(step=rank)
     if config == 4:
-        return wl.MixedChunkSimulator(seed=4000 + 7919 * rank).next_step()
+        return chunked_mix_step0(rank, oracle_layout)
     if config == 5:
         return wl.config5(step=rank)
     raise SystemExit(f"unknown config {config}")
@@ -272,7 +307,7 @@ def cpu_baseline(spec, target_s=12.0):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    spec = make_spec(args.config)
+    spec = make_spec(args.config, oracle_layout=True)
     import workloads as wl
 
     tens = wl.make_tensors(spec, device="cpu")

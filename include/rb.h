@@ -9,6 +9,11 @@
  *   rb_paged_attention  varlen causal GQA attention through the page table
  *   rb_gather_rows      hidden rows at logits_indices (the rows the LM head needs)
  *
+ * and, before rb_prepare_inputs, the runner's per-step merge of scheduler deltas into the
+ * persistent batch:
+ *
+ *   rb_batch_apply_update  remove, append, install and condense rows on the device
+ *
  * Conventions shared by every entry point
  * ---------------------------------------
  *  - Every pointer named d_* is DEVICE memory on the current CUDA device; the caller owns it,
@@ -251,6 +256,101 @@ rb_status rb_paged_attention_static_ws(const rb_dims* dims, int32_t num_reqs, in
 rb_status rb_gather_rows(int32_t num_rows, int32_t hidden_size, int32_t num_hidden_rows,
                          const void* d_hidden, const int32_t* d_indices, void* d_out,
                          int32_t* d_error_word, void* stream);
+
+/*
+ * Persistent batch — one row per resident request, every column device-resident and
+ * caller-owned ("vLLM 源码完全拆解（五）…", "行号是一种短生命周期地址": the row is the common key
+ * of the request's token history, counters and page row; a move must carry every column).
+ * The live rows are always the prefix [0, *d_num_rows).  Contents past a row's d_num_tokens /
+ * d_num_blocks, and rows at or past *d_num_rows, are not state and may hold anything.  Start
+ * an empty batch with *d_num_rows = 0 (the other columns need no initial values).
+ */
+typedef struct rb_batch {
+  int32_t max_num_reqs;       /* rows (<= 4096) */
+  int32_t max_model_len;      /* M: token-table columns */
+  int32_t max_blocks_per_req; /* MB: page-table columns */
+  int32_t reserved;           /* 0 */
+  int64_t* d_req_id;          /* [max_num_reqs] request id of each live row (ids are >= 0) */
+  int32_t* d_token_table;     /* [max_num_reqs, M] token history of each row */
+  int32_t* d_num_tokens;      /* [max_num_reqs] valid history length of each row */
+  int32_t* d_num_prompt;      /* [max_num_reqs] prompt length */
+  int32_t* d_num_computed;    /* [max_num_reqs] tokens already in the KV cache */
+  int32_t* d_block_table;     /* [max_num_reqs, MB] page ids of each row */
+  int32_t* d_num_blocks;      /* [max_num_reqs] valid page-table entries of each row */
+  int32_t* d_num_rows;        /* [1] live rows */
+} rb_batch;
+
+/*
+ * One step's scheduler output in request-id terms ("第8章 ModelRunner…", "8.2.2 三种变更操作";
+ * "vLLM 源码完全拆解（五）…", "新请求建立完整状态" and "驻留请求只合并差量").  All arrays are
+ * device memory (typically slices of one buffer filled by a single host-to-device copy);
+ * offsets arrays have count + 1 non-decreasing entries indexing the payload that follows them.
+ */
+typedef struct rb_batch_update {
+  int32_t num_scheduled;             /* S: requests scheduled this step (new ones included) */
+  int32_t num_new;                   /* NN */
+  int32_t num_cached;                /* NC */
+  int32_t reserved;                  /* 0 */
+  const int64_t* d_sched_req_id;     /* [S] */
+  const int32_t* d_sched_num_tokens; /* [S] tokens scheduled for each */
+  const int64_t* d_new_req_id;       /* [NN] requests entering the batch, whole state: */
+  const int32_t* d_new_num_computed; /* [NN] */
+  const int32_t* d_new_num_prompt;   /* [NN] */
+  const int32_t* d_new_token_start;  /* [NN + 1] -> d_new_tokens: each request's history */
+  const int32_t* d_new_tokens;
+  const int32_t* d_new_block_start;  /* [NN + 1] -> d_new_blocks: each request's page ids */
+  const int32_t* d_new_blocks;
+  const int64_t* d_cached_req_id;      /* [NC] resident requests that changed: */
+  const int32_t* d_cached_num_computed;/* [NC] new num_computed */
+  const int32_t* d_cached_replace;     /* [NC] 1: resumed from preemption, the page row is
+                                          replaced by the given ids; 0: they are appended */
+  const int32_t* d_cached_token_start; /* [NC + 1] -> d_cached_tokens: appended to the history */
+  const int32_t* d_cached_tokens;
+  const int32_t* d_cached_block_start; /* [NC + 1] -> d_cached_blocks */
+  const int32_t* d_cached_blocks;
+} rb_batch_update;
+
+#define RB_EBIT_BATCH_ID 0x200    /* rb_batch_apply_update: a negative or repeated request id, a
+                                     new request that is not scheduled, a delta for a request
+                                     that is not resident, or a scheduled request that is
+                                     neither resident nor new */
+#define RB_EBIT_BATCH_SIZE 0x400  /* rb_batch_apply_update: decreasing offsets, a history longer
+                                     than M or a page row longer than MB */
+
+/* Workspace bytes rb_batch_apply_update needs for a batch of `max_num_reqs` rows. */
+rb_status rb_batch_update_workspace_size(int32_t max_num_reqs, size_t* bytes);
+
+/*
+ * rb_batch_apply_update — merge one step's scheduler output into the persistent batch, in the
+ * order the runner does it, then write this step's per-row scheduled counts.
+ * Source: "vLLM 源码完全拆解（五）…", "先删除完成和本轮未调度的请求", "新请求建立完整状态",
+ * "驻留请求只合并差量", "最后压紧并刷新派生 metadata" and "行号是一种短生命周期地址" (A B C D, B
+ * finishes, D moves to row 1); "第8章 ModelRunner…", "8.2.2.5 _update_states 的真实四段执行"
+ * (removals first; new requests take the freed rows) and "8.2.2.6" (an id that is finished and
+ * scheduled as new again names a new request); "04 · 模型执行与 CUDA Graph", "4.2 块表" (append_row).
+ *
+ *  1. a live row is removed unless its request is scheduled and not announced again as new;
+ *  2. each resident request in the cached list sets num_computed, appends its tokens after its
+ *     history, and appends its page ids (or, with replace, makes them its whole page row);
+ *  3. new requests, in list order, take the freed rows in ascending order, then the rows after
+ *     the old end of the batch, each with its whole history, counters and page row;
+ *  4. condense: the highest live row moves (all columns) into the lowest remaining hole, the
+ *     next highest into the next, until the live rows are [0, S).
+ * Outputs: the batch (columns and *d_num_rows = S); d_num_scheduled [max_num_reqs] int32 =
+ *   tokens scheduled for each row (0 for rows >= S), the d_num_scheduled input of
+ *   rb_prepare_inputs with num_reqs = S; d_row_of_sched [S] int32 (or NULL) = the row of each
+ *   scheduled request.
+ * Work: a one-block planner (request-id hash, hole scan, pairing, counters) and a grid of
+ *   16-byte copies of the moved and installed token and page rows.
+ * Errors: host -> RB_ERR_INVALID_ARG (null pointers, negative counts, NN or NC > S),
+ *   RB_ERR_CAPACITY (S > max_num_reqs, small workspace), RB_ERR_UNSUPPORTED (max_num_reqs >
+ *   4096); device -> RB_EBIT_BATCH_ID / RB_EBIT_BATCH_SIZE in *d_error_word (not zeroed here),
+ *   and then the batch is left exactly as it was and the two outputs are unspecified.
+ */
+rb_status rb_batch_apply_update(const rb_batch* batch, const rb_batch_update* update,
+                                int32_t* d_num_scheduled, int32_t* d_row_of_sched,
+                                void* d_workspace, size_t workspace_bytes,
+                                int32_t* d_error_word, void* stream);
 
 #ifdef __cplusplus
 }

@@ -5,6 +5,8 @@
     kv_write         new K/V rows -> paged cache by slot_mapping
     paged_attention  varlen causal GQA attention through the page table
     gather_rows      hidden rows at logits_indices
+    PersistentBatch  device-resident rows of the resident requests; ``apply`` merges one
+                     step's scheduler output (remove, append, install, condense) on the GPU
     pad_for_graph    smallest captured graph size >= the token count
 
 All compute runs in the library's sm_103a kernels; tensors are caller-owned CUDA tensors.
@@ -14,8 +16,10 @@ from ._binding import (Dims, RbError, EBIT_ATTN_META, EBIT_BLOCK_ID, EBIT_NUM_CO
                        EBIT_TOKEN_SUM, LIB_PATH, gather_rows, kv_write, launch_count, lib,
                        pad_for_graph, paged_attention, prepare_inputs, status_string,
                        workspace_size)
+from ._binding import EBIT_BATCH_ID, EBIT_BATCH_SIZE
+from .persistent_batch import PersistentBatch, batch_workspace_size
 from .step import StepBuffers, run_step
 
 __all__ = ["Dims", "RbError", "gather_rows", "kv_write", "launch_count", "lib", "pad_for_graph",
            "paged_attention", "prepare_inputs", "status_string", "workspace_size", "StepBuffers",
-           "run_step", "LIB_PATH"]
+           "run_step", "LIB_PATH", "PersistentBatch", "batch_workspace_size"]

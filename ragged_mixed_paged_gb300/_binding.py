@@ -30,6 +30,8 @@ EBIT_SLOT = 0x020
 EBIT_ROW_INDEX = 0x040
 EBIT_ATTN_META = 0x080
 EBIT_TIMEOUT = 0x100
+EBIT_BATCH_ID = 0x200
+EBIT_BATCH_SIZE = 0x400
 
 
 class RbError(RuntimeError):
@@ -42,6 +44,25 @@ class rb_dims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "block_size", "num_q_heads", "num_kv_heads", "head_dim", "max_num_reqs", "max_model_len",
         "max_blocks_per_req", "num_blocks", "null_block")]
+
+
+class rb_batch(ctypes.Structure):
+    _fields_ = [("max_num_reqs", ctypes.c_int32), ("max_model_len", ctypes.c_int32),
+                ("max_blocks_per_req", ctypes.c_int32), ("reserved", ctypes.c_int32)] + [
+        (n, ctypes.c_void_p) for n in (
+            "d_req_id", "d_token_table", "d_num_tokens", "d_num_prompt", "d_num_computed",
+            "d_block_table", "d_num_blocks", "d_num_rows")]
+
+
+class rb_batch_update(ctypes.Structure):
+    _fields_ = [("num_scheduled", ctypes.c_int32), ("num_new", ctypes.c_int32),
+                ("num_cached", ctypes.c_int32), ("reserved", ctypes.c_int32)] + [
+        (n, ctypes.c_void_p) for n in (
+            "d_sched_req_id", "d_sched_num_tokens", "d_new_req_id", "d_new_num_computed",
+            "d_new_num_prompt", "d_new_token_start", "d_new_tokens", "d_new_block_start",
+            "d_new_blocks", "d_cached_req_id", "d_cached_num_computed", "d_cached_replace",
+            "d_cached_token_start", "d_cached_tokens", "d_cached_block_start",
+            "d_cached_blocks")]
 
 
 def _load():
@@ -67,6 +88,9 @@ def _load():
                                               ctypes.c_float, P, P, ctypes.c_size_t, P, P,
                                               ctypes.POINTER(ctypes.c_void_p), I32]),
         "rb_gather_rows": (I32, [I32, I32, I32, P, P, P, P, P]),
+        "rb_batch_update_workspace_size": (I32, [I32, ctypes.POINTER(ctypes.c_size_t)]),
+        "rb_batch_apply_update": (I32, [ctypes.POINTER(rb_batch), ctypes.POINTER(rb_batch_update),
+                                        P, P, P, ctypes.c_size_t, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)

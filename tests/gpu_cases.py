@@ -47,14 +47,35 @@ class _Lazy:
         return a if dtype is None else a.astype(dtype)
 
 
+def config4_layouts(num_steps):
+    """The chunked-prefill stream laid out by the oracle's persistent batch, step by step:
+    yields (step index, scheduler step, oracle InputBatch after the update)."""
+    from oracle.persistent_batch import InputBatch
+
+    stream = wl.MixedChunkStream()
+    d = stream.dims
+    batch = InputBatch(d.max_num_reqs, d.max_model_len, d.max_blocks_per_req)
+    for s in range(num_steps):
+        step = stream.next_step()
+        batch.apply(step)
+        yield s, step, batch
+
+
+def spec_of_layout(name, dims, step, batch, seed):
+    cols = batch.columns(step.scheduled)
+    tok, blk = batch.tables()
+    return wl.spec_from_columns(name, dims, cols["num_computed"], cols["num_scheduled"],
+                                cols["num_prompt"], tok, blk, seed)
+
+
 @functools.lru_cache(maxsize=1)
 def config4_specs(steps=(0, 1, 57, 99)):
     out = {}
-    sim = wl.MixedChunkSimulator()
-    for s in range(max(steps) + 1):
-        spec = sim.next_step()
+    dims = wl.MixedChunkStream().dims
+    for s, step, batch in config4_layouts(max(steps) + 1):
         if s in steps:
-            out[s] = spec
+            out[s] = spec_of_layout(f"chunked-prefill mix step {s}", dims, step, batch,
+                                    4000 * 1000 + s)
     return out
 
 

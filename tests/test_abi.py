@@ -130,3 +130,50 @@ def test_gather_rows_host_checks(lib):
     assert L.rb_gather_rows(2, 4096, 8, MISALIGNED, FAKE, FAKE, None, None) == 1
     assert L.rb_gather_rows(0, 4096, 8, None, None, None, None, None) == 0
     assert L.rb_gather_rows(-1, 4096, 8, FAKE, FAKE, FAKE, None, None) == 1
+
+
+def _batch(lib, NR=8, **kw):
+    b = lib.rb_batch(NR, 64, 8, 0, *([FAKE.value] * 8))
+    for k, v in kw.items():
+        setattr(b, k, v)
+    return b
+
+
+def _update(lib, S=2, NN=1, NC=1, **kw):
+    u = lib.rb_batch_update(S, NN, NC, 0, *([FAKE.value] * 16))
+    for k, v in kw.items():
+        setattr(u, k, v)
+    return u
+
+
+def test_batch_update_host_checks(lib):
+    L = lib.lib
+    n = ctypes.c_size_t(0)
+    assert L.rb_batch_update_workspace_size(8, ctypes.byref(n)) == 0 and n.value > 0
+    small = n.value
+    assert L.rb_batch_update_workspace_size(4096, ctypes.byref(n)) == 0 and n.value > small
+    assert L.rb_batch_update_workspace_size(4097, ctypes.byref(n)) == 5
+    assert L.rb_batch_update_workspace_size(0, ctypes.byref(n)) == 1
+    assert L.rb_batch_update_workspace_size(8, None) == 1
+
+    def call(b, u, ws_bytes=small, num_sched=FAKE, err=FAKE, ws=FAKE):
+        return L.rb_batch_apply_update(ctypes.byref(b) if b is not None else None,
+                                       ctypes.byref(u) if u is not None else None,
+                                       num_sched, None, ws, ws_bytes, err, None)
+
+    assert call(None, _update(lib)) == 1
+    assert call(_batch(lib), None) == 1
+    assert call(_batch(lib, NR=4097), _update(lib)) == 5
+    assert call(_batch(lib, reserved=1), _update(lib)) == 1
+    assert call(_batch(lib, d_num_rows=None), _update(lib)) == 1
+    assert call(_batch(lib), _update(lib, S=9, NN=1, NC=1)) == 2        # S > max_num_reqs
+    assert call(_batch(lib), _update(lib, S=1, NN=2, NC=0)) == 1        # NN > S
+    assert call(_batch(lib), _update(lib, S=1, NN=0, NC=2)) == 1        # NC > S
+    assert call(_batch(lib), _update(lib, S=-1, NN=0, NC=0)) == 1
+    assert call(_batch(lib), _update(lib, d_new_tokens=None)) == 1
+    assert call(_batch(lib), _update(lib, d_cached_replace=None)) == 1
+    assert call(_batch(lib), _update(lib, d_sched_req_id=None)) == 1
+    assert call(_batch(lib), _update(lib), num_sched=None) == 1
+    assert call(_batch(lib), _update(lib), err=None) == 1
+    assert call(_batch(lib), _update(lib), ws=MISALIGNED) == 1
+    assert call(_batch(lib), _update(lib), ws_bytes=small - 1) == 2

@@ -266,34 +266,76 @@ def batch_from_lists(num_computed, num_scheduled, *, block_size=16, num_q_heads=
 
 
 # --------------------------------------------------------------------------- #
-# chunked-prefill mixed workload: a persistent batch evolved over many steps
+# chunked-prefill mixed workload: a request stream, one scheduler output per step
 # --------------------------------------------------------------------------- #
+@dataclass
+class NewRequest:
+    """A request entering the persistent batch with its whole state."""
+
+    req_id: int
+    num_computed: int
+    num_prompt: int
+    tokens: np.ndarray   # int32 history known so far (prompt, then any outputs)
+    blocks: np.ndarray   # int32 page ids of the request's first len(blocks) pages
+
+
+@dataclass
+class CachedDelta:
+    """What a resident request adds this step."""
+
+    req_id: int
+    num_computed: int
+    new_tokens: np.ndarray            # int32, appended to the request's history
+    new_blocks: np.ndarray            # int32, appended to its page row (or the whole row)
+    replace_blocks: bool = False      # resumed from preemption: the page row is replaced
+
+
+@dataclass
+class SchedulerStep:
+    """One step's scheduler output, keyed by request id (no batch rows in it)."""
+
+    scheduled: "dict"                 # req_id -> tokens scheduled this step (insertion order)
+    new: List[NewRequest] = field(default_factory=list)
+    cached: List[CachedDelta] = field(default_factory=list)
+
+    @property
+    def num_tokens(self) -> int:
+        return int(sum(self.scheduled.values()))
+
+
 @dataclass
 class _Req:
     uid: int
     kind: str  # "chunk" or "decode"
     computed: int
     prompt_len: int
-    tokens: np.ndarray
+    tokens: np.ndarray      # every token this request will ever show (drawn at arrival)
+    sent: int = 0           # history tokens already handed to the batch
     pages: List[int] = field(default_factory=list)
 
 
-class MixedChunkSimulator:
-    """Persistent-batch harness for the 8192-token-budget chunked-prefill workload.
+class MixedChunkStream:
+    """Request stream of the 8192-token-budget chunked-prefill workload.
 
-    The batch starts with 4 chunked-prefill rows (chunks of U[1024, 2048] tokens on top of
-    U[0, 16384] prior context) and 128 decode rows (context U[256, 32768]).  Every row finishes
-    with probability 5% per step (or when it nears the model length); a fresh request of the same
-    kind arrives one step later.  Finished rows leave holes: arrivals fill the lowest holes first,
-    then append at the tail, and the remaining holes are closed by moving tail rows down
-    (condense).  Page tables grow as sequences cross page boundaries.  Chunk lengths are drawn
-    first and then shrunk in proportion until the step's total fits the token budget.
+    It starts with 4 chunked-prefill requests (chunks of U[1024, 2048] tokens on top of
+    U[0, 16384] prior context, prompts U[4096, 24576] tokens longer) and 128 decodes (context
+    U[256, 32768]).  A chunked prefill leaves when its prompt is done; every request leaves
+    with probability 5% per step (or near the model length); a fresh request of the same kind
+    arrives one step later.  A running decode is preempted with probability 1% per step: it
+    sits out one step and then comes back as a new request carrying its history; with another
+    1% its page row is replaced by fresh pages.  Chunk lengths are drawn first and then shrunk
+    in proportion until the step fits the token budget.
+
+    Each step is emitted as a ``SchedulerStep`` keyed by request id; which batch row holds a
+    request is the runner's business, not the stream's.
     """
 
     BUDGET = 8192
     N_CHUNK = 4
     N_DECODE = 128
     FINISH_P = 0.05
+    PREEMPT_P = 0.01
+    REPLACE_P = 0.01
 
     def __init__(self, seed: int = 4000, num_blocks: int = 180_001, max_model_len: int = 65536,
                  max_num_reqs: int = 160):
@@ -303,18 +345,17 @@ class MixedChunkSimulator:
                          max_num_reqs=max_num_reqs, max_model_len=max_model_len,
                          max_blocks_per_req=max_model_len // 16, num_blocks=num_blocks)
         self.pool = PagePool(num_blocks, 0, self.rng)
-        self.rows: List[Optional[_Req]] = []
+        self.running: List[_Req] = []
         self.arrivals: List[str] = []
+        self.resuming: List[_Req] = []
         self.next_uid = 0
         self.step_index = 0
-        self.moves = 0
-        self.token_table = np.zeros((max_num_reqs, max_model_len), dtype=np.int32)
-        self.block_table = np.full((max_num_reqs, self.dims.max_blocks_per_req), -1, dtype=np.int32)
+        self.fresh: List[_Req] = []
         for kind in ["chunk"] * self.N_CHUNK + ["decode"] * self.N_DECODE:
-            self.rows.append(self._fresh(kind))
-            self._install(len(self.rows) - 1, self.rows[-1])
+            self.running.append(self._draw(kind))
+        self.fresh = list(self.running)
 
-    def _fresh(self, kind: str) -> _Req:
+    def _draw(self, kind: str) -> _Req:
         M = self.dims.max_model_len
         if kind == "chunk":
             c = int(self.rng.integers(0, 16384, endpoint=True))
@@ -327,88 +368,95 @@ class MixedChunkSimulator:
         self.next_uid += 1
         return r
 
-    def _install(self, row: int, r: _Req) -> None:
-        self.token_table[row, :] = r.tokens
-        self.block_table[row, :] = -1
-        if r.pages:
-            self.block_table[row, :len(r.pages)] = r.pages
-
-    def _clear(self, row: int) -> None:
-        self.token_table[row] = 0
-        self.block_table[row] = -1
-        self.rows[row] = None
-
-    def _update_states(self) -> None:
+    def _retire(self) -> None:
+        """Requests that finished or were preempted after the previous step leave."""
         M = self.dims.max_model_len
-        holes, finished = [], []
-        for i, r in enumerate(self.rows):
-            if r.computed + 2048 >= M or self.rng.random() < self.FINISH_P:
+        keep, finished, preempted = [], [], []
+        for r in self.running:
+            done = (r.kind == "chunk" and r.computed >= r.prompt_len) or \
+                r.computed + 2048 >= M or self.rng.random() < self.FINISH_P
+            if done:
                 self.pool.give_back(r.pages)
-                self._clear(i)
-                holes.append(i)
                 finished.append(r.kind)
-        for kind in self.arrivals:
-            r = self._fresh(kind)
-            if holes:
-                row = holes.pop(0)
-                self.rows[row] = r
+            elif r.kind == "decode" and self.rng.random() < self.PREEMPT_P:
+                self.pool.give_back(r.pages)
+                r.pages, r.sent = [], 0
+                preempted.append(r)
             else:
-                self.rows.append(r)
-                row = len(self.rows) - 1
-            self._install(row, r)
-        self.arrivals = finished
-        # condense: close the remaining holes with rows taken from the tail
-        while holes:
-            last = len(self.rows) - 1
-            if self.rows[last] is None:
-                self.rows.pop()
-                holes.remove(last)
-                continue
-            h = holes.pop(0)
-            self.token_table[h] = self.token_table[last]
-            self.block_table[h] = self.block_table[last]
-            self.rows[h] = self.rows[last]
-            self._clear(last)
-            self.rows.pop()
-            self.moves += 1
+                keep.append(r)
+        self.fresh = [self._draw(kind) for kind in self.arrivals] + self.resuming
+        self.running = keep + self.fresh
+        self.arrivals, self.resuming = finished, preempted
 
-    def next_step(self) -> BatchSpec:
+    def next_step(self) -> SchedulerStep:
         if self.step_index > 0:
-            self._update_states()
-        q = [int(self.rng.integers(1024, 2048, endpoint=True)) if r.kind == "chunk" else 1
-             for r in self.rows]
-        chunk_idx = [i for i, r in enumerate(self.rows) if r.kind == "chunk"]
+            self._retire()
+        fresh = {r.uid for r in self.fresh}
+        replace = {r.uid for r in self.running
+                   if r.uid not in fresh and r.kind == "decode" and self.rng.random() < self.REPLACE_P}
+        q = []
+        for r in self.running:
+            if r.kind == "chunk":
+                q.append(int(self.rng.integers(1024, 2048, endpoint=True)))
+            else:
+                q.append(1)
+        chunk_idx = [i for i, r in enumerate(self.running) if r.kind == "chunk"]
         total = sum(q)
         if total > self.BUDGET and chunk_idx:
             room = self.BUDGET - (total - sum(q[i] for i in chunk_idx))
             scale = room / sum(q[i] for i in chunk_idx)
             for i in chunk_idx:
                 q[i] = max(1, int(q[i] * scale))
-        for i, r in enumerate(self.rows):
-            need = pages_for(r.computed + q[i], self.dims.block_size)
-            if need > len(r.pages):
-                r.pages.extend(self.pool.take(need - len(r.pages)))
-                self.block_table[i, :len(r.pages)] = r.pages
-        spec = BatchSpec(name=f"chunked-prefill mix step {self.step_index}", dims=self.dims,
-                         num_computed=np.array([r.computed for r in self.rows], np.int32),
-                         num_scheduled=np.array(q, np.int32),
-                         num_reqs_padded=len(self.rows), num_tokens_padded=int(sum(q)),
-                         token_table=self.token_table.copy(), block_table=self.block_table.copy(),
-                         hidden_size=4096, seed=self.seed * 1000 + self.step_index,
-                         num_prompt=np.array([r.prompt_len for r in self.rows], np.int32))
-        for i, r in enumerate(self.rows):
+        for i, r in enumerate(self.running):  # the last chunk of a prompt stops at its end
+            if r.kind == "chunk" and r.computed < r.prompt_len:
+                q[i] = min(q[i], r.prompt_len - r.computed)
+
+        step = SchedulerStep(scheduled={})
+        B = self.dims.block_size
+        for i, r in enumerate(self.running):
+            step.scheduled[r.uid] = q[i]
+            need_tokens = max(r.computed + q[i], r.prompt_len if r.uid in fresh else 0)
+            if r.uid in fresh:
+                r.pages = self.pool.take(pages_for(r.computed + q[i], B))
+                r.sent = need_tokens
+                step.new.append(NewRequest(r.uid, r.computed, r.prompt_len,
+                                           r.tokens[:r.sent].copy(),
+                                           np.array(r.pages, np.int32)))
+                continue
+            if r.uid in replace:
+                self.pool.give_back(r.pages)
+                r.pages = []
+            add = self.pool.take(pages_for(r.computed + q[i], B) - len(r.pages))
+            new_tokens = r.tokens[r.sent:need_tokens].copy() if need_tokens > r.sent else \
+                np.zeros(0, np.int32)
+            r.sent = max(r.sent, need_tokens)
+            r.pages = r.pages + add
+            step.cached.append(CachedDelta(
+                r.uid, r.computed, new_tokens,
+                np.array(r.pages if r.uid in replace else add, np.int32),
+                replace_blocks=r.uid in replace))
+        for i, r in enumerate(self.running):
             r.computed += q[i]
-            if r.kind == "decode":
-                r.prompt_len = r.computed
         self.step_index += 1
-        return spec
+        return step
 
 
-def config4_steps(num_steps: int = 100, seed: int = 4000) -> Iterator[BatchSpec]:
-    sim = MixedChunkSimulator(seed=seed)
+def config4_stream(num_steps: int = 100, seed: int = 4000) -> Iterator[SchedulerStep]:
+    stream = MixedChunkStream(seed=seed)
     for _ in range(num_steps):
-        yield sim.next_step()
+        yield stream.next_step()
 
+
+def spec_from_columns(name: str, dims: Dims, num_computed, num_scheduled, num_prompt,
+                      token_table: np.ndarray, block_table: np.ndarray, seed: int,
+                      hidden_size: int = 4096) -> BatchSpec:
+    """A step description from a persistent batch's row-order columns (no padding)."""
+    num_scheduled = np.asarray(num_scheduled, np.int32)
+    return BatchSpec(name=name, dims=dims, num_computed=np.asarray(num_computed, np.int32),
+                     num_scheduled=num_scheduled, num_reqs_padded=int(num_scheduled.shape[0]),
+                     num_tokens_padded=int(num_scheduled.sum(dtype=np.int64)),
+                     token_table=token_table, block_table=block_table, hidden_size=hidden_size,
+                     seed=seed, num_prompt=np.asarray(num_prompt, np.int32))
 
 # --------------------------------------------------------------------------- #
 # activations and the paged pool (torch; CPU or CUDA)
@@ -496,3 +544,68 @@ def device_tables(spec: BatchSpec, device):
 def with_padding(spec: BatchSpec, num_reqs_padded: int, num_tokens_padded: int) -> BatchSpec:
     return dataclasses.replace(spec, num_reqs_padded=num_reqs_padded,
                                num_tokens_padded=num_tokens_padded)
+
+
+class RandomRequestStream:
+    """Small seeded request streams for fuzzing the batch update: arrivals, finishes, requests
+    the scheduler skips for a step (they come back later as new requests with their history),
+    ids resubmitted while still resident, deltas with appended tokens and page ids, and
+    replaced page rows.  Request-level only: it never decides which row holds what."""
+
+    def __init__(self, seed: int, max_live: int = 12, max_model_len: int = 64,
+                 max_blocks: int = 8, p_finish: float = 0.2, p_skip: float = 0.1,
+                 p_resubmit: float = 0.05, p_replace: float = 0.1):
+        self.rng = np.random.default_rng(seed)
+        self.max_live, self.M, self.MB = max_live, max_model_len, max_blocks
+        self.max_rows = max_live
+        self.p = dict(finish=p_finish, skip=p_skip, resubmit=p_resubmit, replace=p_replace)
+        self.live: dict = {}     # id -> [computed, prompt, tokens list, blocks list]
+        self.parked: dict = {}   # skipped last step: id -> state, back as new next time
+        self.next_id = 0
+
+    def _fresh_state(self):
+        n = int(self.rng.integers(1, self.M // 2))
+        toks = [int(x) for x in self.rng.integers(0, VOCAB, size=n)]
+        blocks = [int(x) for x in self.rng.integers(1, 10_000, size=int(self.rng.integers(0, self.MB // 2 + 1)))]
+        return [int(self.rng.integers(0, n + 1)), n, toks, blocks]
+
+    def next_step(self) -> SchedulerStep:
+        rng, p = self.rng, self.p
+        step = SchedulerStep(scheduled={})
+        back, self.parked = self.parked, {}
+        for i, st in list(self.live.items()):
+            u = rng.random()
+            if u < p["finish"] or len(st[2]) >= self.M - 4 or len(st[3]) >= self.MB - 2:
+                del self.live[i]
+            elif u < p["finish"] + p["skip"]:
+                self.parked[i] = self.live.pop(i)
+        for i, st in back.items():  # skipped last step: the batch dropped it, resend it whole
+            self.live[i] = st
+        arrivals = int(rng.integers(0, 4))
+        for _ in range(arrivals):
+            if len(self.live) + len(self.parked) >= self.max_live:
+                break
+            self.live[self.next_id] = self._fresh_state()
+            self.next_id += 1
+        fresh = set(back) | set(range(self.next_id - arrivals, self.next_id))
+        for i, st in self.live.items():
+            step.scheduled[i] = int(rng.integers(1, 6))
+            if i not in fresh and rng.random() < p["resubmit"]:
+                st[:] = self._fresh_state()
+                fresh.add(i)
+            if i in fresh:
+                step.new.append(NewRequest(i, st[0], st[1], np.array(st[2], np.int32),
+                                           np.array(st[3], np.int32)))
+                continue
+            if rng.random() < 0.3:
+                continue  # resident and unchanged: no delta this step
+            toks = [int(x) for x in rng.integers(0, VOCAB, size=int(rng.integers(0, 4)))]
+            replace = rng.random() < p["replace"]
+            nb = int(rng.integers(1, self.MB // 2 + 1)) if replace else int(rng.integers(0, 3))
+            blocks = [int(x) for x in rng.integers(1, 10_000, size=nb)]
+            st[0] = min(len(st[2]) + len(toks), st[0] + int(rng.integers(0, 4)))
+            st[2] = st[2] + toks
+            st[3] = blocks if replace else st[3] + blocks
+            step.cached.append(CachedDelta(i, st[0], np.array(toks, np.int32),
+                                           np.array(blocks, np.int32), replace_blocks=replace))
+        return step
