@@ -79,15 +79,15 @@ def chunked_mix_step0(rank: int, oracle_layout: bool = False):
                                 seed=(4000 + 7919 * rank) * 1000)
 
 
-def make_spec(config: int, rank: int = 0, oracle_layout: bool = False):
+def make_spec(config: int, rank: int = 0, oracle_layout: bool = False, manager_ratio: int = 1):
     import workloads as wl
 
     if config == 1:
         return wl.config1(step=rank)
     if config == 2:
-        return wl.config2(step=rank)
+        return wl.config2(step=rank, manager_ratio=manager_ratio)
     if config == 3:
-        return wl.config3(step=rank)
+        return wl.config3(step=rank, manager_ratio=manager_ratio)
     if config == 4:
         return chunked_mix_step0(rank, oracle_layout)
     if config == 5:
@@ -107,6 +107,7 @@ def workload_name(spec, config):
         "num_tokens_padded": spec.num_tokens_padded, "q_heads": d.num_q_heads,
         "kv_heads": d.num_kv_heads, "head_dim": d.head_dim, "block_size": d.block_size,
         "hidden": spec.hidden_size, "kv_pages": d.num_blocks,
+        "kernel_pages_per_table_entry": d.kernel_blocks_per_manager_block,
         "l2": "flushed before every timed step (512 MiB write, outside the events)",
     }
 
@@ -353,7 +354,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream()
-    spec = make_spec(args.config, rank)
+    spec = make_spec(args.config, rank, manager_ratio=args.manager_ratio)
     d = spec.dims
     tens = wl.make_tensors(spec, device=dev)
     tables = wl.device_tables(spec, dev)
@@ -548,6 +549,117 @@ def measure_e2e(spec, tens, buf, dev, args, flush, world):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
 
 
+def run_trajectory(args, rank, world, local):
+    """The chunked-prefill mix as a stream: every step merges the scheduler's deltas into the
+    device-resident persistent batch (packet copy + rb_batch_apply_update), then runs the step
+    on the rows it produced.  Eager launches (the shapes change every step)."""
+    import dataclasses
+
+    import torch
+
+    import workloads as wl
+    import ragged_mixed_paged_gb300 as rb
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = wl.MixedChunkStream(seed=4000 + 7919 * rank)
+    d = stream.dims
+    dims = rb.Dims.of(d)
+    steps = [stream.next_step() for _ in range(args.warmup + args.steps)]
+    nmax, rmax = stream.BUDGET, d.max_num_reqs
+    g = torch.Generator(device=dev).manual_seed(4000 + rank)
+    bf = torch.bfloat16
+    rnd = lambda *shape: torch.randn(*shape, generator=g, device=dev, dtype=torch.float32).to(bf)
+    q, k, v = (rnd(nmax, d.num_q_heads, d.head_dim), rnd(nmax, d.num_kv_heads, d.head_dim),
+               rnd(nmax, d.num_kv_heads, d.head_dim))
+    hidden = rnd(nmax, 4096)
+    k_cache = torch.empty((d.num_blocks * d.block_size, d.num_kv_heads, d.head_dim), dtype=bf,
+                          device=dev).normal_(generator=g)
+    v_cache = torch.empty_like(k_cache).normal_(generator=g)
+    batch = rb.PersistentBatch(d.max_num_reqs, d.max_model_len, d.max_blocks_per_req, device=dev)
+    buf = rb.StepBuffers.allocate(dims, rmax, rmax, nmax, nmax, batch.tables(), q, k, v, hidden,
+                                  k_cache, v_cache)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    host_rows = torch.empty((rmax, 4096), dtype=bf).pin_memory()
+    host_scalars = torch.empty(4, dtype=torch.int32).pin_memory()
+    rec, tokens, h2d, d2h = [], 0, 0, 0
+    sampler = ClockSampler(local)
+    launches0 = None
+    barrier(world)
+    for i, step in enumerate(steps):
+        if i == args.warmup:
+            torch.cuda.synchronize()
+            sampler.start()
+            launches0 = rb.launch_count()
+        flush.zero_()
+        ev = [E() for _ in range(5)]
+        ev[0].record()
+        nbytes = batch.apply(step, copied_event=ev[1])
+        ev[2].record()
+        R, N = batch.num_reqs, batch.num_tokens_scheduled
+        b = dataclasses.replace(buf, num_reqs=R, num_reqs_padded=R, num_tokens=N,
+                                num_tokens_padded=N, q=q[:N], k=k[:N], v=v[:N], hidden=hidden[:N],
+                                attn_out=buf.attn_out[:N])
+        rb.run_step(b)
+        ev[3].record()
+        host_rows[:R].copy_(b.rows_out[:R], non_blocking=True)
+        host_scalars.copy_(b.meta["scalars"], non_blocking=True)
+        ev[4].record()
+        torch.cuda.synchronize()
+        if int(host_scalars[3]) != 0 or int(batch.error_word.item()) != 0:
+            raise SystemExit(f"step {i}: error words {int(host_scalars[3]):#x} "
+                             f"{int(batch.error_word.item()):#x}")
+        if i >= args.warmup:
+            rec.append([ev[0].elapsed_time(e) for e in ev[1:]])
+            tokens += N
+            h2d += nbytes
+            d2h += R * 4096 * 2 + 16
+    launches = rb.launch_count() - launches0
+    clocks = sampler.stop()
+    barrier(world)
+    rec = list(zip(*rec))  # per mark: copy done | update done | step done | results read
+    pack_copy = statistics.mean(rec[0])
+    update = statistics.mean(b2 - b1 for b1, b2 in zip(rec[0], rec[1]))
+    step_ms = statistics.mean(b3 - b2 for b2, b3 in zip(rec[1], rec[2]))
+    e2e_ms = statistics.mean(rec[3])
+    dev_ms = update + step_ms
+    total = reduce_over_ranks(float(tokens), "sum", world, dev)
+    dev_ms = reduce_over_ranks(dev_ms, "max", world, dev)
+    e2e_ms = reduce_over_ranks(e2e_ms, "max", world, dev)
+    K = args.steps
+    # what the update replaces: uploading the whole token and page tables every step
+    tt = torch.empty((rmax, d.max_model_len), dtype=torch.int32).pin_memory()
+    bt = torch.empty((rmax, d.max_blocks_per_req), dtype=torch.int32).pin_memory()
+    gt, gb = torch.empty_like(tt, device=dev), torch.empty_like(bt, device=dev)
+    a, z = E(), E()
+    a.record()
+    for _ in range(5):
+        gt.copy_(tt, non_blocking=True)
+        gb.copy_(bt, non_blocking=True)
+    z.record()
+    torch.cuda.synchronize()
+    if rank == 0:
+        print(json.dumps({
+            "metric": METRIC + " (stream of steps with the batch update)",
+            "value": total / (dev_ms * K / 1000.0),
+            "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+            "ms_per_step": dev_ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic request stream",
+            "config": {"workload": f"chunked-prefill mix stream, steps {args.warmup}.."
+                                   f"{args.warmup + K - 1}", "l2": "512 MiB flush per step",
+                       "launch": "eager"},
+            "components_ms": {"pack_and_packet_h2d": pack_copy, "batch_update": update,
+                              "step": step_ms},
+            "e2e": {"value": total / (e2e_ms * K / 1000.0), "unit": UNIT, "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d / K, "d2h_bytes_per_step": d2h / K},
+            "full_table_h2d_ms": a.elapsed_time(z) / 5,
+            "full_table_bytes": tt.numel() * 4 + bt.numel() * 4,
+            "gpu_launches": launches, "clocks": clocks}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -559,12 +671,20 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step from Python instead of replaying a captured graph")
+    ap.add_argument("--manager-ratio", type=int, default=1,
+                    help="--config 2/3: page tables of manager blocks of this many kernel pages")
+    ap.add_argument("--trajectory", action="store_true",
+                    help="--config 4 only: time a stream of steps, each with its batch update")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.trajectory:
+        if args.config != 4:
+            raise SystemExit("--trajectory needs --config 4")
+        run_trajectory(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

@@ -81,6 +81,17 @@ typedef struct rb_dims {
   int32_t max_blocks_per_req; /* MB: columns of the page table */
   int32_t num_blocks;         /* physical pages in the pool, the null page included */
   int32_t null_block;         /* reserved page id that receives every padding token */
+  int32_t kernel_blocks_per_manager_block; /* r: page-table entries are manager blocks of
+                                 r * block_size tokens ("vLLM 源码完全拆解（五）…", "混合 KV
+                                 Cache：一条请求不止一张页表": a 32-token manager block seen by a
+                                 16-token kernel expands into two kernel pages, manager ids
+                                 [0, 1, 2] -> kernel ids [0 .. 5]); manager id m covers kernel
+                                 pages m*r .. m*r + r - 1, so logical kernel page j of a row is
+                                 block_table[i, j / r] * r + j % r.  1 (or 0) = the table holds
+                                 kernel pages.  With r > 1: num_blocks and null_block are in
+                                 kernel pages and multiples of r, max_blocks_per_req counts
+                                 table entries (a row spans max_blocks_per_req * r kernel pages)
+                                 and the whole manager block null_block / r is reserved. */
 } rb_dims;
 
 /* Human-readable name of a status code (static string). */

@@ -4,7 +4,10 @@ Plain, slow, obviously correct restatements of what the step computes, written
 from the pages' prose and worked examples:
 
 * ``metadata``  — query_start_loc, seq_lens, positions, input_ids, slot_mapping,
-  logits_indices and the padding of a step to a captured graph size;
+  logits_indices, phase flags, the manager-to-kernel page expansion and the padding of a step
+  to a captured graph size;
+* ``persistent_batch`` — the runner's per-step merge of scheduler deltas into the rows of
+  the persistent batch (remove, append, install, condense);
 * ``kv_cache``  — the paged K/V write by slot_mapping;
 * ``attention`` — per-request dense causal GQA attention in float64 over an
   unpaged, contiguous copy of each request's keys and values;
@@ -21,10 +24,11 @@ print, closed forms, special cases that reduce to library routines, and brute
 force over tiny inputs.
 """
 from .metadata import (prepare_inputs, pad_for_graph, padded_layout_tokens,
-                       req_indices_and_query_pos, request_flags)
+                       req_indices_and_query_pos, request_flags, map_to_kernel_blocks)
+from .persistent_batch import InputBatch
 from .kv_cache import kv_write
 from .attention import paged_attention
 from .gather import gather_rows
 
-__all__ = ["prepare_inputs", "request_flags", "pad_for_graph", "padded_layout_tokens", "req_indices_and_query_pos",
+__all__ = ["prepare_inputs", "request_flags", "map_to_kernel_blocks", "InputBatch", "pad_for_graph", "padded_layout_tokens", "req_indices_and_query_pos",
            "kv_write", "paged_attention", "gather_rows"]

@@ -21,6 +21,10 @@ Sources (page title, then section):
   - "8.5.0.5 pad_for_cudagraph 的实现" (smallest captured size >= the token count).
 * "04 · 模型执行与 CUDA Graph", "5. 关键细节与坑": padding tokens use the null block (block 0),
   which never holds real cache.
+* same GPUModelRunner page, "混合 KV Cache：一条请求不止一张页表": when the manager's block is
+  larger than the kernel's, each manager block id expands into several kernel block ids
+  (32-token manager blocks over 16-token kernel pages: [0, 1, 2] -> [0, 1, 2, 3, 4, 5]), and
+  the slot map works on the expanded ids.
 * "变长批处理与一次混合前向", "布局与元数据" and "为什么不填充".
 
 Readings where the pages are silent: padded requests get seq_len 0 and the empty interval at
@@ -45,11 +49,24 @@ def req_indices_and_query_pos(num_scheduled: Sequence[int]):
     return np.array(req_indices, np.int64), np.array(query_pos, np.int64)
 
 
+def map_to_kernel_blocks(manager_ids: Sequence[int], kernel_blocks_per_manager_block: int):
+    """Kernel block ids of a row of manager block ids ("混合 KV Cache：一条请求不止一张页表"):
+    manager block m of r kernel blocks becomes kernel blocks r*m, r*m + 1, ..., r*m + r - 1,
+    in order, so [0, 1, 2] with r = 2 is [0, 1, 2, 3, 4, 5] as the page prints."""
+    r = int(kernel_blocks_per_manager_block)
+    out = []
+    for m in manager_ids:
+        for j in range(r):
+            out.append(int(m) * r + j)
+    return out
+
+
 def prepare_inputs(*, block_size: int, null_block: int, token_table: np.ndarray,
                    block_table: np.ndarray, num_computed: Sequence[int],
                    num_scheduled: Sequence[int], num_reqs_padded: int | None = None,
                    num_tokens_padded: int | None = None,
-                   num_prompt: Sequence[int] | None = None) -> Dict[str, np.ndarray]:
+                   num_prompt: Sequence[int] | None = None,
+                   kernel_blocks_per_manager_block: int = 1) -> Dict[str, np.ndarray]:
     """Flat step inputs and attention metadata of one batch, as plain loops.
 
     Returns int64 arrays ``query_start_loc [R_pad+1]``, ``seq_lens [R_pad]``,
@@ -57,6 +74,9 @@ def prepare_inputs(*, block_size: int, null_block: int, token_table: np.ndarray,
     ``logits_indices [R_pad]``, ``visible_keys [N]`` (keys each query may read, "4. 注意力读取边界")
     and ints ``max_query_len``, ``max_seq_len``, ``num_actual_tokens``.  With ``num_prompt``
     also ``is_prefilling [R_pad]`` and ``discard_request_mask [R_pad]`` (see request_flags).
+    With ``kernel_blocks_per_manager_block`` r > 1 the rows of ``block_table`` hold manager
+    block ids, expanded to kernel block ids (``map_to_kernel_blocks``) before the slot map;
+    ``block_size`` and ``null_block`` are then the kernel's.
     """
     B = int(block_size)
     R = len(num_scheduled)
@@ -78,13 +98,15 @@ def prepare_inputs(*, block_size: int, null_block: int, token_table: np.ndarray,
 
     positions, input_ids, slots, visible = [], [], [], []
     for i in range(R):
+        kernel_row = (block_table[i] if kernel_blocks_per_manager_block == 1 else
+                      map_to_kernel_blocks(block_table[i], kernel_blocks_per_manager_block))
         c = int(num_computed[i])
         for j in range(int(num_scheduled[i])):
             p = c + j                                     # 第二步
             positions.append(p)
             input_ids.append(int(token_table[i, p]))      # 第三步
             logical_block, offset = p // B, p % B         # Block table 是逐请求的页表
-            slots.append(int(block_table[i, logical_block]) * B + offset)
+            slots.append(int(kernel_row[logical_block]) * B + offset)
             visible.append(c + j + 1)                     # 4. 注意力读取边界
     for t in range(N, N_pad):                              # padding tokens -> the null block
         positions.append(0)

@@ -43,7 +43,7 @@ class RbError(RuntimeError):
 class rb_dims(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "block_size", "num_q_heads", "num_kv_heads", "head_dim", "max_num_reqs", "max_model_len",
-        "max_blocks_per_req", "num_blocks", "null_block")]
+        "max_blocks_per_req", "num_blocks", "null_block", "kernel_blocks_per_manager_block")]
 
 
 class rb_batch(ctypes.Structure):
@@ -113,16 +113,18 @@ class Dims:
     max_blocks_per_req: int
     num_blocks: int
     null_block: int = 0
+    kernel_blocks_per_manager_block: int = 1  # kernel pages per page-table entry
 
     def c(self) -> rb_dims:
         return rb_dims(self.block_size, self.num_q_heads, self.num_kv_heads, self.head_dim,
                        self.max_num_reqs, self.max_model_len, self.max_blocks_per_req,
-                       self.num_blocks, self.null_block)
+                       self.num_blocks, self.null_block, self.kernel_blocks_per_manager_block)
 
     @classmethod
     def of(cls, d) -> "Dims":
         return cls(d.block_size, d.num_q_heads, d.num_kv_heads, d.head_dim, d.max_num_reqs,
-                   d.max_model_len, d.max_blocks_per_req, d.num_blocks, d.null_block)
+                   d.max_model_len, d.max_blocks_per_req, d.num_blocks, d.null_block,
+                   getattr(d, "kernel_blocks_per_manager_block", 1))
 
 
 def _check(fn: str, status: int) -> None:

@@ -67,7 +67,8 @@ __device__ __forceinline__ ReqInfo req_info(const AttnArgs& a, int r) {
   x.q = e - s;
   x.L = a.seq_lens[r];
   x.pages = (x.L + kPage - 1) / kPage;
-  x.ok = s >= 0 && x.q >= 0 && e <= a.N && x.L >= x.q && x.pages <= a.MB;
+  x.ok = s >= 0 && x.q >= 0 && e <= a.N && x.L >= x.q &&
+         x.pages <= static_cast<long long>(a.MB) * a.ratio;
   return x;
 }
 
@@ -187,9 +188,8 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
   if (d.num_kv_heads < 1 || d.num_q_heads < 1 || d.num_q_heads % d.num_kv_heads != 0)
     return RB_ERR_INVALID_ARG;
   if (d.num_q_heads / d.num_kv_heads > 16) return RB_ERR_UNSUPPORTED;
-  if (d.num_blocks < 1 || d.null_block < 0 || d.null_block >= d.num_blocks ||
-      d.max_blocks_per_req < 1 || d.max_num_reqs < 0)
-    return RB_ERR_INVALID_ARG;
+  PageGeom g;
+  if (page_geom_of(d, &g) != RB_OK || d.max_num_reqs < 0) return RB_ERR_INVALID_ARG;
   if (static_cast<long long>(d.num_blocks) * kPage > 0x7fffffffLL) return RB_ERR_CAPACITY;
   if (num_reqs < 0 || num_tokens < 0 || num_tokens_padded < num_tokens) return RB_ERR_INVALID_ARG;
   if (num_reqs > d.max_num_reqs) return RB_ERR_CAPACITY;
@@ -239,6 +239,7 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
   a.MB = d.max_blocks_per_req;
   a.num_blocks = d.num_blocks;
   a.null_block = d.null_block;
+  a.ratio = g.ratio;
   const int sms = max(1, device_sm_count());
   a.target_units = min(kMaxTargetUnits, 32 * sms);
   a.tile_m = use_tc ? 256 : kPrefillTileM;  // tcgen05 units are pairs of 128-row tiles

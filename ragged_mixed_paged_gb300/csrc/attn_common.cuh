@@ -63,6 +63,7 @@ struct AttnArgs {
   float2* part_ml;
   float* part_o;
   int R, N, N_pad, nh, nkv, group, MB, num_blocks, null_block;
+  int ratio;  // kernel pages per page-table entry (manager block)
   int target_units;
   int tile_m;  // query rows per prefill unit (256 on the tcgen05 path, 64 on the mma.sync path)
   int fused_ctas;  // > 0: decode and prefill share one launch of this many CTAs (one per SM)

@@ -130,14 +130,18 @@ __device__ void decode_warp(const CUtensorMap* kmap_p, const CUtensorMap* vmap_p
     // page ids of pages [win, win + 32) held one per lane, the next window prefetched
     const int32_t* bt_row = a.block_table + static_cast<size_t>(r) * a.MB;
     int win = p_begin;
-    int bid = (win + lane < p_end) ? __ldg(bt_row + win + lane) : a.null_block;
-    int bid_next = (win + 32 + lane < p_end) ? __ldg(bt_row + win + 32 + lane) : a.null_block;
+    auto page = [&](int pg) {
+      return pg < p_end ? kernel_page(bt_row, pg, a.ratio, a.num_blocks, a.null_block)
+                        : a.null_block;
+    };
+    int bid = page(win + lane);
+    int bid_next = page(win + 32 + lane);
 
     auto issue = [&](int pg, uint32_t stage) {  // called by the whole warp
       if (pg - win >= 32) {
         win += 32;
         bid = bid_next;
-        bid_next = (win + 32 + lane < p_end) ? __ldg(bt_row + win + 32 + lane) : a.null_block;
+        bid_next = page(win + 32 + lane);
       }
       int id = __shfl_sync(0xffffffffu, bid, pg - win);
       if (lane == 0) {

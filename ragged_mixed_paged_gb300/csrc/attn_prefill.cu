@@ -117,7 +117,7 @@ __global__ void __launch_bounds__(PreCfg<HD>::kWarps * 32)
         const int pg = kt * C::kPagesPerTile + pi;
         int id = a.null_block;  // pages past the sequence: any valid page, zeroed below
         if (pg < pages_r) {
-          id = __ldg(bt_row + pg);
+          id = kernel_page(bt_row, pg, a.ratio, a.num_blocks, a.null_block);
           if (id < 0 || id >= a.num_blocks || id == a.null_block) {
             raise_error(a.err, RB_EBIT_BLOCK_ID);
             id = a.null_block;

@@ -176,8 +176,12 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
     }
     const int32_t* bt_row = a.block_table + static_cast<size_t>(un.r) * a.MB;
     int win = 0;
-    int bid = lane < un.pages ? __ldg(bt_row + lane) : a.null_block;
-    int bid_next = 32 + lane < un.pages ? __ldg(bt_row + 32 + lane) : a.null_block;
+    auto page = [&](int pg) {
+      return pg < un.pages ? kernel_page(bt_row, pg, a.ratio, a.num_blocks, a.null_block)
+                           : a.null_block;
+    };
+    int bid = page(lane);
+    int bid_next = page(32 + lane);
     int ids[2] = {a.null_block, a.null_block};  // page id of this lane for tiles j and j-1
     bool ok = true;
     for (int j = 0; j <= un.n_kt; ++j) {
@@ -186,7 +190,7 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
         if (first - win >= 32) {
           win += 32;
           bid = bid_next;
-          bid_next = win + 32 + lane < un.pages ? __ldg(bt_row + win + 32 + lane) : a.null_block;
+          bid_next = page(win + 32 + lane);
         }
         int id = __shfl_sync(0xffffffffu, bid, first + (lane & 7) - win);
         const int pg = first + (lane & 7);

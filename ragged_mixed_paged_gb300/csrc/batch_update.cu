@@ -472,10 +472,17 @@ extern "C" rb_status rb_batch_apply_update(const rb_batch* batch, const rb_batch
   int cap = 64;
   while (cap < 2 * S) cap <<= 1;
   const size_t smem = plan_smem_bytes(b.max_num_reqs, S, cap);
-  if (smem > 48 * 1024 &&
-      cudaFuncSetAttribute(batch_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           static_cast<int>(smem)) != cudaSuccess)
-    return RB_ERR_CUDA;
+  // opt in once per device to the largest planner footprint (4096 rows, all scheduled)
+  static bool configured[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return RB_ERR_CUDA;
+  if (!configured[dev]) {
+    if (cudaFuncSetAttribute(batch_plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(plan_smem_bytes(kMaxRows, kMaxRows, 2 * kMaxRows))) !=
+        cudaSuccess)
+      return RB_ERR_CUDA;
+    configured[dev] = true;
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   PlanArgs pa;
   pa.b = b;

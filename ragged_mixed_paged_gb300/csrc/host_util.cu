@@ -31,6 +31,18 @@ rb_status last_launch_status() {
   return cudaGetLastError() == cudaSuccess ? RB_OK : RB_ERR_CUDA;
 }
 
+rb_status page_geom_of(const rb_dims& d, PageGeom* g) {
+  const int r = d.kernel_blocks_per_manager_block == 0 ? 1 : d.kernel_blocks_per_manager_block;
+  if (r < 1 || r > 64 || d.num_blocks < 1 || d.null_block < 0 || d.null_block >= d.num_blocks ||
+      d.num_blocks % r != 0 || d.null_block % r != 0 || d.max_blocks_per_req < 1 ||
+      static_cast<long long>(d.max_blocks_per_req) * r > 0x7fffffffLL)
+    return RB_ERR_INVALID_ARG;
+  g->ratio = r;
+  g->num_blocks = d.num_blocks;
+  g->null_block = d.null_block;
+  return RB_OK;
+}
+
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;

@@ -6,7 +6,10 @@
 //   seq_lens[i]     = num_computed[i] + num_scheduled[i]           (0 for padded requests)
 //   positions[t]    = num_computed[r] + (t - query_start_loc[r])   (r = owner of token t)
 //   input_ids[t]    = token_table[r, positions[t]]
-//   slot_mapping[t] = block_table[r, pos / B] * B + pos % B         (padding -> null page)
+//   slot_mapping[t] = page(r, pos / B) * B + pos % B                  (padding -> null page)
+//                     page(r, j) = block_table[r, j / ratio] * ratio + j % ratio: the table
+//                     may hold manager blocks of `ratio` kernel pages ("混合 KV Cache：一条请求
+//                     不止一张页表"); ratio 1 reads kernel pages directly
 //   logits_indices  = query_start_loc[1:] - 1
 //   is_prefilling   = num_computed < num_prompt, discard_request_mask = seq_len < num_prompt
 //                     (optional; "Chunked Prefill：query 很长，但仍只是一段区间")
@@ -27,7 +30,7 @@ constexpr int kTokPerCta = kThreads * kTokPerThread;
 constexpr int kMaxReqs = 16384;
 
 struct PrepArgs {
-  int R, R_pad, N, N_pad, B, M, MB, num_blocks, null_block;
+  int R, R_pad, N, N_pad, B, M, MB, num_blocks, null_block, ratio;
   const int32_t* __restrict__ token_table;
   const int32_t* __restrict__ num_computed;
   const int32_t* __restrict__ num_scheduled;
@@ -99,7 +102,8 @@ __global__ void __launch_bounds__(kThreads) prepare_inputs_kernel(PrepArgs a) {
         const long long len = static_cast<long long>(c) + q;
         if (q < 1) bits |= RB_EBIT_NUM_SCHEDULED;
         if (c < 0) bits |= RB_EBIT_NUM_COMPUTED;
-        if (len > a.M || (len + a.B - 1) / a.B > a.MB) bits |= RB_EBIT_SEQ_LEN;
+        if (len > a.M || (len + a.B - 1) / a.B > static_cast<long long>(a.MB) * a.ratio)
+          bits |= RB_EBIT_SEQ_LEN;
         a.seq_lens[i] = static_cast<int32_t>(len);
         a.logits[i] = s_qsl[i + 1] - 1;
         my_q = max(my_q, q);
@@ -159,7 +163,7 @@ __global__ void __launch_bounds__(kThreads) prepare_inputs_kernel(PrepArgs a) {
     const int j = t - s_qsl[r];
     const int c = a.num_computed[r];
     const long long p = static_cast<long long>(c) + j;
-    if (j < 0 || p < 0 || p >= a.M || p / a.B >= a.MB) {
+    if (j < 0 || p < 0 || p >= a.M || p / a.B >= static_cast<long long>(a.MB) * a.ratio) {
       bits |= RB_EBIT_SEQ_LEN;
       slot[k] = a.null_block * a.B;
       continue;
@@ -167,8 +171,9 @@ __global__ void __launch_bounds__(kThreads) prepare_inputs_kernel(PrepArgs a) {
     const int pp = static_cast<int>(p);
     pos[k] = pp;
     ids[k] = a.token_table[static_cast<size_t>(r) * a.M + pp];
-    const int blk = a.block_table[static_cast<size_t>(r) * a.MB + pp / a.B];
-    if (blk < 0 || blk >= a.num_blocks || blk == a.null_block) {
+    const int blk = kernel_page(a.block_table + static_cast<size_t>(r) * a.MB, pp / a.B,
+                                a.ratio, a.num_blocks, a.null_block);
+    if (blk < 0) {
       bits |= RB_EBIT_BLOCK_ID;
       slot[k] = a.null_block * a.B + pp % a.B;
     } else {
@@ -212,9 +217,9 @@ extern "C" rb_status rb_prepare_inputs(const rb_dims* dims, int32_t num_reqs,
   if (dims == nullptr || d_query_start_loc == nullptr || d_scalars == nullptr)
     return RB_ERR_INVALID_ARG;
   const rb_dims& d = *dims;
+  PageGeom g;
   if (d.block_size < 1 || d.max_num_reqs < 0 || d.max_model_len < 1 ||
-      d.max_blocks_per_req < 1 || d.num_blocks < 1 || d.null_block < 0 ||
-      d.null_block >= d.num_blocks)
+      page_geom_of(d, &g) != RB_OK)
     return RB_ERR_INVALID_ARG;
   if (static_cast<long long>(d.num_blocks) * d.block_size > 0x7fffffffLL) return RB_ERR_CAPACITY;
   if (num_reqs < 0 || num_reqs_padded < num_reqs || num_tokens < 0 ||
@@ -241,7 +246,7 @@ extern "C" rb_status rb_prepare_inputs(const rb_dims* dims, int32_t num_reqs,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(d_scalars + 3, 0, sizeof(int32_t), s) != cudaSuccess) return RB_ERR_CUDA;
   PrepArgs a{num_reqs, num_reqs_padded, num_tokens, num_tokens_padded, d.block_size,
-             d.max_model_len, d.max_blocks_per_req, d.num_blocks, d.null_block,
+             d.max_model_len, d.max_blocks_per_req, d.num_blocks, d.null_block, g.ratio,
              d_token_table, d_num_computed, d_num_scheduled, d_block_table, d_input_ids,
              d_positions, d_query_start_loc, d_seq_lens, d_slot_mapping, d_logits_indices,
              d_scalars, d_num_prompt, d_is_prefilling, d_discard_request_mask};

@@ -16,6 +16,16 @@ namespace rb {
 // host side
 // ---------------------------------------------------------------------------------------------
 void note_launches(int n);          // adds to rb_kernel_launch_count()
+
+// Page-table geometry shared by the entry points that read a page table.
+struct PageGeom {
+  int ratio;        // kernel pages per page-table entry (manager block), >= 1
+  int num_blocks;   // kernel pages in the pool
+  int null_block;   // kernel page of the null page
+};
+
+// Validates the page-table fields of rb_dims; fills `g`.  RB_OK or RB_ERR_INVALID_ARG.
+rb_status page_geom_of(const rb_dims& d, PageGeom* g);
 int device_sm_count();              // SM count of the current device (cached per device)
 rb_status last_launch_status();     // RB_ERR_CUDA if the previous launch failed
 
@@ -37,6 +47,21 @@ bool encode_q_tensor_map(CUtensorMap* map, const void* base, int head_dim, int n
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ void raise_error(int32_t* err, int32_t bit) {
   if (err != nullptr) atomicOr(err, bit);
+}
+
+// Kernel page holding logical kernel page `pg` of a row whose page-table entries are manager
+// blocks of `ratio` kernel pages: entry pg / ratio, page pg % ratio inside it.  Returns -1 when
+// the entry is outside the pool or is the manager block that holds the null page, so callers
+// treat it like any invalid page id.
+__device__ __forceinline__ int kernel_page(const int32_t* bt_row, int pg, int ratio,
+                                           int num_blocks, int null_block) {
+  if (ratio == 1) {
+    const int id = __ldg(bt_row + pg);
+    return (id < 0 || id >= num_blocks || id == null_block) ? -1 : id;
+  }
+  const int m = __ldg(bt_row + pg / ratio);
+  if (m < 0 || m >= num_blocks / ratio || m == null_block / ratio) return -1;
+  return m * ratio + pg % ratio;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -127,9 +127,10 @@ class PersistentBatch:
             ("cached_blocks", cat([c.new_blocks for c in cached])),
         ], len(sched_ids), len(new), len(cached)
 
-    def apply(self, step, stream=None) -> int:
+    def apply(self, step, stream=None, copied_event=None) -> int:
         """Merge one step's scheduler output into the batch (enqueued on ``stream``); returns
-        the bytes copied host -> device.  Sets ``num_reqs`` / ``num_tokens_scheduled``."""
+        the bytes copied host -> device.  Sets ``num_reqs`` / ``num_tokens_scheduled``.
+        ``copied_event``, if given, is recorded between the packet copy and the kernels."""
         import torch
 
         sections, S, NN, NC = self.pack(step)
@@ -147,6 +148,8 @@ class PersistentBatch:
             ev = torch.cuda.Event()
             ev.record(s)
         slot[2] = ev
+        if copied_event is not None:
+            copied_event.record(s)
         base = dev.data_ptr()
         ptr = {name: base + 4 * off for name, off in offsets.items()}
         u = rb.rb_batch_update(S, NN, NC, 0, *(ptr[f[0][2:]] for f in rb.rb_batch_update._fields_[4:]))

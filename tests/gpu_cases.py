@@ -24,7 +24,8 @@ def oracle_meta(spec):
                                  num_computed=spec.num_computed, num_scheduled=spec.num_scheduled,
                                  num_reqs_padded=spec.num_reqs_padded,
                                  num_tokens_padded=spec.num_tokens_padded,
-                                 num_prompt=spec.num_prompt)
+                                 num_prompt=spec.num_prompt,
+                                 kernel_blocks_per_manager_block=d.kernel_blocks_per_manager_block)
 
 
 def i32(a, device="cuda"):

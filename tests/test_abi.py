@@ -59,7 +59,8 @@ def test_pad_for_graph_matches_the_pages(lib):
 
 def _dims(lib, **kw):
     base = dict(block_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128, max_num_reqs=8,
-                max_model_len=4096, max_blocks_per_req=256, num_blocks=1000, null_block=0)
+                max_model_len=4096, max_blocks_per_req=256, num_blocks=1000, null_block=0,
+                kernel_blocks_per_manager_block=1)
     base.update(kw)
     return lib.rb_dims(*[base[f] for f, _ in lib.rb_dims._fields_])
 
@@ -85,6 +86,14 @@ def test_prepare_inputs_host_checks(lib):
     assert L.rb_prepare_inputs(ctypes.byref(d), 1, 1, 1, 1, *half, None) == 1
     noprompt = [FAKE] * 11 + [None, FAKE, FAKE]  # flags requested without prompt lengths
     assert L.rb_prepare_inputs(ctypes.byref(d), 1, 1, 1, 1, *noprompt, None) == 1
+    # manager-block page tables: pool and null page must be whole manager blocks
+    for kw in (dict(kernel_blocks_per_manager_block=3),              # 1000 % 3 != 0
+               dict(kernel_blocks_per_manager_block=2, null_block=1),
+               dict(kernel_blocks_per_manager_block=65, num_blocks=65 * 16),
+               dict(kernel_blocks_per_manager_block=-1)):
+        bad = _dims(lib, **kw)
+        assert L.rb_prepare_inputs(ctypes.byref(bad), 1, 1, 1, 1, *args, None) == 1, kw
+        assert _attn(lib, bad) == 1, kw
 
 
 def test_kv_write_host_checks(lib):

@@ -5,6 +5,7 @@ import numpy as np
 import pytest
 
 import oracle
+import workloads as wl
 from conftest import load_golden
 
 
@@ -231,3 +232,34 @@ def test_one_token_query_can_still_be_prefilling():
     flags = oracle.request_flags([5, 9, 12, 0], [1, 1, 1, 4], [9, 9, 12, 2], num_reqs_padded=6)
     assert flags["is_prefilling"].tolist() == [1, 0, 0, 1, 0, 0]
     assert flags["discard_request_mask"].tolist() == [1, 0, 0, 0, 1, 1]
+
+
+def test_manager_to_kernel_blocks_page_example():
+    """"混合 KV Cache：一条请求不止一张页表": 32-token manager blocks over 16-token kernel pages,
+    manager ids [0, 1, 2] become kernel ids [0, 1, 2, 3, 4, 5]."""
+    assert oracle.map_to_kernel_blocks([0, 1, 2], 2) == [0, 1, 2, 3, 4, 5]
+    assert oracle.map_to_kernel_blocks([7, 3], 1) == [7, 3]
+    assert oracle.map_to_kernel_blocks([], 4) == []
+
+
+@pytest.mark.parametrize("ratio", [2, 4])
+@pytest.mark.parametrize("seed", range(6))
+def test_manager_table_slots_equal_one_big_page(ratio, seed):
+    """Closed form: manager block m is r consecutive kernel pages, i.e. r*B consecutive slots,
+    so the slot of position p is m * (r*B) + p % (r*B) with m = table[i, p // (r*B)]."""
+    spec = wl.random_batch(seed, block_size=8, manager_ratio=ratio, max_q=50, max_c=120)
+    d = spec.dims
+    got = oracle.prepare_inputs(block_size=d.block_size, null_block=d.null_block,
+                                token_table=spec.token_table, block_table=spec.block_table,
+                                num_computed=spec.num_computed, num_scheduled=spec.num_scheduled,
+                                kernel_blocks_per_manager_block=ratio)
+    big = ratio * d.block_size
+    want = []
+    for i, (c, q) in enumerate(zip(spec.num_computed, spec.num_scheduled)):
+        for j in range(int(q)):
+            p = int(c) + j
+            want.append(int(spec.block_table[i, p // big]) * big + p % big)
+    assert got["slot_mapping"].tolist() == want
+    # every real slot lies in a manager block the request owns, never in the null one
+    for s in want:
+        assert s // big != d.null_block // ratio

@@ -48,6 +48,9 @@ class Dims:
     max_blocks_per_req: int
     num_blocks: int
     null_block: int = 0
+    # page-table entries are manager blocks of this many kernel pages (block_size tokens each);
+    # a manager block is kernel-page aligned and spans that many consecutive pages of the pool
+    kernel_blocks_per_manager_block: int = 1
 
     @property
     def num_slots(self) -> int:
@@ -118,11 +121,12 @@ def _build_spec(name, dims, computed, scheduled, rng, hidden_size, seed,
     assert R <= dims.max_num_reqs
     token_table = np.zeros((dims.max_num_reqs, dims.max_model_len), dtype=np.int32)
     block_table = np.full((dims.max_num_reqs, dims.max_blocks_per_req), -1, dtype=np.int32)
-    pool = PagePool(dims.num_blocks, dims.null_block, rng)
+    r = dims.kernel_blocks_per_manager_block
+    pool = PagePool(dims.num_blocks // r, dims.null_block // r, rng)  # manager block ids
     for i in range(R):
         total = int(computed[i]) + int(scheduled[i])
         token_table[i, :total] = rng.integers(0, VOCAB, size=total, dtype=np.int32)
-        n = pages_for(total, dims.block_size)
+        n = pages_for(total, dims.block_size * r)
         block_table[i, :n] = pool.take(n)
     n_tok = int(scheduled.sum(dtype=np.int64))
     if num_prompt is None:  # decodes: prompt already computed; longer queries finish their prompt
@@ -134,9 +138,11 @@ def _build_spec(name, dims, computed, scheduled, rng, hidden_size, seed,
                      seed=seed, num_prompt=None if num_prompt is None else np.asarray(num_prompt, np.int32))
 
 
-def _pool_blocks_for(computed, scheduled, block_size, slack=1.25) -> int:
-    need = sum(pages_for(int(c) + int(q), block_size) for c, q in zip(computed, scheduled))
-    return int(np.ceil(need * slack)) + 1
+def _pool_blocks_for(computed, scheduled, block_size, slack=1.25, ratio=1) -> int:
+    """Kernel pages of a pool with room for the batch (in whole manager blocks of ``ratio``
+    pages, the null manager block included)."""
+    need = sum(pages_for(int(c) + int(q), block_size * ratio) for c, q in zip(computed, scheduled))
+    return (int(np.ceil(need * slack)) + 1) * ratio
 
 
 def _round_up(x: int, m: int) -> int:
@@ -159,7 +165,7 @@ def config1(step: int = 0, num_tokens_padded: Optional[int] = None) -> BatchSpec
                        num_tokens_padded=num_tokens_padded)
 
 
-def config2(step: int = 0) -> BatchSpec:
+def config2(step: int = 0, manager_ratio: int = 1) -> BatchSpec:
     """Padding example: query_lens [2000, 512, 1 x 6]; decodes have 1000..4000 cached tokens.
 
     32 q heads / 8 kv heads, head_dim 128, block_size 16, hidden 4096.
@@ -170,13 +176,14 @@ def config2(step: int = 0) -> BatchSpec:
     computed = [0, 0] + [int(x) for x in rng.integers(1000, 4000, size=6, endpoint=True)]
     M = _round_up(max(c + q for c, q in zip(computed, scheduled)), 16) + 16
     dims = Dims(block_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128, max_num_reqs=8,
-                max_model_len=M, max_blocks_per_req=M // 16,
-                num_blocks=_pool_blocks_for(computed, scheduled, 16))
+                max_model_len=M, max_blocks_per_req=-(-M // (16 * manager_ratio)),
+                num_blocks=_pool_blocks_for(computed, scheduled, 16, ratio=manager_ratio),
+                kernel_blocks_per_manager_block=manager_ratio)
     return _build_spec("padding example (2 prefills + 6 decodes)", dims, computed, scheduled, rng,
                        4096, seed)
 
 
-def config3(step: int = 0, num_real: int = 256) -> BatchSpec:
+def config3(step: int = 0, num_real: int = 256, manager_ratio: int = 1) -> BatchSpec:
     """Pure decode: ``num_real`` requests x 1 token, cached context U[512, 8192], padded to 256.
 
     ``num_real=256`` is the workload as stated (no padding tokens); ``num_real=250`` exercises the
@@ -188,8 +195,9 @@ def config3(step: int = 0, num_real: int = 256) -> BatchSpec:
     scheduled = [1] * num_real
     M = _round_up(8192 + 1, 16)
     dims = Dims(block_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128, max_num_reqs=256,
-                max_model_len=M, max_blocks_per_req=M // 16,
-                num_blocks=_pool_blocks_for(computed, scheduled, 16))
+                max_model_len=M, max_blocks_per_req=-(-M // (16 * manager_ratio)),
+                num_blocks=_pool_blocks_for(computed, scheduled, 16, ratio=manager_ratio),
+                kernel_blocks_per_manager_block=manager_ratio)
     return _build_spec(f"pure decode ({num_real} real, padded to 256)", dims, computed, scheduled, rng,
                        4096, seed, num_reqs_padded=256, num_tokens_padded=256)
 
@@ -218,7 +226,8 @@ def config5(step: int = 0, pool_gb: float = 0.0) -> BatchSpec:
 def random_batch(seed: int, *, max_reqs: int = 6, max_q: int = 40, max_c: int = 90,
                  block_size: int = 16, num_q_heads: int = 4, num_kv_heads: int = 2,
                  head_dim: int = 64, pad_tokens: int = 0, pad_reqs: int = 0,
-                 decode_frac: float = 0.4, hidden_size: int = 128) -> BatchSpec:
+                 decode_frac: float = 0.4, hidden_size: int = 128,
+                 manager_ratio: int = 1) -> BatchSpec:
     """A small ragged mix for fuzzing: a seeded blend of decodes, fresh prefills and chunks."""
     rng = np.random.default_rng(seed)
     R = int(rng.integers(1, max_reqs + 1))
@@ -235,10 +244,12 @@ def random_batch(seed: int, *, max_reqs: int = 6, max_q: int = 40, max_c: int = 
             computed.append(int(rng.integers(1, max_c + 1)))
             scheduled.append(int(rng.integers(1, max_q + 1)))
     M = _round_up(max_c + max_q + 1, block_size) + block_size
+    r = manager_ratio
     dims = Dims(block_size=block_size, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                 head_dim=head_dim, max_num_reqs=R + pad_reqs + 1, max_model_len=M,
-                max_blocks_per_req=M // block_size,
-                num_blocks=_pool_blocks_for(computed, scheduled, block_size) + 3)
+                max_blocks_per_req=-(-M // (block_size * r)),
+                num_blocks=_pool_blocks_for(computed, scheduled, block_size, ratio=r) + 3 * r,
+                kernel_blocks_per_manager_block=r)
     n = sum(scheduled)
     spec = _build_spec(f"random mix seed={seed}", dims, computed, scheduled, rng, hidden_size,
                        seed, num_reqs_padded=R + pad_reqs, num_tokens_padded=n + pad_tokens)
@@ -251,16 +262,20 @@ def random_batch(seed: int, *, max_reqs: int = 6, max_q: int = 40, max_c: int = 
 
 def batch_from_lists(num_computed, num_scheduled, *, block_size=16, num_q_heads=4, num_kv_heads=2,
                      head_dim=64, seed=0, num_reqs_padded=None, num_tokens_padded=None,
-                     hidden_size=128, extra_blocks=3, max_model_len=None) -> BatchSpec:
+                     hidden_size=128, extra_blocks=3, max_model_len=None,
+                     manager_ratio=1) -> BatchSpec:
     """A batch with the given per-request counts (and seeded pages/tokens)."""
     rng = np.random.default_rng(seed)
     mx = max([c + q for c, q in zip(num_computed, num_scheduled)] + [1])
     M = max_model_len or (_round_up(mx, block_size) + block_size)
     R = len(num_scheduled)
+    r = manager_ratio
     dims = Dims(block_size=block_size, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
                 head_dim=head_dim, max_num_reqs=max(R, num_reqs_padded or 0, 1), max_model_len=M,
-                max_blocks_per_req=M // block_size,
-                num_blocks=_pool_blocks_for(num_computed, num_scheduled, block_size) + extra_blocks)
+                max_blocks_per_req=-(-M // (block_size * r)),
+                num_blocks=(_pool_blocks_for(num_computed, num_scheduled, block_size, ratio=r)
+                            + extra_blocks * r),
+                kernel_blocks_per_manager_block=r)
     return _build_spec("explicit", dims, num_computed, num_scheduled, rng, hidden_size, seed,
                        num_reqs_padded=num_reqs_padded, num_tokens_padded=num_tokens_padded)
 
@@ -510,12 +525,14 @@ def make_tensors(spec: BatchSpec, device="cpu", with_pool: bool = True, with_his
 
 
 def place_history(spec: BatchSpec, hist: list, cache) -> None:
-    """Copy each request's contiguous history into its pages, one whole page at a time."""
+    """Copy each request's contiguous history into its pages, one whole page-table entry (a
+    manager block of consecutive kernel pages) at a time."""
     import torch
 
     d = spec.dims
-    B = d.block_size
-    pages = cache.view(d.num_blocks, B, d.num_kv_heads, d.head_dim)
+    r = d.kernel_blocks_per_manager_block
+    B = d.block_size * r  # tokens per page-table entry: one manager block of r kernel pages
+    pages = cache.view(d.num_blocks // r, B, d.num_kv_heads, d.head_dim)
     for i, h in enumerate(hist):
         c = h.shape[0]
         full = c // B
