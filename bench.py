@@ -659,6 +659,83 @@ def run_trajectory(args, rank, world, local):
             "full_table_bytes": tt.numel() * 4 + bt.numel() * 4,
             "gpu_launches": launches, "clocks": clocks}), flush=True)
 
+def run_cascade_compare(args, rank, world, local):
+    """Shared system prompt (256 decodes after a common 4096-token prefix, own suffixes
+    U[16, 1024], plus two 512-token chunks): one attention call through the plain path and
+    through the cascade path, each timed alone with a cold L2."""
+    import numpy as np
+    import torch
+
+    import workloads as wl
+    import ragged_mixed_paged_gb300 as rb
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    spec = wl.shared_prefix_batch(11 + rank, num_decodes=256, prefix_tokens=4096,
+                                  suffix_range=(16, 1024), num_chunks=2, chunk_q=512)
+    d = spec.dims
+    dims = rb.Dims.of(d)
+    tens = wl.make_tensors(spec, device=dev)
+    tables = wl.device_tables(spec, dev)
+    R, N = spec.num_reqs, spec.num_tokens
+    meta = rb.prepare_inputs(dims, R, R, N, N, tables["token_table"], tables["num_computed"],
+                             tables["num_scheduled"], tables["block_table"])
+    rb.kv_write(dims, tens.k, tens.v, meta["slot_mapping"], tens.k_cache, tens.v_cache)
+    P = rb.cascade_prefix_len(spec.shared_prefix_tokens, spec.num_computed.tolist(), d.block_size)
+    ws = torch.empty(rb.cascade_workspace_size(dims, R, N), dtype=torch.uint8, device=dev)
+    out = torch.empty_like(tens.q)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    bt, qsl, sl = tables["block_table"], meta["query_start_loc"], meta["seq_lens"]
+    calls = {
+        "plain": lambda: rb.paged_attention(dims, R, N, tens.q, tens.k_cache, tens.v_cache, bt,
+                                            qsl, sl, out=out, workspace=ws, error_word=err),
+        "cascade": lambda: rb.paged_attention_cascade(dims, R, N, P, tens.q, tens.k_cache,
+                                                      tens.v_cache, bt, qsl, sl, out=out,
+                                                      workspace=ws, error_word=err),
+    }
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    res = {}
+    sampler = ClockSampler(local)
+    sampler.start()
+    for name, fn in calls.items():
+        g = torch.cuda.CUDAGraph()
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        with torch.cuda.graph(g):
+            fn()
+        times = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = E(), E()
+            a.record()
+            g.replay()
+            b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        res[name] = statistics.mean(times)
+    clocks = sampler.stop()
+    if int(err.item()) != 0:
+        raise SystemExit(f"device error word {int(err.item()):#x}")
+    kv_token = 2 * d.num_kv_heads * d.head_dim * 2  # K and V bytes of one token, all kv heads
+    L = spec.num_computed.astype(np.int64) + spec.num_scheduled
+    plain_bytes = int(L.sum()) * kv_token
+    casc_bytes = (P + int((L - P).sum())) * kv_token
+    pk, pk_kind = peaks()
+    if rank == 0:
+        print(json.dumps({
+            "metric": "attention call time with a shared prefix (plain vs cascade)",
+            "workload": spec.name, "num_reqs": R, "num_tokens": N, "prefix_len": P,
+            "steps": args.steps, "warmup": args.warmup, "launch": "cuda_graph_replay",
+            "l2": "512 MiB flush before every call",
+            "plain_ms": res["plain"], "cascade_ms": res["cascade"],
+            "speedup": res["plain"] / res["cascade"],
+            "plain_kv_bytes": plain_bytes, "cascade_kv_bytes": casc_bytes,
+            "plain_hbm_frac": plain_bytes / (res["plain"] / 1e3) / 1e9 / pk["hbm_gbs"],
+            "cascade_kv_gbs": casc_bytes / (res["cascade"] / 1e3) / 1e9,
+            "peak_kind": pk_kind, "clocks": clocks}), flush=True)
+
 
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__,
@@ -673,6 +750,8 @@ def main(argv=None):
                     help="launch every step from Python instead of replaying a captured graph")
     ap.add_argument("--manager-ratio", type=int, default=1,
                     help="--config 2/3: page tables of manager blocks of this many kernel pages")
+    ap.add_argument("--cascade", action="store_true",
+                    help="time one attention call on a shared-prefix batch, plain vs cascade")
     ap.add_argument("--trajectory", action="store_true",
                     help="--config 4 only: time a stream of steps, each with its batch update")
     args = ap.parse_args(argv)
@@ -681,6 +760,8 @@ def main(argv=None):
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.cascade:
+        run_cascade_compare(args, rank, world, local)
     elif args.trajectory:
         if args.config != 4:
             raise SystemExit("--trajectory needs --config 4")

@@ -254,6 +254,53 @@ rb_status rb_paged_attention_static_ws(const rb_dims* dims, int32_t num_reqs, in
                                        void* d_out, int32_t* d_error_word, void* stream);
 
 /*
+ * rb_cascade_prefix_len — host function; the shared-prefix length a cascade call may use:
+ * min(shared_prefix_tokens, min_i num_computed[i]) rounded down to a multiple of block_size
+ * (pass the page-table entry's token count, block_size * kernel_blocks_per_manager_block).
+ * Source: "第8章 ModelRunner…", "8.3.2.5 Cascade Attention 的 "最小 num_computed_tokens - 1"
+ * 规则" (the printed rule: cap by the smallest num_computed, then align to the block size, so
+ * no request's query sees a key of the prefix that it must not see).  num_computed is HOST
+ * memory [num_reqs].  0 for num_reqs = 0; -1 for invalid arguments (negative values, NULL
+ * num_computed with num_reqs > 0, block_size < 1).
+ */
+int32_t rb_cascade_prefix_len(int32_t shared_prefix_tokens, const int32_t* num_computed,
+                              int32_t num_reqs, int32_t block_size);
+
+/* Workspace bytes of rb_paged_attention_cascade (the ordinary workspace plus the prefix pass's
+   fp32 outputs [max_num_tokens, nh, head_dim] and log-sum-exps); 0 for invalid arguments. */
+size_t rb_paged_attention_cascade_workspace_size(const rb_dims* dims, int32_t max_num_reqs,
+                                                 int32_t max_num_tokens);
+
+/*
+ * rb_paged_attention_cascade — rb_paged_attention when every request shares its first
+ * common_prefix_len tokens (the same page-table entries): the prefix keys are read once for
+ * all query rows, then each request's own keys.  Same result up to rounding.
+ * Source: "第8章 ModelRunner…", "8.3.2.5 Cascade Attention" (a shared-prefix pass and a
+ * per-request suffix pass).
+ *
+ *   pass 1: every query row of the batch against keys [0, P) of row 0's pages, no mask (P is
+ *           at most every request's cached length, so each query sees all of them) -> fp32
+ *           output and log-sum-exp per (token, head) in the workspace;
+ *   pass 2: the ordinary causal attention over keys [P, seq_len) of each request, whose
+ *           epilogue merges the pass-1 row by log-sum-exp before rounding to bf16.
+ * Arguments as rb_paged_attention, plus common_prefix_len = P (rb_cascade_prefix_len gives
+ * it); the workspace is rb_paged_attention_cascade_workspace_size(dims, num_reqs, num_tokens).
+ * P = 0 (or an empty batch) is rb_paged_attention.
+ * Errors: host -> as rb_paged_attention, RB_ERR_INVALID_ARG when P is not a multiple of
+ *   block_size * kernel_blocks_per_manager_block or spans more than max_blocks_per_req entries,
+ *   RB_ERR_UNSUPPORTED for P > 0 on shapes without the tcgen05 path (head group not a power of
+ *   two, head_dim not 64 or 128); device -> bit ATTN_META when a request caches fewer than P
+ *   tokens or its first P / (block_size * r) entries differ from row 0's (results unspecified).
+ */
+rb_status rb_paged_attention_cascade(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
+                                     int32_t num_tokens_padded, int32_t common_prefix_len,
+                                     const void* d_q, const void* d_k_cache,
+                                     const void* d_v_cache, const int32_t* d_block_table,
+                                     const int32_t* d_query_start_loc, const int32_t* d_seq_lens,
+                                     float softmax_scale, void* d_out, void* d_workspace,
+                                     size_t workspace_bytes, int32_t* d_error_word, void* stream);
+
+/*
  * rb_gather_rows — out[i, :] = hidden[indices[i], :] for i < num_rows.
  * Source: "vLLM 源码完全拆解（五）…", "第四步：只在必要位置计算 logits"; "04 · 模型执行与
  * CUDA Graph", step ⑤ (hidden_states[logits_indices]).

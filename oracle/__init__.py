@@ -11,6 +11,8 @@ from the pages' prose and worked examples:
 * ``kv_cache``  — the paged K/V write by slot_mapping;
 * ``attention`` — per-request dense causal GQA attention in float64 over an
   unpaged, contiguous copy of each request's keys and values;
+* ``cascade``   — the shared-prefix length rule and the two-pass (prefix, suffix) attention
+  merged by log-sum-exp;
 * ``gather``    — selection of the last-token hidden rows.
 
 Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
@@ -28,7 +30,8 @@ from .metadata import (prepare_inputs, pad_for_graph, padded_layout_tokens,
 from .persistent_batch import InputBatch
 from .kv_cache import kv_write
 from .attention import paged_attention
+from .cascade import cascade_attention, cascade_prefix_len
 from .gather import gather_rows
 
-__all__ = ["prepare_inputs", "request_flags", "map_to_kernel_blocks", "InputBatch", "pad_for_graph", "padded_layout_tokens", "req_indices_and_query_pos",
+__all__ = ["cascade_attention", "cascade_prefix_len", "prepare_inputs", "request_flags", "map_to_kernel_blocks", "InputBatch", "pad_for_graph", "padded_layout_tokens", "req_indices_and_query_pos",
            "kv_write", "paged_attention", "gather_rows"]

@@ -4,6 +4,8 @@
                      slot_mapping, logits_indices (+ max_query_len, max_seq_len, error word)
     kv_write         new K/V rows -> paged cache by slot_mapping
     paged_attention  varlen causal GQA attention through the page table
+    paged_attention_cascade  the same when all requests share a prefix (read once), with
+                     cascade_prefix_len giving the usable prefix length
     gather_rows      hidden rows at logits_indices
     PersistentBatch  device-resident rows of the resident requests; ``apply`` merges one
                      step's scheduler output (remove, append, install, condense) on the GPU
@@ -15,11 +17,13 @@ from ._binding import (Dims, RbError, EBIT_ATTN_META, EBIT_BLOCK_ID, EBIT_NUM_CO
                        EBIT_NUM_SCHEDULED, EBIT_ROW_INDEX, EBIT_SEQ_LEN, EBIT_SLOT, EBIT_TIMEOUT,
                        EBIT_TOKEN_SUM, LIB_PATH, gather_rows, kv_write, launch_count, lib,
                        pad_for_graph, paged_attention, prepare_inputs, status_string,
-                       workspace_size)
+                       workspace_size, cascade_prefix_len, cascade_workspace_size,
+                       paged_attention_cascade)
 from ._binding import EBIT_BATCH_ID, EBIT_BATCH_SIZE
 from .persistent_batch import PersistentBatch, batch_workspace_size
 from .step import StepBuffers, run_step
 
 __all__ = ["Dims", "RbError", "gather_rows", "kv_write", "launch_count", "lib", "pad_for_graph",
            "paged_attention", "prepare_inputs", "status_string", "workspace_size", "StepBuffers",
-           "run_step", "LIB_PATH", "PersistentBatch", "batch_workspace_size"]
+           "run_step", "LIB_PATH", "PersistentBatch", "batch_workspace_size",
+           "cascade_prefix_len", "cascade_workspace_size", "paged_attention_cascade"]

@@ -89,6 +89,10 @@ def _load():
                                               ctypes.POINTER(ctypes.c_void_p), I32]),
         "rb_gather_rows": (I32, [I32, I32, I32, P, P, P, P, P]),
         "rb_batch_update_workspace_size": (I32, [I32, ctypes.POINTER(ctypes.c_size_t)]),
+        "rb_cascade_prefix_len": (I32, [I32, P, I32, I32]),
+        "rb_paged_attention_cascade_workspace_size": (ctypes.c_size_t, [PD, I32, I32]),
+        "rb_paged_attention_cascade": (I32, [PD, I32, I32, I32, I32, P, P, P, P, P, P,
+                                             ctypes.c_float, P, P, ctypes.c_size_t, P, P]),
         "rb_batch_apply_update": (I32, [ctypes.POINTER(rb_batch), ctypes.POINTER(rb_batch_update),
                                         P, P, P, ctypes.c_size_t, P, P]),
     }
@@ -260,6 +264,47 @@ def paged_attention(dims: Dims, num_reqs: int, num_tokens: int, q, k_cache, v_ca
         arr = (ctypes.c_void_p * len(handles))(*handles)
         _check("rb_paged_attention_profiled",
                lib.rb_paged_attention_profiled(*args, arr, len(handles)))
+    return out
+
+
+def cascade_prefix_len(shared_prefix_tokens: int, num_computed: Sequence[int],
+                       block_size: int) -> int:
+    """Shared-prefix length a cascade call may use (host rule; -1 for invalid input)."""
+    arr = (ctypes.c_int32 * len(num_computed))(*[int(x) for x in num_computed])
+    return int(lib.rb_cascade_prefix_len(shared_prefix_tokens, ctypes.cast(arr, ctypes.c_void_p),
+                                         len(num_computed), block_size))
+
+
+def cascade_workspace_size(dims: Dims, max_num_reqs: int, max_num_tokens: int) -> int:
+    d = dims.c()
+    return int(lib.rb_paged_attention_cascade_workspace_size(ctypes.byref(d), max_num_reqs,
+                                                             max_num_tokens))
+
+
+def paged_attention_cascade(dims: Dims, num_reqs: int, num_tokens: int, common_prefix_len: int,
+                            q, k_cache, v_cache, block_table, query_start_loc, seq_lens,
+                            out=None, workspace=None, softmax_scale: Optional[float] = None,
+                            error_word=None, stream=None):
+    """Attention of a batch whose requests share their first ``common_prefix_len`` tokens."""
+    import torch
+
+    bf = torch.bfloat16
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = torch.empty(cascade_workspace_size(dims, num_reqs, num_tokens),
+                                dtype=torch.uint8, device=q.device)
+    scale = 1.0 / math.sqrt(dims.head_dim) if softmax_scale is None else softmax_scale
+    d = dims.c()
+    st = lib.rb_paged_attention_cascade(
+        ctypes.byref(d), num_reqs, num_tokens, q.shape[0], common_prefix_len, _ptr(q, bf, "q"),
+        _ptr(k_cache, bf, "k_cache"), _ptr(v_cache, bf, "v_cache"),
+        _ptr(block_table, torch.int32, "block_table"),
+        _ptr(query_start_loc, torch.int32, "query_start_loc"),
+        _ptr(seq_lens, torch.int32, "seq_lens"), ctypes.c_float(scale), _ptr(out, bf, "out"),
+        _ptr(workspace, torch.uint8, "workspace"), workspace.numel(),
+        _ptr(error_word, torch.int32, "error_word"), _stream(stream))
+    _check("rb_paged_attention_cascade", st)
     return out
 
 

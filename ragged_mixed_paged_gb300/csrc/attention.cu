@@ -67,8 +67,7 @@ __device__ __forceinline__ ReqInfo req_info(const AttnArgs& a, int r) {
   x.q = e - s;
   x.L = a.seq_lens[r];
   x.pages = (x.L + kPage - 1) / kPage;
-  x.ok = s >= 0 && x.q >= 0 && e <= a.N && x.L >= x.q &&
-         x.pages <= static_cast<long long>(a.MB) * a.ratio;
+  x.ok = s >= 0 && x.q >= 0 && e <= a.N && x.L >= x.q && x.pages <= a.kp_cap;
   return x;
 }
 
@@ -158,6 +157,38 @@ __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(AttnArgs a, int
   if (bits) raise_error(a.err, bits);
 }
 
+// Cascade: checks the shared prefix, writes the suffix pass's sequence lengths (seq_len - P)
+// and sets the header up for the prefix pass (its units only; no decode units).
+__global__ void __launch_bounds__(kPlanThreads)
+    cascade_prepare_kernel(AttnArgs a, int prefix_len, int prefix_entries, int32_t* lens_out) {
+  const int tid = threadIdx.x;
+  int bits = 0;
+  if (tid == 0 && (a.qsl[0] != 0 || a.qsl[a.R] != a.N)) bits |= RB_EBIT_ATTN_META;
+  for (int r = tid; r < a.R; r += kPlanThreads) {
+    const int q = a.qsl[r + 1] - a.qsl[r], L = a.seq_lens[r];
+    // every query must see the whole prefix: P <= cached length (the 8.3.2.5 cap)
+    if (q < 0 || L - q < prefix_len) bits |= RB_EBIT_ATTN_META;
+    lens_out[r] = L - prefix_len;
+  }
+  // every request's first page-table entries must be the shared ones (those of row 0)
+  const long long total = static_cast<long long>(a.R) * prefix_entries;
+  for (long long i = tid; i < total; i += kPlanThreads) {
+    const int r = static_cast<int>(i / prefix_entries), e = static_cast<int>(i % prefix_entries);
+    if (a.block_table[static_cast<size_t>(r) * a.MB + e] != a.block_table[e])
+      bits |= RB_EBIT_ATTN_META;
+  }
+  if (tid == 0) {
+    a.header[kHNumDecodeUnits] = 0;
+    a.header[kHNumPrefillUnits] = a.nkv * ((a.N * a.group + 255) / 256) * a.prefix_splits;
+    a.header[kHDecodeNext] = 0;
+    a.header[kHPrefillNext] = 0;
+    a.header[kHSplitPages] = kMinSplitPages;
+    a.header[kHDecodeCtas] = 0;
+    a.header[kHRoleNext] = 0;
+  }
+  if (bits) raise_error(a.err, bits);
+}
+
 }  // namespace
 }  // namespace attn
 }  // namespace rb
@@ -178,7 +209,8 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
                                const int32_t* d_query_start_loc, const int32_t* d_seq_lens,
                                float softmax_scale, void* d_out, void* d_workspace,
                                size_t workspace_bytes, int32_t* d_error_word, void* stream,
-                               void* const* events, int32_t num_events) {
+                               void* const* events, int32_t num_events,
+                               int32_t prefix_len = 0) {
   using namespace rb;
   using namespace rb::attn;
   if (dims == nullptr) return RB_ERR_INVALID_ARG;
@@ -203,6 +235,16 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
     return RB_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(d.head_dim, d.num_kv_heads, num_reqs);
   if (workspace_bytes < w.total) return RB_ERR_CAPACITY;
+  // cascade: P page-aligned in whole page-table entries, within a row
+  if (prefix_len < 0 || prefix_len % (kPage * g.ratio) != 0 ||
+      prefix_len / (kPage * g.ratio) > d.max_blocks_per_req)
+    return RB_ERR_INVALID_ARG;
+  if (num_reqs == 0 || num_tokens == 0) prefix_len = 0;  // nothing shares anything
+  const CascadeLayout cl =
+      cascade_layout(d.head_dim, d.num_q_heads, d.num_kv_heads, num_reqs, num_tokens);
+  if (prefix_len > 0 && workspace_bytes < cl.total) return RB_ERR_CAPACITY;
+  if (prefix_len > 0 && !prefill_tc_supported(d.head_dim, d.num_q_heads / d.num_kv_heads))
+    return RB_ERR_UNSUPPORTED;
 
   CUtensorMap kmap, vmap;
   const long long num_slots = static_cast<long long>(d.num_blocks) * kPage;
@@ -240,6 +282,7 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
   a.num_blocks = d.num_blocks;
   a.null_block = d.null_block;
   a.ratio = g.ratio;
+  a.kp_cap = static_cast<long long>(d.max_blocks_per_req) * g.ratio;
   const int sms = max(1, device_sm_count());
   a.target_units = min(kMaxTargetUnits, 32 * sms);
   a.tile_m = use_tc ? 256 : kPrefillTileM;  // tcgen05 units are pairs of 128-row tiles
@@ -249,6 +292,37 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
   a.err = d_error_word;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (prefix_len > 0) {
+    // "8.3.2.5 Cascade Attention": the shared prefix once for every query row, then the
+    // ordinary causal pass over each request's own keys [P, seq_len), merged per row
+    const int entries = prefix_len / (kPage * g.ratio);
+    int32_t* lens = reinterpret_cast<int32_t*>(ws + cl.lens);
+    a.pre_lse = reinterpret_cast<float*>(ws + cl.lse);
+    a.pre_o = reinterpret_cast<float*>(ws + cl.o);
+    // cut the prefix keys into ranges so the prefix pass has a few units per SM (each range
+    // at least 4 key tiles); the suffix epilogues merge one partial per range
+    const int tiles = (prefix_len + 127) / 128;
+    const int base_units = d.num_kv_heads * ((num_tokens * group + 255) / 256);
+    const int sms = max(1, device_sm_count());
+    int splits = (4 * sms + base_units - 1) / base_units;
+    splits = max(1, min(splits, min(kMaxPrefixSplits, tiles / 4)));
+    const int split_keys = (tiles + splits - 1) / splits * 128;
+    splits = (prefix_len + split_keys - 1) / split_keys;
+    a.prefix_splits = splits;
+    a.prefix_split_keys = split_keys;
+    AttnArgs ap = a;
+    ap.cascade = kPrefixPass;
+    ap.prefix_len = prefix_len;
+    cascade_prepare_kernel<<<1, kPlanThreads, 0, s>>>(ap, prefix_len, entries, lens);
+    if (last_launch_status() != RB_OK) return RB_ERR_CUDA;
+    note_launches(1);
+    const rb_status st = launch_prefill_tc(ap, d.head_dim, qmap, kmap, vmap, s);
+    if (st != RB_OK) return st;
+    a.cascade = kSuffixPass;
+    a.seq_lens = lens;
+    a.block_table = d_block_table + entries;  // every row starts at its entry `entries`
+    a.kp_cap = static_cast<long long>(d.max_blocks_per_req - entries) * g.ratio;
+  }
   cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
   if (num_events > 0 && cudaStreamIsCapturing(s, &capturing) != cudaSuccess) return RB_ERR_CUDA;
   auto mark = [&](int i) -> bool {  // inside a stream capture the records become graph nodes
@@ -306,4 +380,42 @@ extern "C" rb_status rb_paged_attention_profiled(
                               d_v_cache, d_block_table, d_query_start_loc, d_seq_lens,
                               softmax_scale, d_out, d_workspace, workspace_bytes, d_error_word,
                               stream, events, num_events);
+}
+
+extern "C" size_t rb_paged_attention_cascade_workspace_size(const rb_dims* dims,
+                                                            int32_t max_num_reqs,
+                                                            int32_t max_num_tokens) {
+  if (dims == nullptr || max_num_reqs < 0 || max_num_tokens < 0 || dims->num_kv_heads < 1 ||
+      dims->num_q_heads < 1 || dims->head_dim < 1)
+    return 0;
+  return rb::attn::cascade_layout(dims->head_dim, dims->num_q_heads, dims->num_kv_heads,
+                                  max_num_reqs, max_num_tokens)
+      .total;
+}
+
+extern "C" rb_status rb_paged_attention_cascade(
+    const rb_dims* dims, int32_t num_reqs, int32_t num_tokens, int32_t num_tokens_padded,
+    int32_t common_prefix_len, const void* d_q, const void* d_k_cache, const void* d_v_cache,
+    const int32_t* d_block_table, const int32_t* d_query_start_loc, const int32_t* d_seq_lens,
+    float softmax_scale, void* d_out, void* d_workspace, size_t workspace_bytes,
+    int32_t* d_error_word, void* stream) {
+  return paged_attention_impl(dims, num_reqs, num_tokens, num_tokens_padded, d_q, d_k_cache,
+                              d_v_cache, d_block_table, d_query_start_loc, d_seq_lens,
+                              softmax_scale, d_out, d_workspace, workspace_bytes, d_error_word,
+                              stream, nullptr, 0, common_prefix_len);
+}
+
+extern "C" int32_t rb_cascade_prefix_len(int32_t shared_prefix_tokens,
+                                         const int32_t* num_computed, int32_t num_reqs,
+                                         int32_t block_size) {
+  if (shared_prefix_tokens < 0 || num_reqs < 0 || block_size < 1 ||
+      (num_reqs > 0 && num_computed == nullptr))
+    return -1;
+  if (num_reqs == 0) return 0;
+  int32_t p = shared_prefix_tokens;
+  for (int32_t i = 0; i < num_reqs; ++i) {
+    if (num_computed[i] < 0) return -1;
+    p = num_computed[i] < p ? num_computed[i] : p;
+  }
+  return p / block_size * block_size;
 }

@@ -50,6 +50,37 @@ inline WsLayout ws_layout(int head_dim, int num_kv_heads, int num_reqs) {
   return w;
 }
 
+// Cascade attention ("第8章 ModelRunner…", "8.3.2.5 Cascade Attention"): a prefix pass runs every
+// query row against the P keys all requests share (no mask: P <= every request's cached
+// length), a suffix pass runs the ordinary causal attention over keys [P, seq_len) and merges
+// the prefix result into each row by log-sum-exp before the single bf16 rounding.
+enum CascadePass : int { kNoCascade = 0, kPrefixPass = 1, kSuffixPass = 2 };
+constexpr int kMaxPrefixSplits = 4;  // the prefix keys may be cut into this many ranges
+
+// Extra workspace of a cascade call, after the ordinary layout: shifted sequence lengths and,
+// per prefix key range, the prefix pass's normalised outputs (fp32) with their log2-domain
+// log-sum-exp.
+struct CascadeLayout {
+  size_t lens, lse, o, total;
+};
+
+inline CascadeLayout cascade_layout(int head_dim, int num_q_heads, int num_kv_heads, int num_reqs,
+                                    int num_tokens) {
+  CascadeLayout c{};
+  size_t off = ws_layout(head_dim, num_kv_heads, num_reqs).total;
+  auto take = [&off](size_t bytes) {
+    const size_t o = off;
+    off += (bytes + 255) & ~static_cast<size_t>(255);
+    return o;
+  };
+  c.lens = take(static_cast<size_t>(num_reqs) * sizeof(int32_t));
+  c.lse = take(static_cast<size_t>(kMaxPrefixSplits) * num_tokens * num_q_heads * sizeof(float));
+  c.o = take(static_cast<size_t>(kMaxPrefixSplits) * num_tokens * num_q_heads * head_dim *
+             sizeof(float));
+  c.total = off;
+  return c;
+}
+
 struct AttnArgs {
   const __nv_bfloat16* q;
   __nv_bfloat16* out;
@@ -70,7 +101,51 @@ struct AttnArgs {
   int decode_warps_per_cta;  // decode warps per CTA in the launch that runs decode units
   float scale_log2;
   int32_t* err;
+  long long kp_cap;   // kernel pages a row may span (max_blocks_per_req * ratio, less a shift)
+  int cascade;        // CascadePass
+  int prefix_len;     // prefix pass: the shared keys [0, P) of row 0
+  int prefix_splits;  // key ranges of the prefix pass (1 .. kMaxPrefixSplits)
+  int prefix_split_keys;  // keys per range (a multiple of 128)
+  float* pre_o;       // [splits, N, nh, HD] prefix-pass outputs per key range, normalised
+  float* pre_lse;     // [splits, N, nh] their log-sum-exp (log2 units of the scaled scores)
 };
+
+// Weights that merge a suffix-pass row (accumulator relative to running max m, sum l; log2
+// units) with the prefix-pass rows of the same (token, head) (one per key range: log-sum-exp
+// lse_s, normalised o_s): out = acc * (return value) + sum_s o_s * w[s].
+__device__ __forceinline__ float cascade_weights(const AttnArgs& a, size_t row, float m, float l,
+                                                 float* w) {
+  const size_t stride = static_cast<size_t>(a.N) * a.nh;
+  float lse[kMaxPrefixSplits];
+  float mx = l > 0.f ? m : -INFINITY;
+#pragma unroll
+  for (int s = 0; s < kMaxPrefixSplits; ++s) {
+    lse[s] = s < a.prefix_splits ? __ldg(a.pre_lse + s * stride + row) : -INFINITY;
+    mx = fmaxf(mx, lse[s]);
+  }
+  if (mx == -INFINITY) {
+#pragma unroll
+    for (int s = 0; s < kMaxPrefixSplits; ++s) w[s] = 0.f;
+    return 0.f;
+  }
+  const float wa = l > 0.f ? fast_exp2(m - mx) : 0.f;
+  float den = l * wa;
+#pragma unroll
+  for (int s = 0; s < kMaxPrefixSplits; ++s) {
+    w[s] = lse[s] == -INFINITY ? 0.f : fast_exp2(lse[s] - mx);
+    den += w[s];
+  }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+#pragma unroll
+  for (int s = 0; s < kMaxPrefixSplits; ++s) w[s] *= inv;
+  return wa * inv;
+}
+
+// Prefix-pass output row of key range s for (token, head) row `row`.
+template <int HD>
+__device__ __forceinline__ const float* cascade_row(const AttnArgs& a, int s, size_t row) {
+  return a.pre_o + (static_cast<size_t>(s) * a.N * a.nh + row) * HD;
+}
 
 // Request classes shared by the planner and the kernels.
 __host__ __device__ inline bool is_decode_class(int q, int group) {

@@ -59,10 +59,30 @@ __device__ void combine_splits(const AttnArgs& a, int h, int first, int nsplit, 
     }
   }
   if (!active) return;
-  const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
   const int j = col / a.group, hh = col - j * a.group;
-  uint4* dst = reinterpret_cast<uint4*>(
-      a.out + (static_cast<size_t>(t0 + j) * a.nh + h * a.group + hh) * HD + part * kPer);
+  const size_t row = static_cast<size_t>(t0 + j) * a.nh + h * a.group + hh;
+  float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+  if (a.cascade == kSuffixPass) {  // fold in the shared-prefix rows (acc and lsum are at mx)
+    float wp[kMaxPrefixSplits];
+    const float wa = cascade_weights(a, row, mx, lsum, wp);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) acc[k] *= wa;
+#pragma unroll
+    for (int ps = 0; ps < kMaxPrefixSplits; ++ps) {
+      if (ps >= a.prefix_splits) break;
+      const float4* o1 = reinterpret_cast<const float4*>(cascade_row<HD>(a, ps, row) + part * kPer);
+#pragma unroll
+      for (int v = 0; v < kPer / 4; ++v) {
+        const float4 x = __ldg(o1 + v);
+        acc[4 * v + 0] += x.x * wp[ps];
+        acc[4 * v + 1] += x.y * wp[ps];
+        acc[4 * v + 2] += x.z * wp[ps];
+        acc[4 * v + 3] += x.w * wp[ps];
+      }
+    }
+    inv = 1.f;
+  }
+  uint4* dst = reinterpret_cast<uint4*>(a.out + row * HD + part * kPer);
 #pragma unroll
   for (int v = 0; v < kPer / 8; ++v) {
     uint4 wv;
@@ -260,7 +280,9 @@ __device__ void decode_warp(const CUtensorMap* kmap_p, const CUtensorMap* vmap_p
       l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
     const int dlo = lane >> 2;
-    if (nsplit == 1) {
+    if (nsplit == 1 && a.cascade != kSuffixPass) {
+      // (in a cascade suffix pass even an unsplit unit goes through the merge below, which
+      // also folds in the shared-prefix rows)
       const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
       __nv_bfloat16* o0 = nullptr;
       __nv_bfloat16* o1 = nullptr;

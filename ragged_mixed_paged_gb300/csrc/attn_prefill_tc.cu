@@ -70,9 +70,20 @@ struct TcCfg {
   __device__ static constexpr uint32_t col_o(int x) { return kColO0 + static_cast<uint32_t>(HD) * x; }
 };
 
+// A unit of work.  In a cascade prefix pass `r` holds the unit's prefix key range (the pages
+// are row 0's), key indices are relative to the range's first key and no row is masked
+// causally: every row sees keys [0, c].
 struct TcUnit {
   int r, h, row0, t0, q, L, c, rows_total, n[2], n_kt, pages, valid;
 };
+
+// First page of a unit's keys and the page-table row they are read from.
+__device__ __forceinline__ int unit_first_page(const AttnArgs& a, const TcUnit& un) {
+  return a.cascade == kPrefixPass ? un.r * (a.prefix_split_keys / kPage) : 0;
+}
+__device__ __forceinline__ int unit_table_row(const AttnArgs& a, const TcUnit& un) {
+  return a.cascade == kPrefixPass ? 0 : un.r;
+}
 
 struct TcShared {
   uint64_t unit_full[4], unit_empty[4];
@@ -108,9 +119,33 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t phase, volatile 
 }
 
 __device__ __forceinline__ int tiles_for(int c, int jmax) { return (c + jmax + 1 + 127) / 128; }
+constexpr int kKeysPerTile = 128;  // keys per K/V tile
 
 __device__ __forceinline__ TcUnit decode_unit(const AttnArgs& a, int u) {
   TcUnit un{};
+  if (a.cascade == kPrefixPass) {
+    // (key range, kv head, 256 query rows of the whole batch) against one range of the shared
+    // keys [0, P) of row 0; key indices are relative to the range's first key
+    const int per_split = a.nkv * ((a.N * a.group + 255) / 256);
+    const int split = u / per_split, rem = u - split * per_split;
+    const int k0 = split * a.prefix_split_keys;
+    const int k1 = min(a.prefix_len, k0 + a.prefix_split_keys);
+    un.r = split;
+    un.h = rem % a.nkv;
+    un.row0 = (rem / a.nkv) * 256;
+    un.t0 = 0;
+    un.q = a.N;
+    un.L = k1 - k0;
+    un.c = un.L - 1;
+    un.rows_total = a.N * a.group;
+    const int nk = (un.L + kKeysPerTile - 1) / kKeysPerTile;
+    un.n[0] = nk;
+    un.n[1] = un.row0 + 128 < un.rows_total ? nk : 0;
+    un.n_kt = nk;
+    un.pages = (un.L + kPage - 1) / kPage;
+    un.valid = 1;
+    return un;
+  }
   const int r = upper_bound_i32(a.pre_off, a.R + 1, u) - 1;
   const int first = a.pre_off[r];
   const int pairs_r = (a.pre_off[r + 1] - first) / a.nkv;
@@ -174,11 +209,14 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
           tma_load_3d(smem_base + C::kQOffset + x * C::kQBytes + hf * C::kQHalfBytes, qmap,
                       &sh.q_full, hf * 64, un.h * a.group, un.t0 + (un.row0 + 128 * x) / a.group);
     }
-    const int32_t* bt_row = a.block_table + static_cast<size_t>(un.r) * a.MB;
+    const int32_t* bt_row =
+        a.block_table + static_cast<size_t>(unit_table_row(a, un)) * a.MB;
+    const int page0 = unit_first_page(a, un);
     int win = 0;
     auto page = [&](int pg) {
-      return pg < un.pages ? kernel_page(bt_row, pg, a.ratio, a.num_blocks, a.null_block)
-                           : a.null_block;
+      return pg < un.pages
+                 ? kernel_page(bt_row, page0 + pg, a.ratio, a.num_blocks, a.null_block)
+                 : a.null_block;
     };
     int bid = page(lane);
     int bid_next = page(32 + lane);
@@ -369,8 +407,9 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
     const bool valid = row < un.rows_total;
     const int jt = valid ? row / a.group : 0;
     const int hh = valid ? row - jt * a.group : 0;
-    const int lim = un.c + jt;
-    const int lim_min = un.c + row0 / a.group;
+    const bool causal = a.cascade != kPrefixPass;
+    const int lim = causal ? un.c + jt : un.c;
+    const int lim_min = causal ? un.c + row0 / a.group : un.c;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -474,23 +513,65 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
       tc_x += n;
       if (!catch_up(tc_x)) break;  // every P V of this unit has landed in O
       tc::fence_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(
-          a.out + (static_cast<size_t>(un.t0 + jt) * a.nh + un.h * a.group + hh) * HD);
+      const size_t orow = static_cast<size_t>(un.t0 + jt) * a.nh + un.h * a.group + hh;
+      if (a.cascade == kPrefixPass) {
+        // shared-prefix row: normalised fp32 output and its log-sum-exp, merged later
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+        const size_t prow = static_cast<size_t>(un.r) * a.N * a.nh + orow;
+        float4* dst = reinterpret_cast<float4*>(a.pre_o + prow * HD);
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        uint32_t r[32];
-        tc::ld32(col_o + c * 32, r);
-        tc::wait_ld();
-        if (valid) {
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t r[32];
+          tc::ld32(col_o + c * 32, r);
+          tc::wait_ld();
+          if (valid) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint4 w;
-            w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv);
-            w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv);
-            w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv);
-            w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv);
-            dst[c * 4 + v] = w;
+            for (int v = 0; v < 8; ++v)
+              dst[c * 8 + v] = make_float4(
+                  __uint_as_float(r[4 * v + 0]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                  __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+          }
+        }
+        if (valid) a.pre_lse[prow] = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
+      } else {
+        // out = O * wa + sum over prefix key ranges of (shared-prefix row) * wp (cascade only)
+        float wa = l > 0.f ? 1.f / l : 0.f;
+        float wp[kMaxPrefixSplits];
+        const bool cas = a.cascade == kSuffixPass && valid;
+        if (cas) wa = cascade_weights(a, orow, m_ref, l, wp);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + orow * HD);
+#pragma unroll
+        for (int c = 0; c < HD / 32; ++c) {
+          uint32_t r[32];
+          tc::ld32(col_o + c * 32, r);
+          tc::wait_ld();
+          if (valid) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * wa);
+            if (cas) {
+#pragma unroll
+              for (int ps = 0; ps < kMaxPrefixSplits; ++ps) {
+                if (ps >= a.prefix_splits) break;
+                const float4* o1 = reinterpret_cast<const float4*>(cascade_row<HD>(a, ps, orow));
+#pragma unroll
+                for (int v = 0; v < 8; ++v) {
+                  const float4 e = __ldg(o1 + c * 8 + v);
+                  r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + e.x * wp[ps]);
+                  r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + e.y * wp[ps]);
+                  r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + e.z * wp[ps]);
+                  r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + e.w * wp[ps]);
+                }
+              }
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 q4;
+              q4.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+              q4.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+              q4.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+              q4.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+              dst[c * 4 + v] = q4;
+            }
           }
         }
       }

@@ -186,3 +186,41 @@ def test_batch_update_host_checks(lib):
     assert call(_batch(lib), _update(lib), err=None) == 1
     assert call(_batch(lib), _update(lib), ws=MISALIGNED) == 1
     assert call(_batch(lib), _update(lib), ws_bytes=small - 1) == 2
+
+
+def test_cascade_prefix_len_host_rule(lib):
+    """The library's host rule equals the oracle's on random batches."""
+    import numpy as np
+
+    import oracle
+
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        R = int(rng.integers(0, 6))
+        c = [int(x) for x in rng.integers(0, 500, size=R)]
+        shared, B = int(rng.integers(0, 600)), int(rng.choice([1, 16, 32]))
+        assert lib.cascade_prefix_len(shared, c, B) == oracle.cascade_prefix_len(shared, c, B)
+    assert lib.cascade_prefix_len(-1, [3], 16) == -1
+    assert lib.cascade_prefix_len(10, [3], 0) == -1
+    assert lib.cascade_prefix_len(10, [-3], 16) == -1
+
+
+def test_cascade_attention_host_checks(lib):
+    L = lib.lib
+
+    def call(d, P, ws_bytes=1 << 30):
+        return L.rb_paged_attention_cascade(ctypes.byref(d), 2, 4, 4, P, FAKE, FAKE, FAKE, FAKE,
+                                            FAKE, FAKE, ctypes.c_float(0.1), FAKE, FAKE, ws_bytes,
+                                            None, None)
+
+    d = _dims(lib)
+    assert call(d, 8) == 1                                  # not a whole page
+    assert call(d, 16 * 257) == 1                           # more entries than a row has
+    assert call(d, -16) == 1
+    assert call(_dims(lib, num_q_heads=24), 16) == 5        # group 3: no tcgen05 path
+    r2 = _dims(lib, kernel_blocks_per_manager_block=2)
+    assert call(r2, 16) == 1                                # half a manager block
+    need = L.rb_paged_attention_cascade_workspace_size(ctypes.byref(d), 2, 4)
+    plain = L.rb_paged_attention_workspace_size(ctypes.byref(d), 2, 4)
+    assert need > plain
+    assert call(d, 16, ws_bytes=need - 1) == 2

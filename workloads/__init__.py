@@ -72,6 +72,7 @@ class BatchSpec:
     hidden_size: int
     seed: int
     num_prompt: Optional[np.ndarray] = None  # int32 [R] prompt lengths, where known
+    shared_prefix_tokens: int = 0  # every request's first tokens, pages and history are shared
 
     @property
     def num_reqs(self) -> int:
@@ -114,7 +115,8 @@ def pages_for(num_tokens: int, block_size: int) -> int:
 
 
 def _build_spec(name, dims, computed, scheduled, rng, hidden_size, seed,
-                num_reqs_padded=None, num_tokens_padded=None, num_prompt=None) -> BatchSpec:
+                num_reqs_padded=None, num_tokens_padded=None, num_prompt=None,
+                shared_prefix=0) -> BatchSpec:
     computed = np.asarray(computed, dtype=np.int32)
     scheduled = np.asarray(scheduled, dtype=np.int32)
     R = computed.shape[0]
@@ -123,11 +125,17 @@ def _build_spec(name, dims, computed, scheduled, rng, hidden_size, seed,
     block_table = np.full((dims.max_num_reqs, dims.max_blocks_per_req), -1, dtype=np.int32)
     r = dims.kernel_blocks_per_manager_block
     pool = PagePool(dims.num_blocks // r, dims.null_block // r, rng)  # manager block ids
+    n_shared = shared_prefix // (dims.block_size * r)
+    assert n_shared * dims.block_size * r == shared_prefix, "shared prefix in whole entries"
+    shared_pages = pool.take(n_shared) if n_shared else []
+    shared_tokens = rng.integers(0, VOCAB, size=shared_prefix, dtype=np.int32)
     for i in range(R):
         total = int(computed[i]) + int(scheduled[i])
         token_table[i, :total] = rng.integers(0, VOCAB, size=total, dtype=np.int32)
+        token_table[i, :shared_prefix] = shared_tokens
         n = pages_for(total, dims.block_size * r)
-        block_table[i, :n] = pool.take(n)
+        block_table[i, :n_shared] = shared_pages
+        block_table[i, n_shared:n] = pool.take(n - n_shared)
     n_tok = int(scheduled.sum(dtype=np.int64))
     if num_prompt is None:  # decodes: prompt already computed; longer queries finish their prompt
         num_prompt = [int(c) if int(q) == 1 else int(c) + int(q) for c, q in zip(computed, scheduled)]
@@ -135,7 +143,8 @@ def _build_spec(name, dims, computed, scheduled, rng, hidden_size, seed,
                      num_reqs_padded=R if num_reqs_padded is None else num_reqs_padded,
                      num_tokens_padded=n_tok if num_tokens_padded is None else num_tokens_padded,
                      token_table=token_table, block_table=block_table, hidden_size=hidden_size,
-                     seed=seed, num_prompt=None if num_prompt is None else np.asarray(num_prompt, np.int32))
+                     seed=seed, num_prompt=None if num_prompt is None else np.asarray(num_prompt, np.int32),
+                     shared_prefix_tokens=int(shared_prefix))
 
 
 def _pool_blocks_for(computed, scheduled, block_size, slack=1.25, ratio=1) -> int:
@@ -278,6 +287,34 @@ def batch_from_lists(num_computed, num_scheduled, *, block_size=16, num_q_heads=
                 kernel_blocks_per_manager_block=r)
     return _build_spec("explicit", dims, num_computed, num_scheduled, rng, hidden_size, seed,
                        num_reqs_padded=num_reqs_padded, num_tokens_padded=num_tokens_padded)
+
+
+def shared_prefix_batch(seed: int, *, num_decodes: int, prefix_tokens: int,
+                        suffix_range=(16, 1024), num_chunks: int = 0, chunk_q: int = 512,
+                        num_q_heads: int = 32, num_kv_heads: int = 8, head_dim: int = 128,
+                        block_size: int = 16, manager_ratio: int = 1,
+                        hidden_size: int = 4096) -> BatchSpec:
+    """Requests that all start with the same ``prefix_tokens`` (a shared system prompt: same
+    token ids, same pages, same cached K/V): ``num_decodes`` decodes with U[suffix_range] own
+    cached tokens after the prefix, and ``num_chunks`` prefill chunks of ``chunk_q`` new tokens
+    on top of U[0, 256] own cached tokens."""
+    rng = np.random.default_rng(seed)
+    lo, hi = suffix_range
+    computed = [prefix_tokens + int(x) for x in rng.integers(lo, hi, size=num_decodes, endpoint=True)]
+    scheduled = [1] * num_decodes
+    for _ in range(num_chunks):
+        computed.append(prefix_tokens + int(rng.integers(0, 256, endpoint=True)))
+        scheduled.append(chunk_q)
+    M = _round_up(max(c + q for c, q in zip(computed, scheduled)), block_size * manager_ratio) + \
+        block_size * manager_ratio
+    r = manager_ratio
+    dims = Dims(block_size=block_size, num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                head_dim=head_dim, max_num_reqs=len(computed), max_model_len=M,
+                max_blocks_per_req=-(-M // (block_size * r)),
+                num_blocks=_pool_blocks_for(computed, scheduled, block_size, ratio=r) + 2 * r,
+                kernel_blocks_per_manager_block=r)
+    return _build_spec(f"shared prefix {prefix_tokens} x {len(computed)} requests", dims,
+                       computed, scheduled, rng, hidden_size, seed, shared_prefix=prefix_tokens)
 
 
 # --------------------------------------------------------------------------- #
@@ -509,10 +546,17 @@ def make_tensors(spec: BatchSpec, device="cpu", with_pool: bool = True, with_his
     hidden = randn(Np, spec.hidden_size)
     hist_k, hist_v = [], []
     if with_history:
+        P = spec.shared_prefix_tokens
+        if P:  # one history for the shared prefix, then each request's own
+            pk, pv = randn(P, d.num_kv_heads, d.head_dim), randn(P, d.num_kv_heads, d.head_dim)
         for i in range(spec.num_reqs):
             c = int(spec.num_computed[i])
-            hist_k.append(randn(c, d.num_kv_heads, d.head_dim))
-            hist_v.append(randn(c, d.num_kv_heads, d.head_dim))
+            if P:
+                hist_k.append(torch.cat([pk, randn(c - P, d.num_kv_heads, d.head_dim)]))
+                hist_v.append(torch.cat([pv, randn(c - P, d.num_kv_heads, d.head_dim)]))
+            else:
+                hist_k.append(randn(c, d.num_kv_heads, d.head_dim))
+                hist_v.append(randn(c, d.num_kv_heads, d.head_dim))
     k_cache = v_cache = None
     if with_pool:
         k_cache = randn(d.num_slots, d.num_kv_heads, d.head_dim)
