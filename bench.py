@@ -364,8 +364,12 @@ def run_ours(args, rank, world, local):
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     E = lambda: torch.cuda.Event(enable_timing=True)
 
+    # the product's step is one rb_step call (one memset, two launches); --four-calls times the
+    # four separate entry points instead
+    step_fn = rb.run_step if args.four_calls else rb.run_step_fused
     for _ in range(args.warmup):
         flush.zero_()
+        step_fn(buf)
         rb.run_step(buf)
     torch.cuda.synchronize()
     if int(buf.meta["scalars"][3].item()) != 0:
@@ -377,19 +381,28 @@ def run_ours(args, rank, world, local):
     for ev in marks + attn_marks:
         ev.record()  # torch creates the handle lazily; the library re-records it in the step
     torch.cuda.synchronize()
-    graph = None
+    graph = graph_marked = None
     launches_per_step = None
     if not args.eager:
         # the step has only scalar host inputs and fixed-address buffers: capture it once and
-        # replay it, as a serving loop would, so host launch latency does not enter the step
+        # replay it, as a serving loop would, so host launch latency does not enter the step.
+        # The timed graph holds the library's launches only: an event-record node inside a
+        # graph costs ~3.5 us, so the per-call and per-kernel events live in a second graph of
+        # the same step, replayed after the timed region
         launches0 = rb.launch_count()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            rb.run_step(buf, marks=marks, attn_marks=attn_marks)
+            step_fn(buf)
         launches_per_step = rb.launch_count() - launches0
+        graph_marked = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph_marked):
+            rb.run_step(buf, marks=marks, attn_marks=attn_marks)
         graph.replay()
+        graph_marked.replay()
         torch.cuda.synchronize()
-    samples = []  # per step: the 8 event timestamps
+    E = lambda: torch.cuda.Event(enable_timing=True)
+    step_events = [(E(), E()) for _ in range(args.steps)]
+    samples = []  # per step of the breakdown pass: the 8 event timestamps
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
@@ -398,19 +411,37 @@ def run_ours(args, rank, world, local):
     w0 = time.perf_counter()
     for k in range(args.steps):
         flush.zero_()
+        a, b = step_events[k]
+        a.record()
         if graph is not None:
             graph.replay()
-        else:
+        elif args.four_calls:
             rb.run_step(buf, marks=marks, attn_marks=attn_marks)
+        else:
+            step_fn(buf)
+        b.record()
         torch.cuda.synchronize()
-        pts = [marks[0], marks[1], marks[2], attn_marks[0], attn_marks[1], attn_marks[2],
-               marks[3], marks[4]]
-        samples.append([pts[0].elapsed_time(p) for p in pts])
+        if graph is None and args.four_calls:
+            pts = [marks[0], marks[1], marks[2], attn_marks[0], attn_marks[1], attn_marks[2],
+                   marks[3], marks[4]]
+            samples.append([pts[0].elapsed_time(p) for p in pts])
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - w0
     launches = (launches_per_step * args.steps if graph is not None
                 else rb.launch_count() - launches0)
+    step_times = [a.elapsed_time(b) for a, b in step_events]
+    if not samples:  # breakdown pass: the same steps, four calls with events between launches
+        for k in range(args.steps):
+            flush.zero_()
+            if graph_marked is not None:
+                graph_marked.replay()
+            else:
+                rb.run_step(buf, marks=marks, attn_marks=attn_marks)
+            torch.cuda.synchronize()
+            pts = [marks[0], marks[1], marks[2], attn_marks[0], attn_marks[1], attn_marks[2],
+                   marks[3], marks[4]]
+            samples.append([pts[0].elapsed_time(p) for p in pts])
     clocks = sampler.stop()
 
     # timestamps: 0 start | 1 after prepare | 2 after kv_write | 3 after plan | 4 after decode |
@@ -422,7 +453,8 @@ def run_ours(args, rank, world, local):
     def kspan(a, b):  # inside the attention call: planner | decode kernel | prefill kernel
         return [s[2 + b] - s[2 + a] for s in samples]
 
-    step_ms = statistics.mean(span(0, 4))
+    step_ms = statistics.mean(step_times)
+    marked_step_ms = statistics.mean(span(0, 4))
     parts = {"prepare_inputs": span(0, 1), "kv_write": span(1, 2),
              "paged_attention": span(2, 3), "gather_rows": span(3, 4)}
     parts_ms = {k: statistics.mean(v) for k, v in parts.items()}
@@ -483,6 +515,11 @@ def run_ours(args, rank, world, local):
             "data": "synthetic (seeded N(0,1) bf16 Q/K/V/hidden, random page ids; no weights)",
             "config": workload_name(spec, args.config), "roofline": roof,
             "components_ms": parts_ms, "attention_kernels_ms": kernels_ms,
+            "step_entry": "four calls" if args.four_calls else "rb_step (one memset, two launches)",
+            "breakdown": ("per-call and per-kernel spans from a second pass of the same steps "
+                          "through the four separate calls with events recorded between the "
+                          f"launches (step {marked_step_ms:.4f} ms there; an event node in a "
+                          "graph adds ~3.5 us, so these spans overstate the kernels slightly)"),
             "work": {"prefill_tflop": w["prefill_flops"] / 1e12,
                      "decode_kv_gb": w["decode_bytes"] / 1e9,
                      "attention_call_tflops": w["attn_flops"] / attn_s / 1e12,
@@ -524,10 +561,12 @@ def measure_e2e(spec, tens, buf, dev, args, flush, world):
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
+    step_fn = rb.run_step if args.four_calls else rb.run_step_fused
+
     def step():
         for k, t in host_in.items():
             dst[k].copy_(t, non_blocking=True)
-        rb.run_step(buf)
+        step_fn(buf)
         for k, t in host_out.items():
             t.copy_(src_out[k], non_blocking=True)
 
@@ -603,7 +642,7 @@ def run_trajectory(args, rank, world, local):
         b = dataclasses.replace(buf, num_reqs=R, num_reqs_padded=R, num_tokens=N,
                                 num_tokens_padded=N, q=q[:N], k=k[:N], v=v[:N], hidden=hidden[:N],
                                 attn_out=buf.attn_out[:N])
-        rb.run_step(b)
+        rb.run_step_fused(b)
         ev[3].record()
         host_rows[:R].copy_(b.rows_out[:R], non_blocking=True)
         host_scalars.copy_(b.meta["scalars"], non_blocking=True)
@@ -748,6 +787,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="launch every step from Python instead of replaying a captured graph")
+    ap.add_argument("--four-calls", action="store_true",
+                    help="time the four separate entry points instead of the one rb_step call")
     ap.add_argument("--manager-ratio", type=int, default=1,
                     help="--config 2/3: page tables of manager blocks of this many kernel pages")
     ap.add_argument("--cascade", action="store_true",

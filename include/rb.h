@@ -8,6 +8,7 @@
  *   rb_kv_write         this step's new K/V rows -> paged KV cache (by slot_mapping)
  *   rb_paged_attention  varlen causal GQA attention through the page table
  *   rb_gather_rows      hidden rows at logits_indices (the rows the LM head needs)
+ *   rb_step             all four in one call (one memset and two launches)
  *
  * and, before rb_prepare_inputs, the runner's per-step merge of scheduler deltas into the
  * persistent batch:
@@ -314,6 +315,54 @@ rb_status rb_paged_attention_cascade(const rb_dims* dims, int32_t num_reqs, int3
 rb_status rb_gather_rows(int32_t num_rows, int32_t hidden_size, int32_t num_hidden_rows,
                          const void* d_hidden, const int32_t* d_indices, void* d_out,
                          int32_t* d_error_word, void* stream);
+
+/*
+ * rb_step — the whole step in one call: rb_prepare_inputs, rb_kv_write (the step's K/V at
+ * slot_mapping), rb_paged_attention and rb_gather_rows (hidden rows at logits_indices), with
+ * the same results bit for bit, enqueued as one memset and two launches instead of five
+ * launches: one preparation kernel writes the metadata, copies the K/V rows, gathers the hidden
+ * rows and plans the attention; the attention launch follows.  Sources: those of the four
+ * calls.  Arguments are those of the four calls, gathered in one struct (all device pointers
+ * but `dims`; the scalars' error word collects every call's bits and is zeroed here).
+ * Errors: the host checks of the four calls; device bits as the four calls set them.
+ */
+typedef struct rb_step_args {
+  const rb_dims* dims;
+  int32_t num_reqs, num_reqs_padded, num_tokens, num_tokens_padded;
+  int32_t hidden_size;      /* columns of d_hidden / d_rows_out */
+  int32_t num_hidden_rows;  /* rows of d_hidden (normally num_tokens_padded) */
+  float softmax_scale;
+  /* persistent batch (rb_prepare_inputs) */
+  const int32_t* d_token_table;
+  const int32_t* d_num_computed;
+  const int32_t* d_num_scheduled;
+  const int32_t* d_block_table;
+  const int32_t* d_num_prompt; /* optional, with the two flag outputs */
+  /* this step's activations and the paged cache */
+  const void* d_q;      /* [num_tokens_padded, nh, hd] bf16 */
+  const void* d_k;      /* [num_tokens_padded, nkv, hd] bf16 */
+  const void* d_v;
+  const void* d_hidden; /* [num_hidden_rows, hidden_size] bf16 */
+  void* d_k_cache;      /* [num_blocks * block_size, nkv, hd] bf16 */
+  void* d_v_cache;
+  /* outputs */
+  int32_t* d_input_ids;
+  int32_t* d_positions;
+  int32_t* d_query_start_loc;
+  int32_t* d_seq_lens;
+  int32_t* d_slot_mapping;
+  int32_t* d_logits_indices;
+  int32_t* d_scalars;
+  int32_t* d_is_prefilling;         /* optional */
+  int32_t* d_discard_request_mask;  /* optional */
+  void* d_attn_out;  /* [num_tokens_padded, nh, hd] bf16 */
+  void* d_rows_out;  /* [num_reqs_padded, hidden_size] bf16 */
+  /* attention workspace: rb_paged_attention_workspace_size(dims, num_reqs, num_tokens) */
+  void* d_workspace;
+  size_t workspace_bytes;
+} rb_step_args;
+
+rb_status rb_step(const rb_step_args* args, void* stream);
 
 /*
  * Persistent batch — one row per resident request, every column device-resident and

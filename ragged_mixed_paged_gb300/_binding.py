@@ -65,6 +65,21 @@ class rb_batch_update(ctypes.Structure):
             "d_cached_blocks")]
 
 
+class rb_step_args(ctypes.Structure):
+    _fields_ = ([("dims", ctypes.POINTER(rb_dims))] +
+                [(n, ctypes.c_int32) for n in ("num_reqs", "num_reqs_padded", "num_tokens",
+                                               "num_tokens_padded", "hidden_size",
+                                               "num_hidden_rows")] +
+                [("softmax_scale", ctypes.c_float)] +
+                [(n, ctypes.c_void_p) for n in (
+                    "d_token_table", "d_num_computed", "d_num_scheduled", "d_block_table",
+                    "d_num_prompt", "d_q", "d_k", "d_v", "d_hidden", "d_k_cache", "d_v_cache",
+                    "d_input_ids", "d_positions", "d_query_start_loc", "d_seq_lens",
+                    "d_slot_mapping", "d_logits_indices", "d_scalars", "d_is_prefilling",
+                    "d_discard_request_mask", "d_attn_out", "d_rows_out", "d_workspace")] +
+                [("workspace_bytes", ctypes.c_size_t)])
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -90,6 +105,7 @@ def _load():
         "rb_gather_rows": (I32, [I32, I32, I32, P, P, P, P, P]),
         "rb_batch_update_workspace_size": (I32, [I32, ctypes.POINTER(ctypes.c_size_t)]),
         "rb_cascade_prefix_len": (I32, [I32, P, I32, I32]),
+        "rb_step": (I32, [ctypes.POINTER(rb_step_args), P]),
         "rb_paged_attention_cascade_workspace_size": (ctypes.c_size_t, [PD, I32, I32]),
         "rb_paged_attention_cascade": (I32, [PD, I32, I32, I32, I32, P, P, P, P, P, P,
                                              ctypes.c_float, P, P, ctypes.c_size_t, P, P]),

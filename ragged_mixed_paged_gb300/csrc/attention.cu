@@ -16,7 +16,7 @@
 //      merges the partials) and prefill units (tcgen05 tiles), starting with the kind the
 //      planner assigned it and then helping with the other, so HBM-bound and tensor-bound work
 //      overlap; other groups run a decode launch and an mma.sync prefill launch instead.
-#include "attn_common.cuh"
+#include "attn_plan.cuh"
 
 namespace rb {
 namespace attn {
@@ -24,137 +24,8 @@ namespace {
 
 constexpr int kPlanThreads = 1024;
 
-// Block-wide exclusive scan of two int32 values per thread; returns totals via *tot.
-__device__ void block_scan2(int v0, int v1, int* ex0, int* ex1, int* tot0, int* tot1) {
-  __shared__ int s0[32], s1[32];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  int i0 = v0, i1 = v1;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int a = __shfl_up_sync(0xffffffffu, i0, o);
-    const int b = __shfl_up_sync(0xffffffffu, i1, o);
-    if (lane >= o) { i0 += a; i1 += b; }
-  }
-  if (lane == 31) { s0[warp] = i0; s1[warp] = i1; }
-  __syncthreads();
-  if (warp == 0) {
-    int w0 = lane < nw ? s0[lane] : 0, w1 = lane < nw ? s1[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int a = __shfl_up_sync(0xffffffffu, w0, o);
-      const int b = __shfl_up_sync(0xffffffffu, w1, o);
-      if (lane >= o) { w0 += a; w1 += b; }
-    }
-    s0[lane] = w0;
-    s1[lane] = w1;
-  }
-  __syncthreads();
-  *ex0 = i0 - v0 + (warp > 0 ? s0[warp - 1] : 0);
-  *ex1 = i1 - v1 + (warp > 0 ? s1[warp - 1] : 0);
-  *tot0 = s0[nw - 1];
-  *tot1 = s1[nw - 1];
-  __syncthreads();
-}
-
-struct ReqInfo {
-  bool ok;
-  int q, L, pages;
-};
-
-__device__ __forceinline__ ReqInfo req_info(const AttnArgs& a, int r) {
-  ReqInfo x;
-  const int s = a.qsl[r], e = a.qsl[r + 1];
-  x.q = e - s;
-  x.L = a.seq_lens[r];
-  x.pages = (x.L + kPage - 1) / kPage;
-  x.ok = s >= 0 && x.q >= 0 && e <= a.N && x.L >= x.q && x.pages <= a.kp_cap;
-  return x;
-}
-
 __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(AttnArgs a, int head_dim) {
-  __shared__ unsigned long long s_pages;
-  __shared__ float s_flops;
-  const int tid = threadIdx.x;
-  const int per = (a.R + kPlanThreads - 1) / kPlanThreads;
-  const int lo = min(tid * per, a.R), hi = min(lo + per, a.R);
-  int bits = 0;
-  if (tid == 0) {
-    s_pages = 0;
-    s_flops = 0.f;
-    if (a.qsl[0] != 0 || a.qsl[a.R] != a.N) bits |= RB_EBIT_ATTN_META;
-  }
-  __syncthreads();
-  unsigned long long my_pages = 0;
-  float my_flops = 0.f;  // prefill work: 4 * nh * hd * visible keys
-  for (int r = lo; r < hi; ++r) {
-    const ReqInfo x = req_info(a, r);
-    if (!x.ok) { bits |= RB_EBIT_ATTN_META; continue; }
-    if (is_decode_class(x.q, a.group)) {
-      my_pages += static_cast<unsigned long long>(x.pages);
-    } else {
-      const float c = static_cast<float>(x.L - x.q), q = static_cast<float>(x.q);
-      my_flops += 4.f * a.nh * head_dim * (q * c + 0.5f * q * (q + 1.f));
-    }
-  }
-  if (my_pages) atomicAdd(&s_pages, my_pages);
-  if (my_flops > 0.f) atomicAdd(&s_flops, my_flops);
-  __syncthreads();
-  const long long page_heads = static_cast<long long>(s_pages) * a.nkv;
-  // Fused launch: split the CTAs between decode (HBM-bound) and prefill (tensor-bound) so both
-  // finish together; CTAs that run out of their own work then help with the other kind.
-  // Rates per SM: ~80 GB/s of paged K/V for decode, ~7 TFLOP/s for prefill tiles.  Splits are
-  // sized for every CTA of the launch (all of them may end up helping with decode), so the
-  // decode tail stays short.
-  int decode_ctas = 0;
-  int target = a.target_units;
-  if (a.fused_ctas > 0) {
-    const float dec_bytes = static_cast<float>(page_heads) * (2.f * kPage * head_dim * 2.f);
-    const float t_dec = dec_bytes / 80e3f;   // microseconds on one SM
-    const float t_pre = s_flops / 7e6f;
-    if (t_dec > 0.f) {
-      const float share = t_pre > 0.f ? t_dec / (t_dec + t_pre) : 1.f;
-      decode_ctas = max(1, min(a.fused_ctas, static_cast<int>(share * a.fused_ctas + 0.5f)));
-    }
-    target = min(kMaxTargetUnits, 4 * a.decode_warps_per_cta * a.fused_ctas);
-  }
-  const int sp = static_cast<int>(max(static_cast<long long>(kMinSplitPages),
-                                      (page_heads + target - 1) / target));
-  int my_d = 0, my_p = 0;
-  for (int r = lo; r < hi; ++r) {
-    const ReqInfo x = req_info(a, r);
-    if (!x.ok || x.q == 0) continue;
-    if (is_decode_class(x.q, a.group)) my_d += (x.pages + sp - 1) / sp * a.nkv;
-    else my_p += (x.q * a.group + a.tile_m - 1) / a.tile_m * a.nkv;
-  }
-  int ex_d, ex_p, tot_d, tot_p;
-  block_scan2(my_d, my_p, &ex_d, &ex_p, &tot_d, &tot_p);
-  for (int r = lo; r < hi; ++r) {
-    const ReqInfo x = req_info(a, r);
-    a.dec_off[r] = ex_d;
-    a.pre_off[r] = ex_p;
-    if (!x.ok || x.q == 0) continue;
-    if (is_decode_class(x.q, a.group)) ex_d += (x.pages + sp - 1) / sp * a.nkv;
-    else ex_p += (x.q * a.group + a.tile_m - 1) / a.tile_m * a.nkv;
-  }
-  if (tid == 0) {
-    a.dec_off[a.R] = tot_d;
-    a.pre_off[a.R] = tot_p;
-    a.header[kHNumDecodeUnits] = tot_d;
-    a.header[kHNumPrefillUnits] = tot_p;
-    a.header[kHDecodeNext] = 0;
-    a.header[kHPrefillNext] = 0;
-    a.header[kHSplitPages] = sp;
-    a.header[kHDecodeCtas] = decode_ctas;
-    a.header[kHRoleNext] = 0;
-  }
-  for (int i = tid; i < a.R * a.nkv; i += kPlanThreads) a.done[i] = 0;
-  // rows of padding tokens are written as zeros
-  const long long row16 = static_cast<long long>(a.nh) * head_dim * 2 / 16;
-  int4* out = reinterpret_cast<int4*>(a.out);
-  const long long first = static_cast<long long>(a.N) * row16;
-  const long long last = static_cast<long long>(a.N_pad) * row16;
-  for (long long i = first + tid; i < last; i += kPlanThreads) out[i] = make_int4(0, 0, 0, 0);
-  if (bits) raise_error(a.err, bits);
+  plan_body(a, head_dim);
 }
 
 // Cascade: checks the shared prefix, writes the suffix pass's sequence lengths (seq_len - P)
@@ -201,18 +72,15 @@ extern "C" size_t rb_paged_attention_workspace_size(const rb_dims* dims, int32_t
   return rb::attn::ws_layout(dims->head_dim, dims->num_kv_heads, max_num_reqs).total;
 }
 
-namespace {
+namespace rb {
+namespace attn {
 
-rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
-                               int32_t num_tokens_padded, const void* d_q, const void* d_k_cache,
-                               const void* d_v_cache, const int32_t* d_block_table,
-                               const int32_t* d_query_start_loc, const int32_t* d_seq_lens,
-                               float softmax_scale, void* d_out, void* d_workspace,
-                               size_t workspace_bytes, int32_t* d_error_word, void* stream,
-                               void* const* events, int32_t num_events,
-                               int32_t prefix_len = 0) {
-  using namespace rb;
-  using namespace rb::attn;
+rb_status attn_setup(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
+                     int32_t num_tokens_padded, const void* d_q, const void* d_k_cache,
+                     const void* d_v_cache, const int32_t* d_block_table,
+                     const int32_t* d_query_start_loc, const int32_t* d_seq_lens,
+                     float softmax_scale, void* d_out, void* d_workspace, size_t workspace_bytes,
+                     int32_t* d_error_word, AttnSetup* su) {
   if (dims == nullptr) return RB_ERR_INVALID_ARG;
   const rb_dims& d = *dims;
   if (d.block_size != kPage) return RB_ERR_UNSUPPORTED;
@@ -235,32 +103,18 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
     return RB_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(d.head_dim, d.num_kv_heads, num_reqs);
   if (workspace_bytes < w.total) return RB_ERR_CAPACITY;
-  // cascade: P page-aligned in whole page-table entries, within a row
-  if (prefix_len < 0 || prefix_len % (kPage * g.ratio) != 0 ||
-      prefix_len / (kPage * g.ratio) > d.max_blocks_per_req)
-    return RB_ERR_INVALID_ARG;
-  if (num_reqs == 0 || num_tokens == 0) prefix_len = 0;  // nothing shares anything
-  const CascadeLayout cl =
-      cascade_layout(d.head_dim, d.num_q_heads, d.num_kv_heads, num_reqs, num_tokens);
-  if (prefix_len > 0 && workspace_bytes < cl.total) return RB_ERR_CAPACITY;
-  if (prefix_len > 0 && !prefill_tc_supported(d.head_dim, d.num_q_heads / d.num_kv_heads))
-    return RB_ERR_UNSUPPORTED;
-
-  CUtensorMap kmap, vmap;
-  const long long num_slots = static_cast<long long>(d.num_blocks) * kPage;
-  if (!encode_kv_tensor_map(&kmap, d_k_cache, d.head_dim, d.num_kv_heads, num_slots) ||
-      !encode_kv_tensor_map(&vmap, d_v_cache, d.head_dim, d.num_kv_heads, num_slots))
-    return RB_ERR_CUDA;
 
   const int group = d.num_q_heads / d.num_kv_heads;
-  const bool use_tc = prefill_tc_supported(d.head_dim, group);
-  CUtensorMap qmap;
-  if (use_tc && num_tokens_padded > 0 &&
-      !encode_q_tensor_map(&qmap, d_q, d.head_dim, d.num_q_heads, num_tokens_padded, group))
-    return RB_ERR_CUDA;
-
+  su->g = g;
+  su->head_dim = d.head_dim;
+  su->use_tc = prefill_tc_supported(d.head_dim, group);
+  su->k_cache = d_k_cache;
+  su->v_cache = d_v_cache;
+  su->num_kv_heads = d.num_kv_heads;
+  su->num_slots = static_cast<long long>(d.num_blocks) * kPage;
   uint8_t* ws = static_cast<uint8_t*>(d_workspace);
-  AttnArgs a{};
+  AttnArgs& a = su->a;
+  a = AttnArgs{};
   a.q = static_cast<const __nv_bfloat16*>(d_q);
   a.out = static_cast<__nv_bfloat16*>(d_out);
   a.block_table = d_block_table;
@@ -277,7 +131,7 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
   a.N_pad = num_tokens_padded;
   a.nh = d.num_q_heads;
   a.nkv = d.num_kv_heads;
-  a.group = d.num_q_heads / d.num_kv_heads;
+  a.group = group;
   a.MB = d.max_blocks_per_req;
   a.num_blocks = d.num_blocks;
   a.null_block = d.null_block;
@@ -285,16 +139,108 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
   a.kp_cap = static_cast<long long>(d.max_blocks_per_req) * g.ratio;
   const int sms = max(1, device_sm_count());
   a.target_units = min(kMaxTargetUnits, 32 * sms);
-  a.tile_m = use_tc ? 256 : kPrefillTileM;  // tcgen05 units are pairs of 128-row tiles
-  a.fused_ctas = use_tc ? sms : 0;
+  a.tile_m = su->use_tc ? 256 : kPrefillTileM;  // tcgen05 units are pairs of 128-row tiles
+  a.fused_ctas = su->use_tc ? sms : 0;
   a.decode_warps_per_cta = 8;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.err = d_error_word;
+  return RB_OK;
+}
 
+rb_status attn_encode_maps(AttnSetup* su) {
+  const AttnArgs& a = su->a;
+  if (!encode_kv_tensor_map(&su->kmap, su->k_cache, su->head_dim, su->num_kv_heads,
+                            su->num_slots) ||
+      !encode_kv_tensor_map(&su->vmap, su->v_cache, su->head_dim, su->num_kv_heads,
+                            su->num_slots))
+    return RB_ERR_CUDA;
+  if (su->use_tc && a.N_pad > 0 &&
+      !encode_q_tensor_map(&su->qmap, a.q, su->head_dim, a.nh, a.N_pad, a.group))
+    return RB_ERR_CUDA;
+  return RB_OK;
+}
+
+template <class Mark>
+rb_status attn_main_impl(const AttnSetup& su, cudaStream_t s, const Mark& mark) {
+  const AttnArgs& a = su.a;
+  rb_status st = RB_OK;
+  if (su.use_tc) {  // one launch runs decode and prefill units side by side
+    if (!mark(1)) return RB_ERR_CUDA;
+    if (a.R > 0) st = launch_prefill_tc(a, su.head_dim, su.qmap, su.kmap, su.vmap, s);
+    if (st != RB_OK) return st;
+    if (!mark(2)) return RB_ERR_CUDA;
+    return RB_OK;
+  }
+  if (a.R > 0) st = launch_decode(a, su.head_dim, su.kmap, su.vmap, s);
+  if (st != RB_OK) return st;
+  if (!mark(1)) return RB_ERR_CUDA;
+  if (a.R > 0) st = launch_prefill(a, su.head_dim, su.kmap, su.vmap, s);
+  if (st != RB_OK) return st;
+  if (!mark(2)) return RB_ERR_CUDA;
+  return RB_OK;
+}
+
+rb_status attn_main(const AttnSetup& su, cudaStream_t s) {
+  return attn_main_impl(su, s, [](int) { return true; });
+}
+
+}  // namespace attn
+}  // namespace rb
+
+namespace {
+
+// Event marks between the launches of one call (profiling); inside a stream capture the
+// records become graph nodes.
+struct Marks {
+  void* const* events;
+  int n;
+  cudaStream_t s;
+  bool capturing;
+  bool operator()(int i) const {
+    return i >= n || events[i] == nullptr ||
+           cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), s,
+                                    capturing ? cudaEventRecordExternal
+                                              : cudaEventRecordDefault) == cudaSuccess;
+  }
+};
+
+rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
+                               int32_t num_tokens_padded, const void* d_q, const void* d_k_cache,
+                               const void* d_v_cache, const int32_t* d_block_table,
+                               const int32_t* d_query_start_loc, const int32_t* d_seq_lens,
+                               float softmax_scale, void* d_out, void* d_workspace,
+                               size_t workspace_bytes, int32_t* d_error_word, void* stream,
+                               void* const* events, int32_t num_events,
+                               int32_t prefix_len = 0) {
+  using namespace rb;
+  using namespace rb::attn;
+  AttnSetup su;
+  rb_status st = attn_setup(dims, num_reqs, num_tokens, num_tokens_padded, d_q, d_k_cache,
+                            d_v_cache, d_block_table, d_query_start_loc, d_seq_lens,
+                            softmax_scale, d_out, d_workspace, workspace_bytes, d_error_word,
+                            &su);
+  if (st != RB_OK) return st;
+  const rb_dims& d = *dims;
+  const PageGeom& g = su.g;
+  AttnArgs& a = su.a;
+  // cascade: P page-aligned in whole page-table entries, within a row
+  if (prefix_len < 0 || prefix_len % (kPage * g.ratio) != 0 ||
+      prefix_len / (kPage * g.ratio) > d.max_blocks_per_req)
+    return RB_ERR_INVALID_ARG;
+  if (num_reqs == 0 || num_tokens == 0) prefix_len = 0;  // nothing shares anything
+  const CascadeLayout cl =
+      cascade_layout(d.head_dim, d.num_q_heads, d.num_kv_heads, num_reqs, num_tokens);
+  if (prefix_len > 0 && workspace_bytes < cl.total) return RB_ERR_CAPACITY;
+  if (prefix_len > 0 && !su.use_tc) return RB_ERR_UNSUPPORTED;
+  st = attn_encode_maps(&su);
+  if (st != RB_OK) return st;
+
+  uint8_t* ws = static_cast<uint8_t*>(d_workspace);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (prefix_len > 0) {
     // "8.3.2.5 Cascade Attention": the shared prefix once for every query row, then the
     // ordinary causal pass over each request's own keys [P, seq_len), merged per row
+    const int group = a.group;
     const int entries = prefix_len / (kPage * g.ratio);
     int32_t* lens = reinterpret_cast<int32_t*>(ws + cl.lens);
     a.pre_lse = reinterpret_cast<float*>(ws + cl.lse);
@@ -316,7 +262,7 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
     cascade_prepare_kernel<<<1, kPlanThreads, 0, s>>>(ap, prefix_len, entries, lens);
     if (last_launch_status() != RB_OK) return RB_ERR_CUDA;
     note_launches(1);
-    const rb_status st = launch_prefill_tc(ap, d.head_dim, qmap, kmap, vmap, s);
+    st = launch_prefill_tc(ap, d.head_dim, su.qmap, su.kmap, su.vmap, s);
     if (st != RB_OK) return st;
     a.cascade = kSuffixPass;
     a.seq_lens = lens;
@@ -325,32 +271,12 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
   }
   cudaStreamCaptureStatus capturing = cudaStreamCaptureStatusNone;
   if (num_events > 0 && cudaStreamIsCapturing(s, &capturing) != cudaSuccess) return RB_ERR_CUDA;
-  auto mark = [&](int i) -> bool {  // inside a stream capture the records become graph nodes
-    return i >= num_events || events[i] == nullptr ||
-           cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), s,
-                                    capturing == cudaStreamCaptureStatusActive
-                                        ? cudaEventRecordExternal
-                                        : cudaEventRecordDefault) == cudaSuccess;
-  };
+  const Marks mark{events, num_events, s, capturing == cudaStreamCaptureStatusActive};
   attn_plan_kernel<<<1, kPlanThreads, 0, s>>>(a, d.head_dim);
   if (last_launch_status() != RB_OK) return RB_ERR_CUDA;
   note_launches(1);
   if (!mark(0)) return RB_ERR_CUDA;
-  rb_status st = RB_OK;
-  if (use_tc) {  // one launch runs decode and prefill units side by side
-    if (!mark(1)) return RB_ERR_CUDA;
-    if (num_reqs > 0) st = launch_prefill_tc(a, d.head_dim, qmap, kmap, vmap, s);
-    if (st != RB_OK) return st;
-    if (!mark(2)) return RB_ERR_CUDA;
-    return RB_OK;
-  }
-  if (num_reqs > 0) st = launch_decode(a, d.head_dim, kmap, vmap, s);
-  if (st != RB_OK) return st;
-  if (!mark(1)) return RB_ERR_CUDA;
-  if (num_reqs > 0) st = launch_prefill(a, d.head_dim, kmap, vmap, s);
-  if (st != RB_OK) return st;
-  if (!mark(2)) return RB_ERR_CUDA;
-  return RB_OK;
+  return attn_main_impl(su, s, mark);
 }
 
 }  // namespace

@@ -152,6 +152,30 @@ __host__ __device__ inline bool is_decode_class(int q, int group) {
   return q >= 1 && q * group <= kMaxCols;
 }
 
+// Host side of one attention call: checked arguments, kernel arguments and TMA descriptors.
+struct AttnSetup {
+  AttnArgs a;
+  PageGeom g;
+  int head_dim, num_kv_heads;
+  bool use_tc;  // decode and prefill units in one tcgen05 launch
+  const void* k_cache;
+  const void* v_cache;
+  long long num_slots;
+  CUtensorMap qmap, kmap, vmap;
+};
+
+// Host checks and kernel arguments of rb_paged_attention (no launch, no driver call).
+rb_status attn_setup(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
+                     int32_t num_tokens_padded, const void* d_q, const void* d_k_cache,
+                     const void* d_v_cache, const int32_t* d_block_table,
+                     const int32_t* d_query_start_loc, const int32_t* d_seq_lens,
+                     float softmax_scale, void* d_out, void* d_workspace, size_t workspace_bytes,
+                     int32_t* d_error_word, AttnSetup* su);
+// Encodes the TMA descriptors of a set-up call.
+rb_status attn_encode_maps(AttnSetup* su);
+// Enqueues what follows the planner: the fused launch, or the decode and prefill launches.
+rb_status attn_main(const AttnSetup& su, cudaStream_t s);
+
 rb_status launch_decode(const AttnArgs& a, int head_dim, const CUtensorMap& kmap,
                         const CUtensorMap& vmap, cudaStream_t s);
 rb_status launch_prefill(const AttnArgs& a, int head_dim, const CUtensorMap& kmap,

@@ -1,0 +1,152 @@
+// rb_step: one whole step of the hot path — metadata, KV write, attention and the last-token
+// row gather — in one memset and two launches.
+//
+// The four separate calls (rb_prepare_inputs, rb_kv_write, rb_paged_attention, rb_gather_rows)
+// cost five launches, each of which waits for cold metadata before it can start.  Here one
+// preparation launch does everything that only needs the batch's metadata:
+//   - every CTA recomputes the prefix sum of num_scheduled in shared memory (as
+//     rb_prepare_inputs does), so each knows the owner of any token and any request's last row;
+//   - CTA 0 writes the per-request outputs and then runs the attention planner on them;
+//   - one warp per token writes its input id, position and slot and copies the token's K and V
+//     rows into that slot (16-byte accesses, lanes over the row);
+//   - one warp per request copies the hidden row at its logits index.
+// The attention launch (fused decode + prefill, or decode and prefill) follows on the stream.
+// Results are those of the four calls in order, bit for bit.
+//
+// Sources: "vLLM 源码完全拆解（五）…" 第一步 .. 第四步, "Block table 是逐请求的页表",
+// "3. 物理 KV 槽位", "4. 注意力读取边界"; "变长批处理与一次混合前向", runner.py (write K/V, then
+// attend); "04 · 模型执行与 CUDA Graph", step ⑤ (hidden_states[logits_indices]).
+#include "attn_plan.cuh"
+#include "prep_common.cuh"
+
+namespace rb {
+namespace {
+
+constexpr int kWarps = prep::kThreads / 32;
+
+struct StepArgs {
+  prep::PrepArgs p;
+  attn::AttnArgs at;
+  int head_dim;
+  const int4* k;
+  const int4* v;
+  int4* kc;
+  int4* vc;
+  int kv_chunks;  // 16-byte chunks per token row of K (or V)
+  long long num_slots;
+  const int4* hidden;
+  int4* rows_out;
+  int hid_chunks;  // 16-byte chunks per hidden row
+  int num_hidden_rows;
+};
+
+__global__ void __launch_bounds__(prep::kThreads) step_prep_kernel(StepArgs s) {
+  using namespace prep;
+  extern __shared__ int32_t s_qsl[];  // [R + 1]
+  const PrepArgs& a = s.p;
+  int32_t* err = a.scalars + 3;
+  block_scan_scheduled(a, s_qsl);
+  const int total = s_qsl[a.R];
+  if (blockIdx.x == 0) {
+    request_outputs(a, s_qsl, total, err);  // ends with a barrier: qsl / seq_lens are visible
+    attn::plan_body(s.at, s.head_dim);
+  }
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5), nw = gridDim.x * kWarps;
+  const int n_real = min(a.N, total);
+  for (int t = gw; t < a.N_pad; t += nw) {
+    int r = -1;
+    const TokMeta m = token_meta(a, s_qsl, n_real, t, r);
+    int bits = m.bits;
+    if (m.slot >= s.num_slots) bits |= RB_EBIT_SLOT;
+    if (lane == 0) {
+      a.input_ids[t] = m.id;
+      a.positions[t] = m.pos;
+      a.slots[t] = m.slot;
+      if (bits) raise_error(err, bits);
+    }
+    if (m.slot < 0 || m.slot >= s.num_slots) continue;
+    const long long src = static_cast<long long>(t) * s.kv_chunks;
+    const long long dst = static_cast<long long>(m.slot) * s.kv_chunks;
+    for (int c = lane; c < s.kv_chunks; c += 32) {
+      const int4 kk = __ldg(s.k + src + c);
+      const int4 vv = __ldg(s.v + src + c);
+      s.kc[dst + c] = kk;
+      s.vc[dst + c] = vv;
+    }
+  }
+  for (int i = gw; i < a.R_pad; i += nw) {
+    const int row = i < a.R ? s_qsl[i + 1] - 1 : max(a.N - 1, 0);
+    const bool ok = row >= 0 && row < s.num_hidden_rows;
+    if (!ok && lane == 0) raise_error(err, RB_EBIT_ROW_INDEX);
+    int4* dst = s.rows_out + static_cast<long long>(i) * s.hid_chunks;
+    const int4* src = s.hidden + static_cast<long long>(ok ? row : 0) * s.hid_chunks;
+    for (int c = lane; c < s.hid_chunks; c += 32)
+      dst[c] = ok ? __ldg(src + c) : make_int4(0, 0, 0, 0);
+  }
+}
+
+}  // namespace
+}  // namespace rb
+
+extern "C" rb_status rb_step(const rb_step_args* args, void* stream) {
+  using namespace rb;
+  if (args == nullptr || args->dims == nullptr) return RB_ERR_INVALID_ARG;
+  const rb_step_args& x = *args;
+  const rb_dims& d = *x.dims;
+  prep::PrepArgs p;
+  rb_status st = prep::prep_args_of(
+      d, x.num_reqs, x.num_reqs_padded, x.num_tokens, x.num_tokens_padded, x.d_token_table,
+      x.d_num_computed, x.d_num_scheduled, x.d_block_table, x.d_input_ids, x.d_positions,
+      x.d_query_start_loc, x.d_seq_lens, x.d_slot_mapping, x.d_logits_indices, x.d_scalars,
+      x.d_num_prompt, x.d_is_prefilling, x.d_discard_request_mask, &p);
+  if (st != RB_OK) return st;
+  // KV write and gather operands
+  const long long row_bytes = 2LL * d.num_kv_heads * d.head_dim;
+  if (row_bytes % 16 != 0 || (2LL * x.hidden_size) % 16 != 0) return RB_ERR_UNSUPPORTED;
+  if (x.hidden_size < 1 || x.num_hidden_rows < 0) return RB_ERR_INVALID_ARG;
+  if (x.num_tokens_padded > 0 && (x.d_k == nullptr || x.d_v == nullptr)) return RB_ERR_INVALID_ARG;
+  if (x.num_reqs_padded > 0 && (x.d_hidden == nullptr || x.d_rows_out == nullptr))
+    return RB_ERR_INVALID_ARG;
+  if (!aligned16(x.d_k) || !aligned16(x.d_v) || !aligned16(x.d_hidden) ||
+      !aligned16(x.d_rows_out))
+    return RB_ERR_INVALID_ARG;
+  attn::AttnSetup su;
+  st = attn::attn_setup(x.dims, x.num_reqs, x.num_tokens, x.num_tokens_padded, x.d_q,
+                        x.d_k_cache, x.d_v_cache, x.d_block_table, x.d_query_start_loc,
+                        x.d_seq_lens, x.softmax_scale, x.d_attn_out, x.d_workspace,
+                        x.workspace_bytes, x.d_scalars + 3, &su);
+  if (st != RB_OK) return st;
+  st = attn::attn_encode_maps(&su);
+  if (st != RB_OK) return st;
+
+  StepArgs sa;
+  sa.p = p;
+  sa.at = su.a;
+  sa.head_dim = d.head_dim;
+  sa.k = static_cast<const int4*>(x.d_k);
+  sa.v = static_cast<const int4*>(x.d_v);
+  sa.kc = static_cast<int4*>(x.d_k_cache);
+  sa.vc = static_cast<int4*>(x.d_v_cache);
+  sa.kv_chunks = static_cast<int>(row_bytes / 16);
+  sa.num_slots = static_cast<long long>(d.num_blocks) * d.block_size;
+  sa.hidden = static_cast<const int4*>(x.d_hidden);
+  sa.rows_out = static_cast<int4*>(x.d_rows_out);
+  sa.hid_chunks = static_cast<int>(2LL * x.hidden_size / 16);
+  sa.num_hidden_rows = x.num_hidden_rows;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(x.d_scalars + 3, 0, sizeof(int32_t), s) != cudaSuccess) return RB_ERR_CUDA;
+  const size_t smem = static_cast<size_t>(x.num_reqs + 1) * sizeof(int32_t);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(step_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return RB_ERR_CUDA;
+  const int sms = max(1, device_sm_count());
+  const int want = (max(x.num_tokens_padded, x.num_reqs_padded) + kWarps - 1) / kWarps;
+  const int grid = max(1, min(want, 2 * sms));
+  step_prep_kernel<<<grid, prep::kThreads, smem, s>>>(sa);
+  if (last_launch_status() != RB_OK) return RB_ERR_CUDA;
+  note_launches(1);
+  return attn::attn_main(su, s);
+}

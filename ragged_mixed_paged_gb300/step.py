@@ -2,10 +2,15 @@
 gather_rows, on one stream, with no host synchronisation inside.
 
 ``StepBuffers`` holds fixed-address device buffers sized once (as a CUDA-graph runner keeps
-them); ``run_step`` only enqueues the four library calls.  The step's error word is the fourth
-scalar written by ``prepare_inputs``; the KV write and the attention OR their bits into it.
+them); ``run_step`` enqueues the four library calls, ``run_step_fused`` the single ``rb_step``
+call that does the same work in one memset and two launches (same results, bit for bit).  The
+step's error word is the fourth scalar written by ``prepare_inputs``; the KV write and the
+attention OR their bits into it.
 """
 from __future__ import annotations
+
+import ctypes
+import math
 
 from dataclasses import dataclass
 from typing import Optional
@@ -35,6 +40,7 @@ class StepBuffers:
     workspace: object
     rows_out: object
     num_prompt: object = None  # int32 prompt lengths: enables is_prefilling / discard mask
+    _step_args: object = None  # rb_step_args built on first use (the buffers never move)
 
     @classmethod
     def allocate(cls, dims: rb.Dims, num_reqs: int, num_reqs_padded: int, num_tokens: int,
@@ -101,3 +107,32 @@ def run_step(b: StepBuffers, stream=None, softmax_scale: Optional[float] = None,
     rb.gather_rows(b.hidden, m["logits_indices"], num_rows=b.num_reqs_padded, out=b.rows_out,
                    error_word=b.error_word, stream=stream)
     mark(4)
+
+
+def _step_args(b: StepBuffers, softmax_scale: Optional[float]):
+    import torch
+
+    i32, bf = torch.int32, torch.bfloat16
+    m = b.meta
+    p = lambda t, dt=None: rb._ptr(t, dt).value
+    flags = b.num_prompt is not None
+    b._dims_c = b.dims.c()  # kept alive with the struct that points at it
+    scale = 1.0 / math.sqrt(b.dims.head_dim) if softmax_scale is None else softmax_scale
+    return rb.rb_step_args(
+        ctypes.pointer(b._dims_c), b.num_reqs, b.num_reqs_padded, b.num_tokens,
+        b.num_tokens_padded, b.hidden.shape[1], b.hidden.shape[0], scale,
+        p(b.token_table, i32), p(b.num_computed, i32), p(b.num_scheduled, i32),
+        p(b.block_table, i32), p(b.num_prompt, i32) if flags and b.num_prompt.numel() else None,
+        p(b.q, bf), p(b.k, bf), p(b.v, bf), p(b.hidden, bf), p(b.k_cache, bf), p(b.v_cache, bf),
+        p(m["input_ids"], i32), p(m["positions"], i32), p(m["query_start_loc"], i32),
+        p(m["seq_lens"], i32), p(m["slot_mapping"], i32), p(m["logits_indices"], i32),
+        p(m["scalars"], i32), p(m["is_prefilling"], i32) if flags else None,
+        p(m["discard_request_mask"], i32) if flags else None, p(b.attn_out, bf),
+        p(b.rows_out, bf), p(b.workspace, torch.uint8), b.workspace.numel())
+
+
+def run_step_fused(b: StepBuffers, stream=None, softmax_scale: Optional[float] = None) -> None:
+    """Enqueue the whole step as one ``rb_step`` call (one memset and two launches)."""
+    if b._step_args is None or softmax_scale is not None:
+        b._step_args = _step_args(b, softmax_scale)
+    rb._check("rb_step", rb.lib.rb_step(ctypes.byref(b._step_args), rb._stream(stream)))

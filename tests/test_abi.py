@@ -224,3 +224,15 @@ def test_cascade_attention_host_checks(lib):
     plain = L.rb_paged_attention_workspace_size(ctypes.byref(d), 2, 4)
     assert need > plain
     assert call(d, 16, ws_bytes=need - 1) == 2
+
+
+def test_step_host_checks(lib):
+    L = lib.lib
+    assert L.rb_step(None, None) == 1
+    args = lib.rb_step_args()
+    assert L.rb_step(ctypes.byref(args), None) == 1            # no dims
+    d = _dims(lib)
+    args.dims = ctypes.pointer(d)
+    args.num_reqs = args.num_reqs_padded = 1
+    args.num_tokens = args.num_tokens_padded = 1
+    assert L.rb_step(ctypes.byref(args), None) == 1            # no metadata buffers

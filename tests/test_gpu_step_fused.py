@@ -1,0 +1,111 @@
+"""rb_step (one memset and two launches) against the four separate calls: every output bit for
+bit — metadata, phase flags, both caches, attention output, gathered rows, error word — and,
+on a few cases, directly against the oracle."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as wl
+from gpu_cases import compare_attention, config4_specs, oracle_attention, oracle_meta
+
+pytestmark = pytest.mark.gpu
+
+
+def _buffers(rb, spec):
+    tens = wl.make_tensors(spec, device="cuda")
+    tables = wl.device_tables(spec, "cuda")
+    buf = rb.StepBuffers.allocate(rb.Dims.of(spec.dims), spec.num_reqs, spec.num_reqs_padded,
+                                  spec.num_tokens, spec.num_tokens_padded, tables, tens.q,
+                                  tens.k, tens.v, tens.hidden, tens.k_cache, tens.v_cache)
+    return buf, tens
+
+
+def _twins(rb, spec):
+    """Two StepBuffers over the same inputs, each with its own copy of the paged cache."""
+    a, tens = _buffers(rb, spec)
+    b, _ = _buffers(rb, spec)
+    b.k_cache.copy_(a.k_cache)
+    b.v_cache.copy_(a.v_cache)
+    return a, b, tens
+
+
+def _same(a, b):
+    for k in a.meta:
+        assert torch.equal(a.meta[k], b.meta[k]), k
+    assert torch.equal(a.k_cache, b.k_cache)
+    assert torch.equal(a.v_cache, b.v_cache)
+    assert torch.equal(a.attn_out, b.attn_out)
+    assert torch.equal(a.rows_out, b.rows_out)
+
+
+CASES = {
+    "cfg1": lambda: wl.config1(),
+    "cfg1_pad24": lambda: wl.config1(num_tokens_padded=24),
+    "cfg2": lambda: wl.config2(),
+    "cfg2_r2": lambda: wl.config2(manager_ratio=2),
+    "cfg3": lambda: wl.config3(),
+    "cfg3_pad": lambda: wl.config3(num_real=250),
+    "cfg5": lambda: wl.config5(),
+    "mix_step57": lambda: config4_specs()[57],
+    "many_decodes": lambda: wl.batch_from_lists([int(x) for x in np.arange(3000) % 300 + 1],
+                                                [1] * 3000, num_q_heads=8, num_kv_heads=2,
+                                                head_dim=128, seed=3),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_fused_step_equals_four_calls(rb, name):
+    spec = CASES[name]()
+    a, b, _ = _twins(rb, spec)
+    rb.run_step(a)
+    rb.run_step_fused(b)
+    torch.cuda.synchronize()
+    assert int(a.meta["scalars"][3].item()) == 0
+    _same(a, b)
+
+
+@pytest.mark.parametrize("seed", range(16))
+def test_fused_step_fuzz(rb, seed):
+    """Both attention paths (power-of-two groups fused, group 3 in two launches), padding."""
+    nh, nkv = [(32, 8), (6, 2), (8, 1), (4, 4)][seed % 4]
+    spec = wl.random_batch(seed, num_q_heads=nh, num_kv_heads=nkv, head_dim=[64, 128][seed % 2],
+                           max_reqs=9, max_q=150, max_c=300, pad_tokens=seed % 5,
+                           pad_reqs=seed % 3, manager_ratio=[1, 2, 4, 1][seed % 4])
+    a, b, _ = _twins(rb, spec)
+    rb.run_step(a)
+    rb.run_step_fused(b)
+    torch.cuda.synchronize()
+    _same(a, b)
+
+
+@pytest.mark.parametrize("name", ["cfg1_pad24", "fuzz"])
+def test_fused_step_vs_oracle(rb, name):
+    spec = (wl.config1(num_tokens_padded=24) if name == "cfg1_pad24" else
+            wl.random_batch(9, num_q_heads=8, num_kv_heads=2, head_dim=128, pad_tokens=3))
+    buf, tens = _buffers(rb, spec)
+    rb.run_step_fused(buf)
+    torch.cuda.synchronize()
+    assert int(buf.meta["scalars"][3].item()) == 0
+    want = oracle_meta(spec)
+    for k in ("input_ids", "positions", "query_start_loc", "seq_lens", "slot_mapping",
+              "logits_indices"):
+        assert np.array_equal(buf.meta[k].cpu().numpy(), want[k]), k
+    ref = oracle_attention(spec, tens, want)
+    compare_attention(buf.attn_out, ref, spec.num_tokens)
+    hid = tens.hidden.float().cpu().numpy()
+    rows = oracle.gather_rows(hid, want["logits_indices"])
+    assert np.array_equal(buf.rows_out.float().cpu().numpy(), rows)
+
+
+def test_fused_step_error_bits(rb):
+    """A page id outside the pool: the same bits, the same null-page routing."""
+    spec = wl.batch_from_lists([3, 0, 9], [2, 4, 1], block_size=16, seed=1,
+                               num_q_heads=4, num_kv_heads=2, head_dim=64)
+    spec.block_table[1, 0] = spec.dims.num_blocks + 5
+    a, b, _ = _twins(rb, spec)
+    rb.run_step(a)
+    rb.run_step_fused(b)
+    torch.cuda.synchronize()
+    assert int(a.meta["scalars"][3].item()) & 0x010
+    _same(a, b)
