@@ -69,7 +69,8 @@ extern "C" size_t rb_paged_attention_workspace_size(const rb_dims* dims, int32_t
   if (dims == nullptr || max_num_reqs < 0 || max_num_tokens < 0 || dims->num_kv_heads < 1 ||
       dims->head_dim < 1)
     return 0;
-  return rb::attn::ws_layout(dims->head_dim, dims->num_kv_heads, max_num_reqs).total;
+  return rb::attn::ws_layout(dims->head_dim, dims->num_kv_heads, max_num_reqs, max_num_tokens)
+      .total;
 }
 
 namespace rb {
@@ -101,7 +102,7 @@ rb_status attn_setup(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
   if (!aligned16(d_q) || !aligned16(d_k_cache) || !aligned16(d_v_cache) || !aligned16(d_out) ||
       (reinterpret_cast<uintptr_t>(d_workspace) & 255u) != 0)
     return RB_ERR_INVALID_ARG;
-  const WsLayout w = ws_layout(d.head_dim, d.num_kv_heads, num_reqs);
+  const WsLayout w = ws_layout(d.head_dim, d.num_kv_heads, num_reqs, num_tokens);
   if (workspace_bytes < w.total) return RB_ERR_CAPACITY;
 
   const int group = d.num_q_heads / d.num_kv_heads;
@@ -124,6 +125,7 @@ rb_status attn_setup(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
   a.dec_off = reinterpret_cast<int32_t*>(ws + w.dec_off);
   a.pre_off = reinterpret_cast<int32_t*>(ws + w.pre_off);
   a.done = reinterpret_cast<int32_t*>(ws + w.done);
+  a.pre_list = reinterpret_cast<int32_t*>(ws + w.pre_list);
   a.part_ml = reinterpret_cast<float2*>(ws + w.part_ml);
   a.part_o = reinterpret_cast<float*>(ws + w.part_o);
   a.R = num_reqs;

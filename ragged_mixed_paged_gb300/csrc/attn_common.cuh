@@ -25,13 +25,19 @@ enum HeaderField : int {
 };
 
 // Workspace: [header][decode unit offsets R+1][prefill unit offsets R+1]
-//            [finished-split counters R x nkv][partial (m, l)][partial o]
+//            [finished-split counters R x nkv][prefill pair list][partial (m, l)][partial o]
 struct WsLayout {
-  size_t header, dec_off, pre_off, done, part_ml, part_o, total;
+  size_t header, dec_off, pre_off, done, pre_list, part_ml, part_o, total;
   long long max_units;
 };
 
-inline WsLayout ws_layout(int head_dim, int num_kv_heads, int num_reqs) {
+// Prefill (request, 256-row pair) entries a batch can have: sum over requests of
+// ceil(q_i * group / 256) <= N * 16 / 256 + R for groups up to 16.
+__host__ __device__ inline long long max_prefill_pairs(int num_reqs, int num_tokens) {
+  return static_cast<long long>(num_tokens) / 16 + num_reqs + 1;
+}
+
+inline WsLayout ws_layout(int head_dim, int num_kv_heads, int num_reqs, int num_tokens) {
   WsLayout w{};
   size_t off = 0;
   auto take = [&off](size_t bytes) {
@@ -44,6 +50,7 @@ inline WsLayout ws_layout(int head_dim, int num_kv_heads, int num_reqs) {
   w.dec_off = take(static_cast<size_t>(num_reqs + 1) * sizeof(int32_t));
   w.pre_off = take(static_cast<size_t>(num_reqs + 1) * sizeof(int32_t));
   w.done = take(static_cast<size_t>(num_reqs) * num_kv_heads * sizeof(int32_t));
+  w.pre_list = take(static_cast<size_t>(max_prefill_pairs(num_reqs, num_tokens)) * sizeof(int32_t));
   w.part_ml = take(static_cast<size_t>(w.max_units) * kMaxCols * sizeof(float2));
   w.part_o = take(static_cast<size_t>(w.max_units) * kMaxCols * head_dim * sizeof(float));
   w.total = off;
@@ -67,7 +74,7 @@ struct CascadeLayout {
 inline CascadeLayout cascade_layout(int head_dim, int num_q_heads, int num_kv_heads, int num_reqs,
                                     int num_tokens) {
   CascadeLayout c{};
-  size_t off = ws_layout(head_dim, num_kv_heads, num_reqs).total;
+  size_t off = ws_layout(head_dim, num_kv_heads, num_reqs, num_tokens).total;
   auto take = [&off](size_t bytes) {
     const size_t o = off;
     off += (bytes + 255) & ~static_cast<size_t>(255);
@@ -91,6 +98,7 @@ struct AttnArgs {
   int32_t* dec_off;
   int32_t* pre_off;
   int32_t* done;  // per (request, kv head): decode splits finished so far
+  int32_t* pre_list;  // tcgen05 prefill (request, pair) entries, longest first: r * 65536 + pair
   float2* part_ml;
   float* part_o;
   int R, N, N_pad, nh, nkv, group, MB, num_blocks, null_block;

@@ -54,56 +54,52 @@ __device__ __forceinline__ ReqInfo req_info(const AttnArgs& a, int r) {
   return x;
 }
 
+// Key tiles (128 keys) of tcgen05 prefill unit `pair` (query rows [256 pair, 256 pair + 256)
+// of a request with c cached tokens and q new ones): the larger of its two 128-row tiles.
+__device__ __forceinline__ int pair_key_tiles(int c, int q, int group, int pair) {
+  const int rows = q * group, row0 = pair * 256;
+  const int last_row = min(row0 + (row0 + 128 < rows ? 256 : 128), rows) - 1;
+  return (c + last_row / group + 1 + 127) / 128;
+}
+
+// Finish-time model of the fused launch (microseconds, this GPU, cold caches; fitted to per-unit
+// timestamps and whole-launch times): a decode unit of p pages takes about 6 + 0.6 p on one
+// warp, a CTA streams at most ~73 GB/s of paged K/V and all of them together ~6.4 TB/s; a
+// tcgen05 prefill unit of n key tiles takes about 8 + 2.3 n on one CTA.
+constexpr float kDecUnitUs = 6.f, kDecPageUs = 0.6f, kDecBytesPerUsPerCta = 73e3f;
+constexpr float kHbmBytesPerUs = 6.4e6f;
+constexpr float kPreUnitUs = 8.f, kPreTileUs = 2.3f;
+constexpr int kTileBins = 512;  // histogram bins of prefill units by key tiles (longer: last bin)
+
 // The planner, run by one whole CTA of any size: validates the metadata, classifies requests,
-// splits the CTAs of a fused launch between decode and prefill work, sizes the KV splits,
-// writes per-request unit offsets and the header, clears the split counters and writes the
-// padding rows of the output as zeros.
+// sizes the KV splits, writes per-request unit offsets, lists the tcgen05 prefill units
+// longest first, splits the CTAs of a fused launch between decode and prefill work, writes the
+// header, clears the split counters and writes the padding rows of the output as zeros.
 __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim) {
   __shared__ unsigned long long s_pages;
-  __shared__ float s_flops;
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int per = (a.R + nthreads - 1) / nthreads;
   const int lo = min(tid * per, a.R), hi = min(lo + per, a.R);
   int bits = 0;
   if (tid == 0) {
     s_pages = 0;
-    s_flops = 0.f;
     if (a.qsl[0] != 0 || a.qsl[a.R] != a.N) bits |= RB_EBIT_ATTN_META;
   }
   __syncthreads();
   unsigned long long my_pages = 0;
-  float my_flops = 0.f;  // prefill work: 4 * nh * hd * visible keys
   for (int r = lo; r < hi; ++r) {
     const ReqInfo x = req_info(a, r);
     if (!x.ok) { bits |= RB_EBIT_ATTN_META; continue; }
-    if (is_decode_class(x.q, a.group)) {
-      my_pages += static_cast<unsigned long long>(x.pages);
-    } else {
-      const float c = static_cast<float>(x.L - x.q), q = static_cast<float>(x.q);
-      my_flops += 4.f * a.nh * head_dim * (q * c + 0.5f * q * (q + 1.f));
-    }
+    if (is_decode_class(x.q, a.group)) my_pages += static_cast<unsigned long long>(x.pages);
   }
   if (my_pages) atomicAdd(&s_pages, my_pages);
-  if (my_flops > 0.f) atomicAdd(&s_flops, my_flops);
   __syncthreads();
   const long long page_heads = static_cast<long long>(s_pages) * a.nkv;
-  // Fused launch: split the CTAs between decode (HBM-bound) and prefill (tensor-bound) so both
-  // finish together; CTAs that run out of their own work then help with the other kind.
-  // Rates per SM: ~80 GB/s of paged K/V for decode, ~7 TFLOP/s for prefill tiles.  Splits are
-  // sized for every CTA of the launch (all of them may end up helping with decode), so the
-  // decode tail stays short.
-  int decode_ctas = 0;
-  int target = a.target_units;
-  if (a.fused_ctas > 0) {
-    const float dec_bytes = static_cast<float>(page_heads) * (2.f * kPage * head_dim * 2.f);
-    const float t_dec = dec_bytes / 80e3f;   // microseconds on one SM
-    const float t_pre = s_flops / 7e6f;
-    if (t_dec > 0.f) {
-      const float share = t_pre > 0.f ? t_dec / (t_dec + t_pre) : 1.f;
-      decode_ctas = max(1, min(a.fused_ctas, static_cast<int>(share * a.fused_ctas + 0.5f)));
-    }
-    target = min(kMaxTargetUnits, 4 * a.decode_warps_per_cta * a.fused_ctas);
-  }
+  // Fused launch: splits are sized for every CTA of the launch (all of them may end up helping
+  // with decode), so the decode tail stays short.
+  const int target = a.fused_ctas > 0
+                         ? min(kMaxTargetUnits, 4 * a.decode_warps_per_cta * a.fused_ctas)
+                         : a.target_units;
   const int sp = static_cast<int>(max(static_cast<long long>(kMinSplitPages),
                                       (page_heads + target - 1) / target));
   int my_d = 0, my_p = 0;
@@ -123,7 +119,99 @@ __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim) {
     if (is_decode_class(x.q, a.group)) ex_d += (x.pages + sp - 1) / sp * a.nkv;
     else ex_p += (x.q * a.group + a.tile_m - 1) / a.tile_m * a.nkv;
   }
+
+  // tcgen05 prefill units in one global longest-first order: a counting sort of the (request,
+  // pair) entries by key tiles, so the long units start first whatever request they belong to
+  __shared__ int s_bin[kTileBins];
+  __shared__ float s_pre_us;
+  __shared__ int s_pre_max;
+  const bool fused = a.fused_ctas > 0;
+  if (fused) {
+    for (int i = tid; i < kTileBins; i += nthreads) s_bin[i] = 0;
+    if (tid == 0) {
+      s_pre_us = 0.f;
+      s_pre_max = 0;
+    }
+    __syncthreads();
+    float my_us = 0.f;
+    int my_max = 0;
+    for (int r = lo; r < hi; ++r) {
+      const ReqInfo x = req_info(a, r);
+      if (!x.ok || x.q == 0 || is_decode_class(x.q, a.group)) continue;
+      const int pairs = (x.q * a.group + 255) / 256;
+      for (int p = 0; p < pairs; ++p) {
+        const int n = pair_key_tiles(x.L - x.q, x.q, a.group, p);
+        atomicAdd(&s_bin[min(n, kTileBins - 1)], 1);
+        my_us += kPreUnitUs + kPreTileUs * n;
+        my_max = max(my_max, n);
+      }
+    }
+    if (my_us > 0.f) atomicAdd(&s_pre_us, my_us);
+    if (my_max > 0) atomicMax(&s_pre_max, my_max);
+    __syncthreads();
+    // bins in descending tile order: start position of each bin in the list
+    const int per_bin = (kTileBins + nthreads - 1) / nthreads;
+    int cnt = 0;
+    for (int i = 0; i < per_bin; ++i) {
+      const int b = kTileBins - 1 - (tid * per_bin + i);
+      if (b >= 0) cnt += s_bin[b];
+    }
+    int start, total, dummy0, dummy1;
+    block_scan2(cnt, 0, &start, &dummy0, &total, &dummy1);
+    for (int i = 0; i < per_bin; ++i) {
+      const int b = kTileBins - 1 - (tid * per_bin + i);
+      if (b < 0) continue;
+      const int c = s_bin[b];
+      s_bin[b] = start;
+      start += c;
+    }
+    __syncthreads();
+    for (int r = lo; r < hi; ++r) {
+      const ReqInfo x = req_info(a, r);
+      if (!x.ok || x.q == 0 || is_decode_class(x.q, a.group)) continue;
+      const int pairs = (x.q * a.group + 255) / 256;
+      for (int p = 0; p < pairs; ++p) {
+        const int n = pair_key_tiles(x.L - x.q, x.q, a.group, p);
+        a.pre_list[atomicAdd(&s_bin[min(n, kTileBins - 1)], 1)] = r * 65536 + p;
+      }
+    }
+  }
+
+  // Decode-first CTAs: the count that minimises the later of the two finish times under the
+  // model above (CTAs that run out of their own kind then help with the other kind); every
+  // thread scores a few counts, the best (time, count) wins.
+  __shared__ unsigned long long s_best;
+  if (tid == 0) s_best = ~0ull;
+  __syncthreads();
+  if (fused) {
+    const int C = a.fused_ctas;
+    const float dec_bytes = static_cast<float>(page_heads) * (2.f * kPage * head_dim * 2.f);
+    const float t_unit = kDecUnitUs + kDecPageUs * sp;
+    const float pre_total = s_pre_us * a.nkv, pre_long = kPreUnitUs + kPreTileUs * s_pre_max;
+    auto t_dec = [&](int d) {
+      if (tot_d == 0) return 0.f;
+      const int waves = (tot_d + a.decode_warps_per_cta * d - 1) / (a.decode_warps_per_cta * d);
+      return fmaxf(waves * t_unit, dec_bytes / fminf(d * kDecBytesPerUsPerCta, kHbmBytesPerUs));
+    };
+    auto t_pre = [&](int p) { return tot_p == 0 ? 0.f : fmaxf(pre_long, pre_total / p); };
+    auto key = [](float t, int d) {
+      return (static_cast<unsigned long long>(__float_as_uint(t)) << 32) |
+             static_cast<unsigned>(d);
+    };
+    // d = C: everything decodes first, then prefills (also the only choice without prefill).
+    // A split must beat it by 10 %: split CTAs also contend for HBM and L2, which the model
+    // leaves out, and the decode-first pass measured faster whenever the two were close.
+    unsigned long long best =
+        tid == 0 ? key(0.9f * (t_dec(C) + t_pre(C)), tot_d > 0 ? C : 0) : ~0ull;
+    if (tot_d > 0 && tot_p > 0)
+      for (int d = 1 + tid; d < C; d += nthreads)
+        best = min(best, key(fmaxf(t_dec(d), t_pre(C - d)), d));
+    atomicMin(&s_best, best);
+  }
+  __syncthreads();
+
   if (tid == 0) {
+    const int decode_ctas = fused ? static_cast<int>(s_best & 0xffffffffu) : 0;
     a.dec_off[a.R] = tot_d;
     a.pre_off[a.R] = tot_p;
     a.header[kHNumDecodeUnits] = tot_d;

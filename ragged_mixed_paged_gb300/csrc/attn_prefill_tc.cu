@@ -146,13 +146,12 @@ __device__ __forceinline__ TcUnit decode_unit(const AttnArgs& a, int u) {
     un.valid = 1;
     return un;
   }
-  const int r = upper_bound_i32(a.pre_off, a.R + 1, u) - 1;
-  const int first = a.pre_off[r];
-  const int pairs_r = (a.pre_off[r + 1] - first) / a.nkv;
-  const int local = u - first;
+  // the planner lists the (request, pair) entries longest first; the kv heads of one entry
+  // are consecutive units
+  const int entry = __ldg(a.pre_list + u / a.nkv);
+  const int r = entry >> 16, pair = entry & 0xffff;
   un.r = r;
-  un.h = local % a.nkv;
-  const int pair = pairs_r - 1 - local / a.nkv;
+  un.h = u % a.nkv;
   un.t0 = a.qsl[r];
   un.q = a.qsl[r + 1] - un.t0;
   un.L = a.seq_lens[r];

@@ -51,8 +51,13 @@ __global__ void __launch_bounds__(prep::kThreads) step_prep_kernel(StepArgs s) {
     request_outputs(a, s_qsl, total, err);  // ends with a barrier: qsl / seq_lens are visible
     attn::plan_body(s.at, s.head_dim);
   }
+  // CTA 0 carries the planner on the launch's critical path: the other CTAs take the tokens
+  // and rows when there are any
   const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * kWarps + (threadIdx.x >> 5), nw = gridDim.x * kWarps;
+  const int skip = gridDim.x > 1 ? 1 : 0;
+  if (static_cast<int>(blockIdx.x) < skip) return;
+  const int gw = (blockIdx.x - skip) * kWarps + (threadIdx.x >> 5);
+  const int nw = (gridDim.x - skip) * kWarps;
   const int n_real = min(a.N, total);
   for (int t = gw; t < a.N_pad; t += nw) {
     int r = -1;
@@ -144,7 +149,7 @@ extern "C" rb_status rb_step(const rb_step_args* args, void* stream) {
     return RB_ERR_CUDA;
   const int sms = max(1, device_sm_count());
   const int want = (max(x.num_tokens_padded, x.num_reqs_padded) + kWarps - 1) / kWarps;
-  const int grid = max(1, min(want, 2 * sms));
+  const int grid = max(1, min(want, 2 * sms)) + (want > 0 ? 1 : 0);  // + the planner's CTA
   step_prep_kernel<<<grid, prep::kThreads, smem, s>>>(sa);
   if (last_launch_status() != RB_OK) return RB_ERR_CUDA;
   note_launches(1);
