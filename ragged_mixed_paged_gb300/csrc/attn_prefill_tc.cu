@@ -383,18 +383,16 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
   const int t = threadIdx.x & 127;
   const uint32_t lane_off = static_cast<uint32_t>((t >> 5) * 32) << 16;
   const uint32_t col_s = tmem + lane_off + C::col_s(x), col_o = tmem + lane_off + C::col_o(x);
-  uint32_t tc_x = 0, pv_seen = 0, itk = 0;
+  uint32_t tc_x = 0, itk = 0;
   auto wait_all = [&](uint64_t* bar, uint32_t phase) -> bool {
     const bool ok = tc_wait(bar, phase, abort, a.err);
     return !__any_sync(0xffffffffu, !ok);
   };
-  auto catch_up = [&](uint32_t target) -> bool {  // consume o_done phases up to `target`
-    while (pv_seen < target) {
-      if (!wait_all(&sh.o_done[x], pv_seen & 1)) return false;
-      ++pv_seen;
-    }
-    return true;
-  };
+  // P V of side tile T (and so every earlier one: the tensor pipe runs in order) has landed.
+  // o_done completes once per P V and nothing has to consume every phase: while this side waits
+  // for P V of tile T, the P V of tile T + 1 cannot complete (it needs P of tile T + 1), so the
+  // barrier is at most one phase past the awaited one and its parity is unambiguous.
+  auto wait_pv = [&](uint32_t T) -> bool { return wait_all(&sh.o_done[x], T & 1); };
   for (int k = 0;; ++k) {
     const int slot = k % C::kRing;
     if (!wait_all(&sh.unit_full[slot], (k / C::kRing) & 1)) break;
@@ -450,7 +448,7 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
         const float m_new = need ? m_tile : m_ref;
         const float alpha = fast_exp2(m_ref - m_new);
         if (j > 0) {
-          if (!catch_up(tj)) { ok = false; break; }  // O must hold P_{j-1} V_{j-1}
+          if (!wait_pv(tj - 1)) { ok = false; break; }  // O must hold P_{j-1} V_{j-1}
           tc::fence_after_sync();
           uint32_t r[32];
 #pragma unroll
@@ -499,18 +497,17 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
         tc::st16(col_s + c * 16, pk);
       }
       tc::wait_st();
-      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
-      // observe P_{j-1} V_{j-1} before P_j lets the next one start: o_done then never runs more
-      // than one phase ahead of pv_seen, so its parity waits stay unambiguous
-      if (!catch_up(tj)) { ok = false; break; }
+      // P_j overwrites the S columns P_{j-1} V_{j-1} read: that product is done, since S_j (the
+      // MMA after it) has landed
       tc::fence_before_sync();
       tc::mbar_arrive(&sh.p_full[x]);
+      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
     }
     if (!ok) break;
     itk += un.n_kt;
     if (n > 0) {
+      if (!wait_pv(tc_x + n - 1)) break;  // the unit's last P V (and so every one) is in O
       tc_x += n;
-      if (!catch_up(tc_x)) break;  // every P V of this unit has landed in O
       tc::fence_after_sync();
       const size_t orow = static_cast<size_t>(un.t0 + jt) * a.nh + un.h * a.group + hh;
       if (a.cascade == kPrefixPass) {
