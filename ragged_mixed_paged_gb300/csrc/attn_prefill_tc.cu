@@ -293,28 +293,31 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
   uint32_t ucount[2] = {0, 0};            // units per side that used O
   bool issued = false;
   auto wait = [&](uint64_t* bar, uint32_t phase) { return tc_wait(bar, phase, abort, a.err); };
+  // Shared-memory descriptors are built once: a k-step moves the start address by 32 bytes
+  // within a 128-byte swizzle atom, a 64-dim half by a half tile (the address field counts
+  // 16-byte units in the descriptor's low bits, which no step carries out of).
+  const uint64_t q_desc0 = tc::sdesc_sw128(smem_base + C::kQOffset, 16, 1024);
+  const uint64_t k_desc0 = tc::sdesc_sw128(smem_base, 16, 1024);
+  const uint64_t v_desc0 = tc::sdesc_sw128(smem_base + C::kVOffset, C::kHalfBytes, 1024);
+  auto step = [](int ks, uint32_t half_bytes) -> uint64_t {
+    return static_cast<uint64_t>(((ks >> 2) * half_bytes + (ks & 3) * 32) >> 4);
+  };
   auto issue_s = [&](int x, uint32_t kt) {  // S_x = Q_x K^T into S_x
-    const uint32_t kb = smem_base + (kt % C::kStagesK) * C::kTileBytes;
-    const uint32_t qs = smem_base + C::kQOffset + x * C::kQBytes;
+    const uint64_t kd = k_desc0 + (((kt % C::kStagesK) * C::kTileBytes) >> 4);
+    const uint64_t qd = q_desc0 + ((x * C::kQBytes) >> 4);
 #pragma unroll
-    for (int ks = 0; ks < HD / 16; ++ks) {
-      const uint64_t adesc =
-          tc::sdesc_sw128(qs + (ks >> 2) * C::kQHalfBytes + (ks & 3) * 32, 16, 1024);
-      const uint64_t bdesc =
-          tc::sdesc_sw128(kb + (ks >> 2) * C::kHalfBytes + (ks & 3) * 32, 16, 1024);
-      tc::mma_ss(tmem + C::col_s(x), adesc, bdesc, idesc_s, ks > 0 ? 1u : 0u);
-    }
+    for (int ks = 0; ks < HD / 16; ++ks)
+      tc::mma_ss(tmem + C::col_s(x), qd + step(ks, C::kQHalfBytes), kd + step(ks, C::kHalfBytes),
+                 idesc_s, ks > 0 ? 1u : 0u);
     tc::commit(&sh.s_full[x]);
     issued = true;
   };
   auto issue_pv = [&](int x, uint32_t kt, bool first) {  // O_x (+)= P_x V
-    const uint32_t vb = smem_base + C::kVOffset + (kt % C::kStagesV) * C::kTileBytes;
+    const uint64_t vd = v_desc0 + (((kt % C::kStagesV) * C::kTileBytes) >> 4);
 #pragma unroll
-    for (int kk = 0; kk < C::kN / 16; ++kk) {
-      const uint64_t bdesc = tc::sdesc_sw128(vb + kk * (16 * 128), C::kHalfBytes, 1024);
-      tc::mma_ts(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, bdesc, idesc_o,
-                 (first && kk == 0) ? 0u : 1u);
-    }
+    for (int kk = 0; kk < C::kN / 16; ++kk)
+      tc::mma_ts(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, vd + ((kk * 16 * 128) >> 4),
+                 idesc_o, (first && kk == 0) ? 0u : 1u);
     tc::commit(&sh.o_done[x]);
   };
   for (int k = 0;; ++k) {
