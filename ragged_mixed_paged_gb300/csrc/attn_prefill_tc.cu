@@ -312,13 +312,15 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
     tc::commit(&sh.s_full[x]);
     issued = true;
   };
-  auto issue_pv = [&](int x, uint32_t kt, bool first) {  // O_x (+)= P_x V
+  // O_x (+)= P_x V.  Only the side's last P V of a unit is committed on its own (o_done): an
+  // earlier one is covered by the commit of the S issued after it.
+  auto issue_pv = [&](int x, uint32_t kt, bool first, bool last) {
     const uint64_t vd = v_desc0 + (((kt % C::kStagesV) * C::kTileBytes) >> 4);
 #pragma unroll
     for (int kk = 0; kk < C::kN / 16; ++kk)
       tc::mma_ts(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, vd + ((kk * 16 * 128) >> 4),
                  idesc_o, (first && kk == 0) ? 0u : 1u);
-    tc::commit(&sh.o_done[x]);
+    if (last) tc::commit(&sh.o_done[x]);
   };
   for (int k = 0;; ++k) {
     const int slot = k % C::kRing;
@@ -335,28 +337,24 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
     bool ok = true;
     for (int j = 0; j < un.n_kt && ok; ++j) {
       const uint32_t kt = itk + j;
-      bool k_ready = false;
+      bool k_ready = false, v_ready = false;
       for (int x = 0; x < 2; ++x) {
         if (j >= un.n[x]) continue;
+        // every wait of this side's step first, then one fence before its MMAs
+        const bool next_s = j + 1 < un.n[x];
         if (!wait(&sh.p_full[x], (tcount[x] + j) & 1) ||
-            !wait(&sh.v_full[kt % C::kStagesV], (kt / C::kStagesV) & 1) ||
-            (j == 0 && ucount[x] > 0 && !wait(&sh.o_free[x], (ucount[x] - 1) & 1))) {
+            (!v_ready && !wait(&sh.v_full[kt % C::kStagesV], (kt / C::kStagesV) & 1)) ||
+            (j == 0 && ucount[x] > 0 && !wait(&sh.o_free[x], (ucount[x] - 1) & 1)) ||
+            (next_s && !k_ready &&
+             !wait(&sh.k_full[(kt + 1) % C::kStagesK], ((kt + 1) / C::kStagesK) & 1))) {
           ok = false;
           break;
         }
+        k_ready = k_ready || next_s;
+        v_ready = true;
         tc::fence_after_sync();
-        issue_pv(x, kt, j == 0);
-        if (j + 1 < un.n[x]) {
-          if (!k_ready) {
-            if (!wait(&sh.k_full[(kt + 1) % C::kStagesK], ((kt + 1) / C::kStagesK) & 1)) {
-              ok = false;
-              break;
-            }
-            tc::fence_after_sync();
-            k_ready = true;
-          }
-          issue_s(x, kt + 1);
-        }
+        issue_pv(x, kt, j == 0, !next_s);
+        if (next_s) issue_s(x, kt + 1);
       }
       if (!ok) break;
       tc::commit(&sh.v_empty[kt % C::kStagesV]);                        // P V of tile j issued
@@ -386,16 +384,13 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
   const int t = threadIdx.x & 127;
   const uint32_t lane_off = static_cast<uint32_t>((t >> 5) * 32) << 16;
   const uint32_t col_s = tmem + lane_off + C::col_s(x), col_o = tmem + lane_off + C::col_o(x);
-  uint32_t tc_x = 0, itk = 0;
+  uint32_t tc_x = 0, itk = 0, uc_x = 0;  // S tiles, K/V tiles and units (with n > 0) of this side
   auto wait_all = [&](uint64_t* bar, uint32_t phase) -> bool {
     const bool ok = tc_wait(bar, phase, abort, a.err);
     return !__any_sync(0xffffffffu, !ok);
   };
-  // P V of side tile T (and so every earlier one: the tensor pipe runs in order) has landed.
-  // o_done completes once per P V and nothing has to consume every phase: while this side waits
-  // for P V of tile T, the P V of tile T + 1 cannot complete (it needs P of tile T + 1), so the
-  // barrier is at most one phase past the awaited one and its parity is unambiguous.
-  auto wait_pv = [&](uint32_t T) -> bool { return wait_all(&sh.o_done[x], T & 1); };
+  // s_full of tile j tracks every MMA issued before S_j, P V of tile j - 1 among them; o_done
+  // completes once per unit of this side, after its last P V.
   for (int k = 0;; ++k) {
     const int slot = k % C::kRing;
     if (!wait_all(&sh.unit_full[slot], (k / C::kRing) & 1)) break;
@@ -450,9 +445,7 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
       if (__any_sync(0xffffffffu, need)) {
         const float m_new = need ? m_tile : m_ref;
         const float alpha = fast_exp2(m_ref - m_new);
-        if (j > 0) {
-          if (!wait_pv(tj - 1)) { ok = false; break; }  // O must hold P_{j-1} V_{j-1}
-          tc::fence_after_sync();
+        if (j > 0) {  // O holds P_{j-1} V_{j-1}: S_j, issued after it, has landed
           uint32_t r[32];
 #pragma unroll
           for (int c = 0; c < HD / 32; ++c) {
@@ -509,7 +502,8 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
     if (!ok) break;
     itk += un.n_kt;
     if (n > 0) {
-      if (!wait_pv(tc_x + n - 1)) break;  // the unit's last P V (and so every one) is in O
+      if (!wait_all(&sh.o_done[x], uc_x & 1)) break;  // the unit's last P V is in O
+      ++uc_x;
       tc_x += n;
       tc::fence_after_sync();
       const size_t orow = static_cast<size_t>(un.t0 + jt) * a.nh + un.h * a.group + hh;
