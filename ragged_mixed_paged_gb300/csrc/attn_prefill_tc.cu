@@ -7,17 +7,19 @@
 // Prefill unit = (request, kv head, pair of 128-row query tiles A and B); rows are (query token,
 // head of the group) pairs, token-major, so every K/V tile serves the whole query-head group
 // and both tiles of the pair.  One CTA per SM (persistent; units pulled from an atomic
-// counter, the most expensive pair of each request first), 12 warps with fixed roles:
-//   warp 8     TMA producer: fetches units into a 4-entry ring, loads Q_A and Q_B once per unit
+// counter, the most expensive pair of each request first), 12 warps with fixed roles (the
+// single-thread MMA issuer is warp 0, the oldest warp of its SM sub-partition, which shares that
+// scheduler with one softmax warp of each tile):
+//   warp 1     TMA producer: fetches units into a 4-entry ring, loads Q_A and Q_B once per unit
 //              (3-D boxes {64 dims, group heads, 128/group tokens}) and each 128-key K and V
 //              tile (8 pages x 128-byte boxes, 128B swizzle, one page per lane) into a 3-stage
 //              K ring and a 2-stage V ring, V one tile behind K (K is freed once S is done);
-//   warp 9     allocates all 512 TMEM columns (S_A, S_B, O_A, O_B); one thread issues the MMAs
+//   warp 0     allocates all 512 TMEM columns (S_A, S_B, O_A, O_B); one thread issues the MMAs
 //              in the order S_A(0) S_B(0) | PV_A(0) S_A(1) | PV_B(0) S_B(1) | PV_A(1) ...
 //              S = Q K^T: M=128, N=128, K=hd, both operands K-major in shared memory;
 //              O += P V:  M=128, N=hd,  K=128, P read from TMEM, V MN-major in shared memory;
 //              so one tile's softmax runs while the tensor core works on the other tile;
-//   warps 0-3  softmax of tile A, warps 4-7 softmax of tile B; thread t = query row t: reads its
+//   warps 4-7  softmax of tile A, warps 8-11 softmax of tile B; thread t = query row t: reads its
 //              S row from TMEM, masks causally, keeps a running max and sum in the log2
 //              domain, writes P (bf16) back over the S columns, and rescales its O row in TMEM
 //              only when the max grows by more than 2^8 (exact either way: P and the sum share
@@ -60,8 +62,8 @@ struct TcCfg {
   static constexpr int kControlRegs = 72;
   static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
-  static constexpr int kProducerWarp = 8;
-  static constexpr int kMmaWarp = 9;  // warps 10 and 11 only complete the third warpgroup
+  static constexpr int kMmaWarp = 0;
+  static constexpr int kProducerWarp = 1;  // warps 2 and 3 only complete the first warpgroup
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0;                   // S_A at 0, S_B at 128
   static constexpr uint32_t kColO0 = 256;                 // O_A at 256, O_B at 256 + HD
@@ -100,16 +102,19 @@ struct TcShared {
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
 
-// Bounded wait that also gives up as soon as another role has aborted.
+// Bounded wait that also gives up as soon as another role has aborted.  `Relaxed`: for the
+// MMA issuer (see mma_issuer).
+template <bool Relaxed = false>
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t phase, volatile int* abort,
                                         int32_t* err) {
+  auto test = [&]() { return Relaxed ? mbar_try_wait_relaxed(bar, phase) : mbar_try_wait(bar, phase); };
 #pragma unroll 1
   for (int i = 0; i < 128; ++i)
-    if (mbar_try_wait(bar, phase)) return true;
+    if (test()) return true;
   const uint64_t t0 = global_timer_ns();
 #pragma unroll 1
   while (true) {
-    if (mbar_try_wait(bar, phase)) return true;
+    if (test()) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > kWaitLimitNs) {
       if (atomicExch(const_cast<int*>(abort), 1) == 0) raise_error(err, RB_EBIT_TIMEOUT);
@@ -292,7 +297,18 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
   uint32_t tcount[2] = {0, 0};            // S (= P V) tiles per side
   uint32_t ucount[2] = {0, 0};            // units per side that used O
   bool issued = false;
-  auto wait = [&](uint64_t* bar, uint32_t phase) { return tc_wait(bar, phase, abort, a.err); };
+  // Every barrier of the loop below guards data that only tcgen05.mma reads (P and O in tensor
+  // memory, Q, K and V that TMA wrote to shared memory), and each wait is followed by
+  // tcgen05.fence::after_thread_sync before the MMAs that read it, so the waits are relaxed: an
+  // acquiring try_wait behind queued MMAs left the tensor pipe idle ~140 cycles per wait on this
+  // GPU, a relaxed one costs nothing.  The unit descriptor is plain shared memory written by the
+  // producer warp: its barrier keeps the acquiring wait.
+  auto wait = [&](uint64_t* bar, uint32_t phase) { return tc_wait<true>(bar, phase, abort, a.err); };
+  // A wait whose result decides a branch costs the issuing thread a few hundred cycles even when
+  // the phase is long complete; so every barrier of one step is first tested at once (the tests
+  // issue back to back, one branch on their conjunction) and only a step that finds one not yet
+  // complete takes the bounded waits one by one.
+  auto test = [](uint64_t* bar, uint32_t phase) { return mbar_test_relaxed(bar, phase); };
   // Shared-memory descriptors are built once: a k-step moves the start address by 32 bytes
   // within a 128-byte swizzle atom, a 64-dim half by a half tile (the address field counts
   // 16-byte units in the descriptor's low bits, which no step carries out of).
@@ -324,11 +340,13 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
   };
   for (int k = 0;; ++k) {
     const int slot = k % C::kRing;
-    if (!wait(&sh.unit_full[slot], (k / C::kRing) & 1)) break;
+    if (!tc_wait(&sh.unit_full[slot], (k / C::kRing) & 1, abort, a.err)) break;
     const TcUnit un = sh.units[slot];
     if (!un.valid) break;
-    if (!wait(&sh.q_full, k & 1)) break;
-    if (!wait(&sh.k_full[itk % C::kStagesK], (itk / C::kStagesK) & 1)) break;
+    const bool q_k = test(&sh.q_full, k & 1) & test(&sh.k_full[itk % C::kStagesK], (itk / C::kStagesK) & 1);
+    if (!q_k && (!wait(&sh.q_full, k & 1) ||
+                 !wait(&sh.k_full[itk % C::kStagesK], (itk / C::kStagesK) & 1)))
+      break;
     tc::fence_after_sync();
     issue_s(0, itk);
     if (un.n[1] > 0) issue_s(1, itk);
@@ -338,15 +356,20 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
     for (int j = 0; j < un.n_kt && ok; ++j) {
       const uint32_t kt = itk + j;
       bool k_ready = false, v_ready = false;
-      for (int x = 0; x < 2; ++x) {
+#pragma unroll
+      for (int x = 0; x < 2; ++x) {  // unrolled: the per-side counters stay in registers
         if (j >= un.n[x]) continue;
         // every wait of this side's step first, then one fence before its MMAs
         const bool next_s = j + 1 < un.n[x];
-        if (!wait(&sh.p_full[x], (tcount[x] + j) & 1) ||
-            (!v_ready && !wait(&sh.v_full[kt % C::kStagesV], (kt / C::kStagesV) & 1)) ||
-            (j == 0 && ucount[x] > 0 && !wait(&sh.o_free[x], (ucount[x] - 1) & 1)) ||
-            (next_s && !k_ready &&
-             !wait(&sh.k_full[(kt + 1) % C::kStagesK], ((kt + 1) / C::kStagesK) & 1))) {
+        const bool need_v = !v_ready, need_o = j == 0 && ucount[x] > 0, need_k = next_s && !k_ready;
+        const uint32_t ph_p = (tcount[x] + j) & 1, ph_v = (kt / C::kStagesV) & 1,
+                       ph_o = (ucount[x] - 1) & 1, ph_k = ((kt + 1) / C::kStagesK) & 1;
+        uint64_t* bar_v = &sh.v_full[kt % C::kStagesV];
+        uint64_t* bar_k = &sh.k_full[(kt + 1) % C::kStagesK];
+        const bool ready = test(&sh.p_full[x], ph_p) & (!need_v || test(bar_v, ph_v)) &
+                           (!need_o || test(&sh.o_free[x], ph_o)) & (!need_k || test(bar_k, ph_k));
+        if (!ready && (!wait(&sh.p_full[x], ph_p) || (need_v && !wait(bar_v, ph_v)) ||
+                       (need_o && !wait(&sh.o_free[x], ph_o)) || (need_k && !wait(bar_k, ph_k)))) {
           ok = false;
           break;
         }
@@ -363,6 +386,7 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
     }
     if (!ok) break;
     tc::mbar_arrive(&sh.unit_empty[slot]);
+#pragma unroll
     for (int x = 0; x < 2; ++x) {
       tcount[x] += un.n[x];
       if (un.n[x] > 0) ++ucount[x];
@@ -388,6 +412,13 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
   auto wait_all = [&](uint64_t* bar, uint32_t phase) -> bool {
     const bool ok = tc_wait(bar, phase, abort, a.err);
     return !__any_sync(0xffffffffu, !ok);
+  };
+  // One lane of each warp arrives for the warp: 128 arrivals on one barrier load the barrier
+  // unit that the MMA issuer's waits go through.
+  const bool lane0 = (t & 31) == 0;
+  auto arrive_warp = [&](uint64_t* bar) {
+    __syncwarp();
+    if (lane0) tc::mbar_arrive(bar);
   };
   // s_full of tile j tracks every MMA issued before S_j, P V of tile j - 1 among them; o_done
   // completes once per unit of this side, after its last P V.
@@ -496,7 +527,7 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
       // P_j overwrites the S columns P_{j-1} V_{j-1} read: that product is done, since S_j (the
       // MMA after it) has landed
       tc::fence_before_sync();
-      tc::mbar_arrive(&sh.p_full[x]);
+      arrive_warp(&sh.p_full[x]);
       l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
     }
     if (!ok) break;
@@ -569,9 +600,9 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
         }
       }
       tc::fence_before_sync();
-      tc::mbar_arrive(&sh.o_free[x]);
+      arrive_warp(&sh.o_free[x]);
     }
-    tc::mbar_arrive(&sh.unit_empty[slot]);
+    arrive_warp(&sh.unit_empty[slot]);
   }
 }
 
@@ -590,7 +621,7 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < C::kRing; ++i) {
       mbar_init(&sh.unit_full[i], 1);
-      mbar_init(&sh.unit_empty[i], 1 + 256);
+      mbar_init(&sh.unit_empty[i], 1 + 8);  // the issuer and one lane of each softmax warp
     }
     mbar_init(&sh.q_full, 1);
     mbar_init(&sh.q_empty, 1);
@@ -602,9 +633,9 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
       mbar_init(&sh.v_full[i], 1);
       mbar_init(&sh.v_empty[i], 1);
       mbar_init(&sh.s_full[i], 1);
-      mbar_init(&sh.p_full[i], 128);
+      mbar_init(&sh.p_full[i], 4);  // one lane of each softmax warp
       mbar_init(&sh.o_done[i], 1);
-      mbar_init(&sh.o_free[i], 128);
+      mbar_init(&sh.o_free[i], 4);
     }
     mbar_init(&sh.drain, 1);
     for (int w = 0; w < 8; ++w)
@@ -623,7 +654,7 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
   const uint32_t tmem = sh.tmem_base;
 
   // Two phases: the kind of work the planner assigned this CTA first, then the other kind
-  // until its queue is empty too.  The decode phase runs on warps 0-7, each with its own ring of
+  // until its queue is empty too.  The decode phase runs on warps 4-11, each with its own ring of
   // decode stages in the same shared memory the prefill phase uses.  Each register class keeps
   // its own loop so the code after setmaxnreg stays within that class's budget.
   const bool decode_first = sh.decode_first != 0;
@@ -633,7 +664,7 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
     __syncthreads();
     tc::fence_after_sync();
   };
-  if (warp >= 8) {
+  if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(C::kControlRegs));
     for (int phase = 0; phase < 2; ++phase) {
       if ((phase == 0) != decode_first) {
@@ -650,11 +681,11 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
     for (int phase = 0; phase < 2; ++phase) {
       if ((phase == 0) == decode_first) {
         using D = DecCfg<HD>;
-        decode_warp<HD>(&kmap, &vmap, a, sh.dec_bars[warp],
-                        base + warp * D::kStages * D::kStageBytes,
-                        base_ptr + warp * D::kStages * D::kStageBytes);
+        const int w = warp - 4;
+        decode_warp<HD>(&kmap, &vmap, a, sh.dec_bars[w], base + w * D::kStages * D::kStageBytes,
+                        base_ptr + w * D::kStages * D::kStageBytes);
       } else {
-        softmax_wg<HD>(a, sh, tmem, base_ptr, warp >> 2);
+        softmax_wg<HD>(a, sh, tmem, base_ptr, (warp >> 2) - 1);
       }
       phase_end();
     }

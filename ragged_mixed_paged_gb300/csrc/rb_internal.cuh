@@ -98,6 +98,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking test of a phase, relaxed (see mbar_try_wait_relaxed).  Several of these issued
+// back to back, their results combined before one branch, overlap their latencies.
+__device__ __forceinline__ bool mbar_test_relaxed(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.relaxed.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
+// The same test with relaxed semantics: no acquire ordering of this thread's later memory
+// accesses.  For a thread whose only consumers of the awaited data are asynchronous tcgen05
+// operations ordered after the wait by tcgen05.fence::after_thread_sync.
+__device__ __forceinline__ bool mbar_try_wait_relaxed(uint64_t* bar, uint32_t phase) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.relaxed.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(phase)
+      : "memory");
+  return ok != 0;
+}
 
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
