@@ -537,70 +537,78 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
       ++uc_x;
       tc_x += n;
       tc::fence_after_sync();
+      // the whole O row into registers at once; O is then free for the next unit's P V while
+      // this row is scaled and stored
+      uint32_t o[HD];
+#pragma unroll
+      for (int c = 0; c < HD / 32; ++c)
+        tc::ld32(col_o + c * 32, *reinterpret_cast<uint32_t(*)[32]>(o + c * 32));
+      tc::wait_ld();
+      tc::fence_before_sync();
+      arrive_warp(&sh.o_free[x]);
       const size_t orow = static_cast<size_t>(un.t0 + jt) * a.nh + un.h * a.group + hh;
+      // rows are written with 32-byte stores when the output is 32-byte aligned (a warp's
+      // rows are scattered: fewer, whole-sector stores), else 16-byte ones
       if (a.cascade == kPrefixPass) {
         // shared-prefix row: normalised fp32 output and its log-sum-exp, merged later
         const float inv = l > 0.f ? 1.f / l : 0.f;
         const size_t prow = static_cast<size_t>(un.r) * a.N * a.nh + orow;
-        float4* dst = reinterpret_cast<float4*>(a.pre_o + prow * HD);
+        float* dst = a.pre_o + prow * HD;
+        if (valid) {
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t r[32];
-          tc::ld32(col_o + c * 32, r);
-          tc::wait_ld();
-          if (valid) {
+          for (int i = 0; i < HD; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * inv);
+          if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
 #pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[c * 8 + v] = make_float4(
-                  __uint_as_float(r[4 * v + 0]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                  __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+            for (int v = 0; v < HD / 8; ++v)
+              st_global_v8(dst + 8 * v, o[8 * v], o[8 * v + 1], o[8 * v + 2], o[8 * v + 3],
+                           o[8 * v + 4], o[8 * v + 5], o[8 * v + 6], o[8 * v + 7]);
+          } else {
+#pragma unroll
+            for (int v = 0; v < HD / 4; ++v)
+              reinterpret_cast<uint4*>(dst)[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+          }
+          a.pre_lse[prow] = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
+        }
+      } else if (valid) {
+        // out = O * wa + sum over prefix key ranges of (shared-prefix row) * wp (cascade only)
+        float wa = 1.f / l;
+        float wp[kMaxPrefixSplits];
+        const bool cas = a.cascade == kSuffixPass;
+        if (cas) wa = cascade_weights(a, orow, m_ref, l, wp);
+        else if (!(l > 0.f)) wa = 0.f;
+#pragma unroll
+        for (int i = 0; i < HD; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * wa);
+        if (cas) {
+#pragma unroll
+          for (int ps = 0; ps < kMaxPrefixSplits; ++ps) {
+            if (ps >= a.prefix_splits) break;
+            const float4* o1 = reinterpret_cast<const float4*>(cascade_row<HD>(a, ps, orow));
+#pragma unroll
+            for (int v = 0; v < HD / 4; ++v) {
+              const float4 e = __ldg(o1 + v);
+              o[4 * v + 0] = __float_as_uint(__uint_as_float(o[4 * v + 0]) + e.x * wp[ps]);
+              o[4 * v + 1] = __float_as_uint(__uint_as_float(o[4 * v + 1]) + e.y * wp[ps]);
+              o[4 * v + 2] = __float_as_uint(__uint_as_float(o[4 * v + 2]) + e.z * wp[ps]);
+              o[4 * v + 3] = __float_as_uint(__uint_as_float(o[4 * v + 3]) + e.w * wp[ps]);
+            }
           }
         }
-        if (valid) a.pre_lse[prow] = l > 0.f ? m_ref + __log2f(l) : -INFINITY;
-      } else {
-        // out = O * wa + sum over prefix key ranges of (shared-prefix row) * wp (cascade only)
-        float wa = l > 0.f ? 1.f / l : 0.f;
-        float wp[kMaxPrefixSplits];
-        const bool cas = a.cascade == kSuffixPass && valid;
-        if (cas) wa = cascade_weights(a, orow, m_ref, l, wp);
-        uint4* dst = reinterpret_cast<uint4*>(a.out + orow * HD);
+        uint32_t pk[HD / 2];
 #pragma unroll
-        for (int c = 0; c < HD / 32; ++c) {
-          uint32_t r[32];
-          tc::ld32(col_o + c * 32, r);
-          tc::wait_ld();
-          if (valid) {
+        for (int i = 0; i < HD / 2; ++i)
+          pk[i] = pack_bf16x2(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+        __nv_bfloat16* dst = a.out + orow * HD;
+        if ((reinterpret_cast<uintptr_t>(dst) & 31) == 0) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * wa);
-            if (cas) {
+          for (int v = 0; v < HD / 16; ++v)
+            st_global_v8(dst + 16 * v, pk[8 * v], pk[8 * v + 1], pk[8 * v + 2], pk[8 * v + 3],
+                         pk[8 * v + 4], pk[8 * v + 5], pk[8 * v + 6], pk[8 * v + 7]);
+        } else {
 #pragma unroll
-              for (int ps = 0; ps < kMaxPrefixSplits; ++ps) {
-                if (ps >= a.prefix_splits) break;
-                const float4* o1 = reinterpret_cast<const float4*>(cascade_row<HD>(a, ps, orow));
-#pragma unroll
-                for (int v = 0; v < 8; ++v) {
-                  const float4 e = __ldg(o1 + c * 8 + v);
-                  r[4 * v + 0] = __float_as_uint(__uint_as_float(r[4 * v + 0]) + e.x * wp[ps]);
-                  r[4 * v + 1] = __float_as_uint(__uint_as_float(r[4 * v + 1]) + e.y * wp[ps]);
-                  r[4 * v + 2] = __float_as_uint(__uint_as_float(r[4 * v + 2]) + e.z * wp[ps]);
-                  r[4 * v + 3] = __float_as_uint(__uint_as_float(r[4 * v + 3]) + e.w * wp[ps]);
-                }
-              }
-            }
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 q4;
-              q4.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-              q4.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-              q4.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-              q4.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-              dst[c * 4 + v] = q4;
-            }
-          }
+          for (int v = 0; v < HD / 8; ++v)
+            reinterpret_cast<uint4*>(dst)[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
         }
       }
-      tc::fence_before_sync();
-      arrive_warp(&sh.o_free[x]);
     }
     arrive_warp(&sh.unit_empty[slot]);
   }

@@ -98,6 +98,15 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t phase) {
       : "memory");
   return ok != 0;
 }
+// 32-byte global store (sm_100 family); `p` must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* p, uint32_t r0, uint32_t r1, uint32_t r2,
+                                             uint32_t r3, uint32_t r4, uint32_t r5, uint32_t r6,
+                                             uint32_t r7) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(r0),
+               "r"(r1), "r"(r2), "r"(r3), "r"(r4), "r"(r5), "r"(r6), "r"(r7)
+               : "memory");
+}
+
 // Non-blocking test of a phase, relaxed (see mbar_try_wait_relaxed).  Several of these issued
 // back to back, their results combined before one branch, overlap their latencies.
 __device__ __forceinline__ bool mbar_test_relaxed(uint64_t* bar, uint32_t phase) {
