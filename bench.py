@@ -38,8 +38,8 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_write.sum), keyed by (kernel, workload, hash of the kernel's sources): a figure is
 # reported only while the kernel's sources are the ones it was measured on (profiles/).
 KNOWN_TRAFFIC = {
-    ("fused", 2, "37732985234d3580"): 79217408 + 4070400,
-    ("fused", 4, "37732985234d3580"): 10891009536 + 92549120,
+    ("fused", 2, "13eeef8630ada2ad"): 78978304 + 3656448,
+    ("fused", 4, "13eeef8630ada2ad"): 10039013632 + 99673088,
 }
 
 
