@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(DecCfg<HD>::kWarps * 32)
     fence_barrier_init();
   }
   __syncwarp();
-  decode_warp<HD>(&kmap, &vmap, a, bars[warp], wbase, wbase_ptr);
+  decode_warp<HD>(&kmap, &vmap, a, bars[warp], wbase, wbase_ptr, -1);
 }
 
 template <int HD>

@@ -97,22 +97,28 @@ __device__ void combine_splits(const AttnArgs& a, int h, int first, int nsplit, 
 // One decode warp: pulls (request, kv head, split) units from the shared counter until none
 // are left.  `bars` are this warp's kStages mbarriers (initialised, count 1) and `wbase` /
 // `wbase_ptr` the shared-memory address / pointer of its kStages stages (1024-byte aligned).
+// `first_unit` >= 0: the warp's first unit, handed out statically (the counter then starts
+// past every statically handed unit), which saves the first atomic's round trip.
 template <int HD>
 __device__ void decode_warp(const CUtensorMap* kmap_p, const CUtensorMap* vmap_p,
                             const AttnArgs& a, uint64_t* bars, uint32_t wbase,
-                            uint8_t* wbase_ptr) {
+                            uint8_t* wbase_ptr, int first_unit) {
   using C = DecCfg<HD>;
   const int lane = threadIdx.x & 31;
   const int n_units = a.header[kHNumDecodeUnits];
   const int sp = a.header[kHSplitPages];
   uint32_t it = 0;  // pages this warp has consumed (selects stage and phase)
 
+  int next_static = first_unit;
   while (true) {
-    int u = 0;
-    if (lane == 0) u = atomicAdd(a.header + kHDecodeNext, 1);
-    u = __shfl_sync(0xffffffffu, u, 0);
+    int u = next_static;
+    if (u < 0) {
+      if (lane == 0) u = atomicAdd(a.header + kHDecodeNext, 1);
+      u = __shfl_sync(0xffffffffu, u, 0);
+    }
+    next_static = -1;
     if (u >= n_units) break;
-    const int r = upper_bound_i32(a.dec_off, a.R + 1, u) - 1;
+    const int r = warp_upper_bound_i32(a.dec_off, a.R + 1, u) - 1;
     const int first = a.dec_off[r];
     const int nsplit = (a.dec_off[r + 1] - first) / a.nkv;
     const int local = u - first;

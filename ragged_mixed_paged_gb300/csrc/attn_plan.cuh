@@ -216,7 +216,8 @@ __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim) {
     a.pre_off[a.R] = tot_p;
     a.header[kHNumDecodeUnits] = tot_d;
     a.header[kHNumPrefillUnits] = tot_p;
-    a.header[kHDecodeNext] = 0;
+    // decode-first CTAs of a fused launch take their warps' first units statically
+    a.header[kHDecodeNext] = decode_ctas * a.decode_warps_per_cta;
     a.header[kHPrefillNext] = 0;
     a.header[kHSplitPages] = sp;
     a.header[kHDecodeCtas] = decode_ctas;

@@ -98,6 +98,7 @@ struct TcShared {
   uint32_t tmem_base;
   int abort;
   int decode_first;
+  int role_rank;  // order in which this CTA took its role: decode-first CTAs are ranks 0..D-1
 };
 
 constexpr uint64_t kWaitLimitNs = 1000000000ull;
@@ -649,7 +650,8 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
     for (int w = 0; w < 8; ++w)
       for (int st = 0; st < DecCfg<128>::kStages; ++st) mbar_init(&sh.dec_bars[w][st], 1);
     sh.abort = 0;
-    sh.decode_first = atomicAdd(a.header + kHRoleNext, 1) < a.header[kHDecodeCtas];
+    sh.role_rank = atomicAdd(a.header + kHRoleNext, 1);
+    sh.decode_first = sh.role_rank < a.header[kHDecodeCtas];
     fence_barrier_init();
   }
   if (warp == C::kMmaWarp) {
@@ -690,8 +692,10 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
       if ((phase == 0) == decode_first) {
         using D = DecCfg<HD>;
         const int w = warp - 4;
+        // a decode-first CTA's warps start on units rank x 8 + w without the counter
         decode_warp<HD>(&kmap, &vmap, a, sh.dec_bars[w], base + w * D::kStages * D::kStageBytes,
-                        base_ptr + w * D::kStages * D::kStageBytes);
+                        base_ptr + w * D::kStages * D::kStageBytes,
+                        decode_first ? sh.role_rank * a.decode_warps_per_cta + w : -1);
       } else {
         softmax_wg<HD>(a, sh, tmem, base_ptr, (warp >> 2) - 1);
       }

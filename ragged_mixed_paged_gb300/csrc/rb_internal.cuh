@@ -216,6 +216,27 @@ __device__ __forceinline__ int upper_bound_i32(const int32_t* a, int n, int32_t 
   return lo;
 }
 
+// The same, by a whole converged warp: each round the 32 lanes test 32 evenly spaced entries
+// at once, so a search takes ceil(log32 n) dependent loads instead of log2 n.
+__device__ __forceinline__ int warp_upper_bound_i32(const int32_t* a, int n, int32_t x) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = n;  // the answer lies in [lo, hi]
+  while (lo < hi) {
+    const int stride = (hi - lo + 31) / 32;
+    const int idx = lo + lane * stride;
+    const bool above = idx < hi && a[idx] > x;
+    const unsigned valid = __ballot_sync(0xffffffffu, idx < hi);
+    const unsigned hit = __ballot_sync(0xffffffffu, above);
+    if (hit & 1u) return lo;  // a[lo] > x
+    const int f = hit ? __ffs(hit) - 1 : 32 - __clz(valid);  // first lane above (or past the last valid)
+    const int prev = lo + (f - 1) * stride;                  // a[prev] <= x
+    if (hit) hi = lo + f * stride;
+    lo = prev + 1;
+    if (stride == 1) return hit ? hi : lo;
+  }
+  return lo;
+}
+
 // Byte offset of (row, 16-byte chunk) in a TMA box of 16 rows x 128 bytes with 128B swizzle.
 __device__ __forceinline__ uint32_t swz128(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
