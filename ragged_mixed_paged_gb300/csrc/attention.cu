@@ -25,7 +25,7 @@ namespace {
 constexpr int kPlanThreads = 1024;
 
 __global__ void __launch_bounds__(kPlanThreads) attn_plan_kernel(AttnArgs a, int head_dim) {
-  plan_body(a, head_dim);
+  plan_body(a, head_dim, ReqSrc{a.qsl, a.seq_lens, nullptr});
 }
 
 // Cascade: checks the shared prefix, writes the suffix pass's sequence lengths (seq_len - P)

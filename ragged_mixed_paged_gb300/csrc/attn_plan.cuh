@@ -44,11 +44,22 @@ struct ReqInfo {
   int q, L, pages;
 };
 
-__device__ __forceinline__ ReqInfo req_info(const AttnArgs& a, int r) {
+// Where the planner reads request metadata: query_start_loc (global, or a shared-memory copy)
+// and either the sequence lengths or, with `computed`, num_computed (seq_len = num_computed + q,
+// as the preparation step writes it).
+struct ReqSrc {
+  const int32_t* qsl;
+  const int32_t* seq_lens;
+  const int32_t* computed;
+};
+
+__device__ __forceinline__ ReqInfo req_info(const AttnArgs& a, const ReqSrc& src, int r) {
   ReqInfo x;
-  const int s = a.qsl[r], e = a.qsl[r + 1];
+  const int s = src.qsl[r], e = src.qsl[r + 1];
   x.q = e - s;
-  x.L = a.seq_lens[r];
+  x.L = src.computed != nullptr
+            ? static_cast<int32_t>(static_cast<long long>(src.computed[r]) + x.q)
+            : src.seq_lens[r];
   x.pages = (x.L + kPage - 1) / kPage;
   x.ok = s >= 0 && x.q >= 0 && e <= a.N && x.L >= x.q && x.pages <= a.kp_cap;
   return x;
@@ -75,24 +86,42 @@ constexpr int kTileBins = 512;  // histogram bins of prefill units by key tiles 
 // sizes the KV splits, writes per-request unit offsets, lists the tcgen05 prefill units
 // longest first, splits the CTAs of a fused launch between decode and prefill work, writes the
 // header, clears the split counters and writes the padding rows of the output as zeros.
-__device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim) {
+// `src`: defaults to the call's query_start_loc and seq_lens in global memory; the fused step
+// passes its shared-memory scan and num_computed, so the planner need not wait for (and read
+// back) the request outputs the same launch writes.
+__device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim, ReqSrc src) {
   __shared__ unsigned long long s_pages;
-  const int tid = threadIdx.x, nthreads = blockDim.x;
-  const int per = (a.R + nthreads - 1) / nthreads;
+  const int tid = threadIdx.x, nthreads = blockDim.x, lane = tid & 31;
+  const int per = (a.R + nthreads - 1) / nthreads;  // the same for every thread
   const int lo = min(tid * per, a.R), hi = min(lo + per, a.R);
+  // Each request's metadata is read once: a thread keeps its first kCache requests in a local
+  // array for the later passes (a pass over global metadata costs an L2 round trip).  The loops
+  // stay rolled: the planner runs once per step, from a cold instruction cache, and its time
+  // follows its code size more than its arithmetic.
+  constexpr int kCache = 4;
+  ReqInfo cache[kCache];
+#pragma unroll 1
+  for (int k = 0; k < kCache; ++k)
+    cache[k] = lo + k < hi ? req_info(a, src, lo + k) : ReqInfo{false, 0, 0, 0};
+  auto get = [&](int k) { return k < kCache ? cache[k] : req_info(a, src, lo + k); };
+  auto each = [&](auto&& fn) {  // fn(r, info) over this thread's requests, in order
+#pragma unroll 1
+    for (int k = 0; lo + k < hi; ++k) fn(lo + k, get(k));
+  };
   int bits = 0;
   if (tid == 0) {
     s_pages = 0;
-    if (a.qsl[0] != 0 || a.qsl[a.R] != a.N) bits |= RB_EBIT_ATTN_META;
+    if (src.qsl[0] != 0 || src.qsl[a.R] != a.N) bits |= RB_EBIT_ATTN_META;
   }
   __syncthreads();
   unsigned long long my_pages = 0;
-  for (int r = lo; r < hi; ++r) {
-    const ReqInfo x = req_info(a, r);
-    if (!x.ok) { bits |= RB_EBIT_ATTN_META; continue; }
-    if (is_decode_class(x.q, a.group)) my_pages += static_cast<unsigned long long>(x.pages);
-  }
-  if (my_pages) atomicAdd(&s_pages, my_pages);
+  each([&](int, const ReqInfo& x) {
+    if (!x.ok) bits |= RB_EBIT_ATTN_META;
+    else if (is_decode_class(x.q, a.group)) my_pages += static_cast<unsigned long long>(x.pages);
+  });
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) my_pages += __shfl_xor_sync(0xffffffffu, my_pages, o);
+  if (lane == 0 && my_pages) atomicAdd(&s_pages, my_pages);
   __syncthreads();
   const long long page_heads = static_cast<long long>(s_pages) * a.nkv;
   // Fused launch: splits are sized for every CTA of the launch (all of them may end up helping
@@ -102,30 +131,49 @@ __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim) {
                          : a.target_units;
   const int sp = static_cast<int>(max(static_cast<long long>(kMinSplitPages),
                                       (page_heads + target - 1) / target));
+  auto units_of = [&](const ReqInfo& x, int* d, int* p) {
+    if (!x.ok || x.q == 0) return;
+    if (is_decode_class(x.q, a.group)) *d += (x.pages + sp - 1) / sp * a.nkv;
+    else *p += (x.q * a.group + a.tile_m - 1) / a.tile_m * a.nkv;
+  };
   int my_d = 0, my_p = 0;
-  for (int r = lo; r < hi; ++r) {
-    const ReqInfo x = req_info(a, r);
-    if (!x.ok || x.q == 0) continue;
-    if (is_decode_class(x.q, a.group)) my_d += (x.pages + sp - 1) / sp * a.nkv;
-    else my_p += (x.q * a.group + a.tile_m - 1) / a.tile_m * a.nkv;
-  }
+  each([&](int, const ReqInfo& x) { units_of(x, &my_d, &my_p); });
   int ex_d, ex_p, tot_d, tot_p;
   block_scan2(my_d, my_p, &ex_d, &ex_p, &tot_d, &tot_p);
-  for (int r = lo; r < hi; ++r) {
-    const ReqInfo x = req_info(a, r);
+  each([&](int r, const ReqInfo& x) {
     a.dec_off[r] = ex_d;
     a.pre_off[r] = ex_p;
-    if (!x.ok || x.q == 0) continue;
-    if (is_decode_class(x.q, a.group)) ex_d += (x.pages + sp - 1) / sp * a.nkv;
-    else ex_p += (x.q * a.group + a.tile_m - 1) / a.tile_m * a.nkv;
-  }
+    units_of(x, &ex_d, &ex_p);
+  });
 
   // tcgen05 prefill units in one global longest-first order: a counting sort of the (request,
-  // pair) entries by key tiles, so the long units start first whatever request they belong to
+  // pair) entries by key tiles, so the long units start first whatever request they belong to.
+  // The pairs of each prefill request are spread over the lanes of its thread's warp.
   __shared__ int s_bin[kTileBins];
   __shared__ float s_pre_us;
   __shared__ int s_pre_max;
   const bool fused = a.fused_ctas > 0;
+  auto warp_pairs = [&](auto&& body) {  // body(r, c, q, pair) for every pair, warp-cooperative
+    auto one = [&](int r, const ReqInfo& x, bool has) {
+      const bool pre = has && x.ok && x.q > 0 && !is_decode_class(x.q, a.group);
+      const int pairs = pre ? (x.q * a.group + 255) / 256 : 0;
+      unsigned m = __ballot_sync(0xffffffffu, pairs > 0);
+      while (m) {
+        const int src = __ffs(m) - 1;
+        m &= m - 1;
+        const int rr = __shfl_sync(0xffffffffu, r, src);
+        const int q = __shfl_sync(0xffffffffu, x.q, src);
+        const int c = __shfl_sync(0xffffffffu, x.L - x.q, src);
+        const int np = __shfl_sync(0xffffffffu, pairs, src);
+        for (int p = lane; p < np; p += 32) body(rr, c, q, p);
+      }
+    };
+#pragma unroll 1
+    for (int k = 0; k < per; ++k) {  // uniform: every thread has the same `per`
+      const int r = lo + k;
+      one(r, r < hi ? get(k) : ReqInfo{false, 0, 0, 0}, r < hi);
+    }
+  };
   if (fused) {
     for (int i = tid; i < kTileBins; i += nthreads) s_bin[i] = 0;
     if (tid == 0) {
@@ -135,19 +183,19 @@ __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim) {
     __syncthreads();
     float my_us = 0.f;
     int my_max = 0;
-    for (int r = lo; r < hi; ++r) {
-      const ReqInfo x = req_info(a, r);
-      if (!x.ok || x.q == 0 || is_decode_class(x.q, a.group)) continue;
-      const int pairs = (x.q * a.group + 255) / 256;
-      for (int p = 0; p < pairs; ++p) {
-        const int n = pair_key_tiles(x.L - x.q, x.q, a.group, p);
-        atomicAdd(&s_bin[min(n, kTileBins - 1)], 1);
-        my_us += kPreUnitUs + kPreTileUs * n;
-        my_max = max(my_max, n);
-      }
+    warp_pairs([&](int, int c, int q, int p) {
+      const int n = pair_key_tiles(c, q, a.group, p);
+      atomicAdd(&s_bin[min(n, kTileBins - 1)], 1);
+      my_us += kPreUnitUs + kPreTileUs * n;
+      my_max = max(my_max, n);
+    });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      my_us += __shfl_xor_sync(0xffffffffu, my_us, o);
+      my_max = max(my_max, __shfl_xor_sync(0xffffffffu, my_max, o));
     }
-    if (my_us > 0.f) atomicAdd(&s_pre_us, my_us);
-    if (my_max > 0) atomicMax(&s_pre_max, my_max);
+    if (lane == 0 && my_us > 0.f) atomicAdd(&s_pre_us, my_us);
+    if (lane == 0 && my_max > 0) atomicMax(&s_pre_max, my_max);
     __syncthreads();
     // bins in descending tile order: start position of each bin in the list
     const int per_bin = (kTileBins + nthreads - 1) / nthreads;
@@ -166,15 +214,10 @@ __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim) {
       start += c;
     }
     __syncthreads();
-    for (int r = lo; r < hi; ++r) {
-      const ReqInfo x = req_info(a, r);
-      if (!x.ok || x.q == 0 || is_decode_class(x.q, a.group)) continue;
-      const int pairs = (x.q * a.group + 255) / 256;
-      for (int p = 0; p < pairs; ++p) {
-        const int n = pair_key_tiles(x.L - x.q, x.q, a.group, p);
-        a.pre_list[atomicAdd(&s_bin[min(n, kTileBins - 1)], 1)] = r * 65536 + p;
-      }
-    }
+    warp_pairs([&](int r, int c, int q, int p) {
+      const int n = pair_key_tiles(c, q, a.group, p);
+      a.pre_list[atomicAdd(&s_bin[min(n, kTileBins - 1)], 1)] = r * 65536 + p;
+    });
   }
 
   // Decode-first CTAs: the count that minimises the later of the two finish times under the

@@ -627,6 +627,11 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* base_ptr = smem_raw + (base - raw);
+  if (tid == 32) {  // the three descriptors every role's first copies use
+    prefetch_tmap(&qmap);
+    prefetch_tmap(&kmap);
+    prefetch_tmap(&vmap);
+  }
   if (tid == 0) {
     for (int i = 0; i < C::kRing; ++i) {
       mbar_init(&sh.unit_full[i], 1);

@@ -155,6 +155,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t phase,
   }
 }
 
+// Fetch a tensor map (a __grid_constant__ kernel parameter) into the TMA unit's descriptor cache
+// ahead of its first use.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 // 3-D tiled TMA load into shared memory, completion counted on `bar` (bytes).
 __device__ __forceinline__ void tma_load_3d(uint32_t dst_smem, const CUtensorMap* map,
                                             uint64_t* bar, int c0, int c1, int c2) {

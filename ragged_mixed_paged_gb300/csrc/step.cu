@@ -6,7 +6,8 @@
 // preparation launch does everything that only needs the batch's metadata:
 //   - every CTA recomputes the prefix sum of num_scheduled in shared memory (as
 //     rb_prepare_inputs does), so each knows the owner of any token and any request's last row;
-//   - CTA 0 writes the per-request outputs and then runs the attention planner on them;
+//   - CTA 0 runs the attention planner (from its scan and num_computed) while the last CTA
+//     writes the per-request outputs;
 //   - one warp per token writes its input id, position and slot and copies the token's K and V
 //     rows into that slot (16-byte accesses, lanes over the row);
 //   - one warp per request copies the hidden row at its logits index.
@@ -47,9 +48,13 @@ __global__ void __launch_bounds__(prep::kThreads) step_prep_kernel(StepArgs s) {
   int32_t* err = a.scalars + 3;
   block_scan_scheduled(a, s_qsl);
   const int total = s_qsl[a.R];
+  // CTA 0 plans the attention from its own scan and num_computed (the values the request
+  // outputs hold); the last CTA writes the request outputs, then helps with the tokens
   if (blockIdx.x == 0) {
-    request_outputs(a, s_qsl, total, err);  // ends with a barrier: qsl / seq_lens are visible
-    attn::plan_body(s.at, s.head_dim);
+    if (gridDim.x == 1) request_outputs(a, s_qsl, total, err);
+    attn::plan_body(s.at, s.head_dim, attn::ReqSrc{s_qsl, nullptr, a.num_computed});
+  } else if (blockIdx.x == gridDim.x - 1) {
+    request_outputs(a, s_qsl, total, err);
   }
   // CTA 0 carries the planner on the launch's critical path: the other CTAs take the tokens
   // and rows when there are any
