@@ -41,6 +41,32 @@ struct StepArgs {
   int num_hidden_rows;
 };
 
+// One warp copies `chunks` 16-byte chunks of row pair (s0 -> d0, s1 -> d1); each batch's loads
+// are issued before its stores (the compiler must assume a store may alias a later load, so a
+// load-store loop would wait one memory round trip per chunk).  s1 / d1 may be null.
+template <int kBatch>
+__device__ __forceinline__ void warp_copy_rows(int4* d0, const int4* s0, int4* d1,
+                                               const int4* s1, int chunks, int lane) {
+  for (int c0 = 0; c0 < chunks; c0 += 32 * kBatch) {
+    int4 x0[kBatch], x1[kBatch];
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int c = c0 + u * 32 + lane;
+      const bool in = c < chunks;
+      x0[u] = in && s0 != nullptr ? __ldg(s0 + c) : make_int4(0, 0, 0, 0);
+      x1[u] = in && s1 != nullptr ? __ldg(s1 + c) : make_int4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int c = c0 + u * 32 + lane;
+      if (c < chunks) {
+        d0[c] = x0[u];
+        if (d1 != nullptr) d1[c] = x1[u];
+      }
+    }
+  }
+}
+
 __global__ void __launch_bounds__(prep::kThreads) step_prep_kernel(StepArgs s) {
   using namespace prep;
   extern __shared__ int32_t s_qsl[];  // [R + 1]
@@ -64,7 +90,18 @@ __global__ void __launch_bounds__(prep::kThreads) step_prep_kernel(StepArgs s) {
   const int gw = (blockIdx.x - skip) * kWarps + (threadIdx.x >> 5);
   const int nw = (gridDim.x - skip) * kWarps;
   const int n_real = min(a.N, total);
+  constexpr int kPre = 4;  // chunks per lane of each row fetched before the token's metadata
   for (int t = gw; t < a.N_pad; t += nw) {
+    // the token's K and V rows need no metadata: their loads are in flight while the owner,
+    // position and slot are looked up
+    const long long src = static_cast<long long>(t) * s.kv_chunks;
+    int4 xk[kPre], xv[kPre];
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int c = u * 32 + lane;
+      xk[u] = c < s.kv_chunks ? __ldg(s.k + src + c) : make_int4(0, 0, 0, 0);
+      xv[u] = c < s.kv_chunks ? __ldg(s.v + src + c) : make_int4(0, 0, 0, 0);
+    }
     int r = -1;
     const TokMeta m = token_meta(a, s_qsl, n_real, t, r);
     int bits = m.bits;
@@ -76,23 +113,26 @@ __global__ void __launch_bounds__(prep::kThreads) step_prep_kernel(StepArgs s) {
       if (bits) raise_error(err, bits);
     }
     if (m.slot < 0 || m.slot >= s.num_slots) continue;
-    const long long src = static_cast<long long>(t) * s.kv_chunks;
     const long long dst = static_cast<long long>(m.slot) * s.kv_chunks;
-    for (int c = lane; c < s.kv_chunks; c += 32) {
-      const int4 kk = __ldg(s.k + src + c);
-      const int4 vv = __ldg(s.v + src + c);
-      s.kc[dst + c] = kk;
-      s.vc[dst + c] = vv;
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) {
+      const int c = u * 32 + lane;
+      if (c < s.kv_chunks) {
+        s.kc[dst + c] = xk[u];
+        s.vc[dst + c] = xv[u];
+      }
     }
+    if (s.kv_chunks > 32 * kPre)  // wider rows: the rest in batches
+      warp_copy_rows<4>(s.kc + dst + 32 * kPre, s.k + src + 32 * kPre, s.vc + dst + 32 * kPre,
+                        s.v + src + 32 * kPre, s.kv_chunks - 32 * kPre, lane);
   }
   for (int i = gw; i < a.R_pad; i += nw) {
     const int row = i < a.R ? s_qsl[i + 1] - 1 : max(a.N - 1, 0);
     const bool ok = row >= 0 && row < s.num_hidden_rows;
     if (!ok && lane == 0) raise_error(err, RB_EBIT_ROW_INDEX);
     int4* dst = s.rows_out + static_cast<long long>(i) * s.hid_chunks;
-    const int4* src = s.hidden + static_cast<long long>(ok ? row : 0) * s.hid_chunks;
-    for (int c = lane; c < s.hid_chunks; c += 32)
-      dst[c] = ok ? __ldg(src + c) : make_int4(0, 0, 0, 0);
+    const int4* src = ok ? s.hidden + static_cast<long long>(row) * s.hid_chunks : nullptr;
+    warp_copy_rows<8>(dst, src, nullptr, nullptr, s.hid_chunks, lane);
   }
 }
 
