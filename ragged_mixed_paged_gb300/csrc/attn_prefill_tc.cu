@@ -311,32 +311,38 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
   // complete takes the bounded waits one by one.
   auto test = [](uint64_t* bar, uint32_t phase) { return mbar_test_relaxed(bar, phase); };
   // Shared-memory descriptors are built once: a k-step moves the start address by 32 bytes
-  // within a 128-byte swizzle atom, a 64-dim half by a half tile (the address field counts
-  // 16-byte units in the descriptor's low bits, which no step carries out of).
+  // within a 128-byte swizzle atom, a 64-dim half by a half tile, a stage or a Q tile by whole
+  // tiles.  All of these only add to the address field in the descriptor's low word (which no
+  // step carries out of), so the MMAs take the two 32-bit halves and add to the low one.
   const uint64_t q_desc0 = tc::sdesc_sw128(smem_base + C::kQOffset, 16, 1024);
   const uint64_t k_desc0 = tc::sdesc_sw128(smem_base, 16, 1024);
   const uint64_t v_desc0 = tc::sdesc_sw128(smem_base + C::kVOffset, C::kHalfBytes, 1024);
-  auto step = [](int ks, uint32_t half_bytes) -> uint64_t {
-    return static_cast<uint64_t>(((ks >> 2) * half_bytes + (ks & 3) * 32) >> 4);
+  const uint32_t q_lo = static_cast<uint32_t>(q_desc0), k_lo = static_cast<uint32_t>(k_desc0),
+                 v_lo = static_cast<uint32_t>(v_desc0);
+  const uint32_t q_hi = static_cast<uint32_t>(q_desc0 >> 32),
+                 k_hi = static_cast<uint32_t>(k_desc0 >> 32),
+                 v_hi = static_cast<uint32_t>(v_desc0 >> 32);
+  auto step = [](int ks, uint32_t half_bytes) -> uint32_t {
+    return ((ks >> 2) * half_bytes + (ks & 3) * 32) >> 4;
   };
   auto issue_s = [&](int x, uint32_t kt) {  // S_x = Q_x K^T into S_x
-    const uint64_t kd = k_desc0 + (((kt % C::kStagesK) * C::kTileBytes) >> 4);
-    const uint64_t qd = q_desc0 + ((x * C::kQBytes) >> 4);
+    const uint32_t kd = k_lo + (((kt % C::kStagesK) * C::kTileBytes) >> 4);
+    const uint32_t qd = q_lo + ((x * C::kQBytes) >> 4);
 #pragma unroll
     for (int ks = 0; ks < HD / 16; ++ks)
-      tc::mma_ss(tmem + C::col_s(x), qd + step(ks, C::kQHalfBytes), kd + step(ks, C::kHalfBytes),
-                 idesc_s, ks > 0 ? 1u : 0u);
+      tc::mma_ss_lh(tmem + C::col_s(x), qd + step(ks, C::kQHalfBytes), q_hi,
+                    kd + step(ks, C::kHalfBytes), k_hi, idesc_s, ks > 0 ? 1u : 0u);
     tc::commit(&sh.s_full[x]);
     issued = true;
   };
   // O_x (+)= P_x V.  Only the side's last P V of a unit is committed on its own (o_done): an
   // earlier one is covered by the commit of the S issued after it.
   auto issue_pv = [&](int x, uint32_t kt, bool first, bool last) {
-    const uint64_t vd = v_desc0 + (((kt % C::kStagesV) * C::kTileBytes) >> 4);
+    const uint32_t vd = v_lo + (((kt % C::kStagesV) * C::kTileBytes) >> 4);
 #pragma unroll
     for (int kk = 0; kk < C::kN / 16; ++kk)
-      tc::mma_ts(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, vd + ((kk * 16 * 128) >> 4),
-                 idesc_o, (first && kk == 0) ? 0u : 1u);
+      tc::mma_ts_lh(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, vd + ((kk * 16 * 128) >> 4),
+                    v_hi, idesc_o, (first && kk == 0) ? 0u : 1u);
     if (last) tc::commit(&sh.o_done[x]);
   };
   for (int k = 0;; ++k) {
