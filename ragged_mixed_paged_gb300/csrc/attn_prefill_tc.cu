@@ -328,10 +328,12 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
   auto issue_s = [&](int x, uint32_t kt) {  // S_x = Q_x K^T into S_x
     const uint32_t kd = k_lo + (((kt % C::kStagesK) * C::kTileBytes) >> 4);
     const uint32_t qd = q_lo + ((x * C::kQBytes) >> 4);
+    const uint32_t d = tmem + C::col_s(x);
+    tc::mma_ss_lh(d, qd, q_hi, kd, k_hi, idesc_s, 0u);
 #pragma unroll
-    for (int ks = 0; ks < HD / 16; ++ks)
-      tc::mma_ss_lh(tmem + C::col_s(x), qd + step(ks, C::kQHalfBytes), q_hi,
-                    kd + step(ks, C::kHalfBytes), k_hi, idesc_s, ks > 0 ? 1u : 0u);
+    for (int ks = 1; ks < HD / 16; ++ks)
+      tc::mma_ss_lh_acc(d, qd + step(ks, C::kQHalfBytes), q_hi, kd + step(ks, C::kHalfBytes),
+                        k_hi, idesc_s);
     tc::commit(&sh.s_full[x]);
     issued = true;
   };
@@ -339,10 +341,11 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
   // earlier one is covered by the commit of the S issued after it.
   auto issue_pv = [&](int x, uint32_t kt, bool first, bool last) {
     const uint32_t vd = v_lo + (((kt % C::kStagesV) * C::kTileBytes) >> 4);
+    const uint32_t d = tmem + C::col_o(x), p = tmem + C::col_s(x);
+    tc::mma_ts_lh(d, p, vd, v_hi, idesc_o, first ? 0u : 1u);
 #pragma unroll
-    for (int kk = 0; kk < C::kN / 16; ++kk)
-      tc::mma_ts_lh(tmem + C::col_o(x), tmem + C::col_s(x) + kk * 8, vd + ((kk * 16 * 128) >> 4),
-                    v_hi, idesc_o, (first && kk == 0) ? 0u : 1u);
+    for (int kk = 1; kk < C::kN / 16; ++kk)
+      tc::mma_ts_lh_acc(d, p + kk * 8, vd + ((kk * 16 * 128) >> 4), v_hi, idesc_o);
     if (last) tc::commit(&sh.o_done[x]);
   };
   for (int k = 0;; ++k) {
