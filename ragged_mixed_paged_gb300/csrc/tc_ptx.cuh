@@ -30,25 +30,10 @@ __device__ __forceinline__ void fence_after_sync() {
 }
 
 // ---- MMA: D[tmem] (+)= A * B, kind::f16 (bf16 inputs, fp32 accumulate), one CTA ----
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// A operand read from tensor memory.
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-// The same two with each shared-memory descriptor passed as its 32-bit halves (the MMA loops
-// only ever add to a descriptor's low word: start address and leading byte offset).
+// Each shared-memory descriptor is passed as its two 32-bit halves and joined inside the PTX:
+// the MMA loops only ever add to a descriptor's low word (start address and leading byte
+// offset), so they need no 64-bit arithmetic per MMA.  `_ss`: A and B in shared memory;
+// `_ts`: A read from tensor memory.
 __device__ __forceinline__ void mma_ss_lh(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi,
                                           uint32_t b_lo, uint32_t b_hi, uint32_t idesc,
                                           uint32_t accumulate) {
