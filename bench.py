@@ -537,8 +537,8 @@ def run_ours(args, rank, world, local):
 
 
 def measure_e2e(spec, tens, buf, dev, args, flush, world):
-    """Same step through the public API with inputs copied from pinned host memory and the
-    results read back, copies inside the timed region."""
+    """Same step through the C ABI with host buffers (``rb_step_host``): inputs copied from
+    pinned host memory and the results read back inside the timed region."""
     import torch
 
     import ragged_mixed_paged_gb300 as rb
@@ -562,14 +562,13 @@ def measure_e2e(spec, tens, buf, dev, args, flush, world):
     h2d = sum(t.numel() * t.element_size() for t in host_in.values())
     d2h = sum(t.numel() * t.element_size() for t in host_out.values())
 
-    step_fn = rb.run_step if args.four_calls else rb.run_step_fused
+    # one rb_step_host call: the C ABI enqueues the host-to-device copies of the step's inputs,
+    # the step and the device-to-host copies of its results
+    ins = [(dst[k], t) for k, t in host_in.items()]
+    outs = [(t, src_out[k]) for k, t in host_out.items()]
 
     def step():
-        for k, t in host_in.items():
-            dst[k].copy_(t, non_blocking=True)
-        step_fn(buf)
-        for k, t in host_out.items():
-            t.copy_(src_out[k], non_blocking=True)
+        rb.run_step_host(buf, ins, outs)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -586,7 +585,8 @@ def measure_e2e(spec, tens, buf, dev, args, flush, world):
     ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     ms = reduce_over_ranks(ms, "max", world, dev)
     return {"value": world * spec.num_tokens / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "entry": "rb_step_host (C ABI, host buffers)"}
 
 
 def run_trajectory(args, rank, world, local):

@@ -365,6 +365,35 @@ typedef struct rb_step_args {
 rb_status rb_step(const rb_step_args* args, void* stream);
 
 /*
+ * rb_host_copy — one contiguous copy between caller-owned host memory and caller-owned device
+ * memory: `bytes` bytes from `src` to `dst` (both null only when `bytes` is 0).  Page-locked
+ * host memory makes the copy asynchronous; pageable memory works but the copy then blocks the
+ * calling thread.
+ */
+typedef struct rb_host_copy {
+  void* dst;
+  const void* src;
+  size_t bytes;
+} rb_host_copy;
+
+/*
+ * rb_step_host — rb_step with its inputs brought in from host memory and its results returned
+ * to it: after every host check of rb_step passes, enqueues on `stream` the `num_in` host-to-
+ * device copies `in` (typically the token and page tables, the counters, q / k / v and the
+ * hidden states, into the device buffers `args` points at), then the step exactly as rb_step,
+ * then the `num_out` device-to-host copies `out` (typically the attention output, the gathered
+ * rows and the scalars with the error word).  One cudaMemcpyAsync per copy, in array order;
+ * nothing else is allocated or synchronised.  The step's inputs and outputs are what the
+ * caller names: the library does not check that the copies cover them.
+ * Errors: RB_ERR_INVALID_ARG for a null `args`, negative counts, a null array with a nonzero
+ * count or a null pointer in a copy of nonzero size; the host checks of rb_step; all returned
+ * before anything is enqueued.  RB_ERR_CUDA if enqueueing a copy or a launch fails (what was
+ * enqueued before stays enqueued).  Device bits as rb_step sets them.
+ */
+rb_status rb_step_host(const rb_step_args* args, const rb_host_copy* in, int32_t num_in,
+                       const rb_host_copy* out, int32_t num_out, void* stream);
+
+/*
  * Persistent batch — one row per resident request, every column device-resident and
  * caller-owned ("vLLM 源码完全拆解（五）…", "行号是一种短生命周期地址": the row is the common key
  * of the request's token history, counters and page row; a move must carry every column).

@@ -65,6 +65,10 @@ class rb_batch_update(ctypes.Structure):
             "d_cached_blocks")]
 
 
+class rb_host_copy(ctypes.Structure):
+    _fields_ = [("dst", ctypes.c_void_p), ("src", ctypes.c_void_p), ("bytes", ctypes.c_size_t)]
+
+
 class rb_step_args(ctypes.Structure):
     _fields_ = ([("dims", ctypes.POINTER(rb_dims))] +
                 [(n, ctypes.c_int32) for n in ("num_reqs", "num_reqs_padded", "num_tokens",
@@ -106,6 +110,8 @@ def _load():
         "rb_batch_update_workspace_size": (I32, [I32, ctypes.POINTER(ctypes.c_size_t)]),
         "rb_cascade_prefix_len": (I32, [I32, P, I32, I32]),
         "rb_step": (I32, [ctypes.POINTER(rb_step_args), P]),
+        "rb_step_host": (I32, [ctypes.POINTER(rb_step_args), ctypes.POINTER(rb_host_copy), I32,
+                               ctypes.POINTER(rb_host_copy), I32, P]),
         "rb_paged_attention_cascade_workspace_size": (ctypes.c_size_t, [PD, I32, I32]),
         "rb_paged_attention_cascade": (I32, [PD, I32, I32, I32, I32, P, P, P, P, P, P,
                                              ctypes.c_float, P, P, ctypes.c_size_t, P, P]),

@@ -139,10 +139,11 @@ __global__ void __launch_bounds__(prep::kThreads) step_prep_kernel(StepArgs s) {
 }  // namespace
 }  // namespace rb
 
-extern "C" rb_status rb_step(const rb_step_args* args, void* stream) {
-  using namespace rb;
-  if (args == nullptr || args->dims == nullptr) return RB_ERR_INVALID_ARG;
-  const rb_step_args& x = *args;
+namespace rb {
+namespace {
+
+// Every host check of rb_step, and the launch arguments it builds; nothing is enqueued.
+rb_status step_build(const rb_step_args& x, StepArgs* out_sa, attn::AttnSetup* out_su) {
   const rb_dims& d = *x.dims;
   prep::PrepArgs p;
   rb_status st = prep::prep_args_of(
@@ -161,7 +162,7 @@ extern "C" rb_status rb_step(const rb_step_args* args, void* stream) {
   if (!aligned16(x.d_k) || !aligned16(x.d_v) || !aligned16(x.d_hidden) ||
       !aligned16(x.d_rows_out))
     return RB_ERR_INVALID_ARG;
-  attn::AttnSetup su;
+  attn::AttnSetup& su = *out_su;
   st = attn::attn_setup(x.dims, x.num_reqs, x.num_tokens, x.num_tokens_padded, x.d_q,
                         x.d_k_cache, x.d_v_cache, x.d_block_table, x.d_query_start_loc,
                         x.d_seq_lens, x.softmax_scale, x.d_attn_out, x.d_workspace,
@@ -170,7 +171,7 @@ extern "C" rb_status rb_step(const rb_step_args* args, void* stream) {
   st = attn::attn_encode_maps(&su);
   if (st != RB_OK) return st;
 
-  StepArgs sa;
+  StepArgs& sa = *out_sa;
   sa.p = p;
   sa.at = su.a;
   sa.head_dim = d.head_dim;
@@ -184,8 +185,12 @@ extern "C" rb_status rb_step(const rb_step_args* args, void* stream) {
   sa.rows_out = static_cast<int4*>(x.d_rows_out);
   sa.hid_chunks = static_cast<int>(2LL * x.hidden_size / 16);
   sa.num_hidden_rows = x.num_hidden_rows;
+  return RB_OK;
+}
 
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
+// The step's memset and two launches on stream `s`.
+rb_status step_enqueue(const rb_step_args& x, const StepArgs& sa, const attn::AttnSetup& su,
+                       cudaStream_t s) {
   if (cudaMemsetAsync(x.d_scalars + 3, 0, sizeof(int32_t), s) != cudaSuccess) return RB_ERR_CUDA;
   const size_t smem = static_cast<size_t>(x.num_reqs + 1) * sizeof(int32_t);
   if (smem > 48 * 1024 &&
@@ -199,4 +204,48 @@ extern "C" rb_status rb_step(const rb_step_args* args, void* stream) {
   if (last_launch_status() != RB_OK) return RB_ERR_CUDA;
   note_launches(1);
   return attn::attn_main(su, s);
+}
+
+}  // namespace
+}  // namespace rb
+
+extern "C" rb_status rb_step(const rb_step_args* args, void* stream) {
+  using namespace rb;
+  if (args == nullptr || args->dims == nullptr) return RB_ERR_INVALID_ARG;
+  StepArgs sa;
+  attn::AttnSetup su;
+  const rb_status st = step_build(*args, &sa, &su);
+  if (st != RB_OK) return st;
+  return step_enqueue(*args, sa, su, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" rb_status rb_step_host(const rb_step_args* args, const rb_host_copy* in,
+                                  int32_t num_in, const rb_host_copy* out, int32_t num_out,
+                                  void* stream) {
+  using namespace rb;
+  if (args == nullptr || args->dims == nullptr || num_in < 0 || num_out < 0 ||
+      (num_in > 0 && in == nullptr) || (num_out > 0 && out == nullptr))
+    return RB_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < num_in; ++i)
+    if (in[i].bytes > 0 && (in[i].dst == nullptr || in[i].src == nullptr))
+      return RB_ERR_INVALID_ARG;
+  for (int32_t i = 0; i < num_out; ++i)
+    if (out[i].bytes > 0 && (out[i].dst == nullptr || out[i].src == nullptr))
+      return RB_ERR_INVALID_ARG;
+  StepArgs sa;
+  attn::AttnSetup su;
+  rb_status st = step_build(*args, &sa, &su);
+  if (st != RB_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int32_t i = 0; i < num_in; ++i)
+    if (in[i].bytes > 0 &&
+        cudaMemcpyAsync(in[i].dst, in[i].src, in[i].bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+      return RB_ERR_CUDA;
+  st = step_enqueue(*args, sa, su, s);
+  if (st != RB_OK) return st;
+  for (int32_t i = 0; i < num_out; ++i)
+    if (out[i].bytes > 0 &&
+        cudaMemcpyAsync(out[i].dst, out[i].src, out[i].bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+      return RB_ERR_CUDA;
+  return RB_OK;
 }

@@ -3,7 +3,9 @@ gather_rows, on one stream, with no host synchronisation inside.
 
 ``StepBuffers`` holds fixed-address device buffers sized once (as a CUDA-graph runner keeps
 them); ``run_step`` enqueues the four library calls, ``run_step_fused`` the single ``rb_step``
-call that does the same work in one memset and two launches (same results, bit for bit).  The
+call that does the same work in one memset and two launches (same results, bit for bit), and
+``run_step_host`` the ``rb_step_host`` call that also copies the inputs in from host memory
+and the results back.  The
 step's error word is the fourth scalar written by ``prepare_inputs``; the KV write and the
 attention OR their bits into it.
 """
@@ -136,3 +138,25 @@ def run_step_fused(b: StepBuffers, stream=None, softmax_scale: Optional[float] =
     if b._step_args is None or softmax_scale is not None:
         b._step_args = _step_args(b, softmax_scale)
     rb._check("rb_step", rb.lib.rb_step(ctypes.byref(b._step_args), rb._stream(stream)))
+
+
+def _copies(pairs):
+    arr = (rb.rb_host_copy * max(len(pairs), 1))()
+    for i, (dst, src) in enumerate(pairs):
+        n = src.numel() * src.element_size()
+        if dst.numel() * dst.element_size() != n:
+            raise ValueError("a host copy's source and destination differ in size")
+        arr[i] = rb.rb_host_copy(dst.data_ptr(), src.data_ptr(), n)
+    return arr
+
+
+def run_step_host(b: StepBuffers, host_in, host_out, stream=None,
+                  softmax_scale: Optional[float] = None) -> None:
+    """Enqueue one ``rb_step_host`` call: the ``host_in`` copies (``(device_dst, host_src)``
+    tensor pairs, contiguous), the step, then the ``host_out`` copies (``(host_dst,
+    device_src)``).  Page-locked host tensors keep the copies asynchronous."""
+    if b._step_args is None or softmax_scale is not None:
+        b._step_args = _step_args(b, softmax_scale)
+    ins, outs = _copies(host_in), _copies(host_out)
+    rb._check("rb_step_host", rb.lib.rb_step_host(ctypes.byref(b._step_args), ins, len(host_in),
+                                                  outs, len(host_out), rb._stream(stream)))

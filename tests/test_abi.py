@@ -236,3 +236,27 @@ def test_step_host_checks(lib):
     args.num_reqs = args.num_reqs_padded = 1
     args.num_tokens = args.num_tokens_padded = 1
     assert L.rb_step(ctypes.byref(args), None) == 1            # no metadata buffers
+
+
+def test_step_host_copy_checks(lib):
+    """rb_step_host rejects bad copy lists (and rb_step's own bad arguments) before it enqueues
+    anything: no GPU is touched."""
+    L = lib.lib
+    none = ctypes.POINTER(lib.rb_host_copy)()
+    assert L.rb_step_host(None, none, 0, none, 0, None) == 1
+    args = lib.rb_step_args()
+    d = _dims(lib)
+    args.dims = ctypes.pointer(d)
+    args.num_reqs = args.num_reqs_padded = 1
+    args.num_tokens = args.num_tokens_padded = 1
+    two = (lib.rb_host_copy * 2)()
+    buf = ctypes.create_string_buffer(64)
+    addr = ctypes.addressof(buf)
+    two[0] = lib.rb_host_copy(addr, addr, 16)
+    two[1] = lib.rb_host_copy(None, addr, 16)                # null destination, 16 bytes
+    assert L.rb_step_host(ctypes.byref(args), none, -1, none, 0, None) == 1   # negative count
+    assert L.rb_step_host(ctypes.byref(args), none, 1, none, 0, None) == 1    # null array
+    assert L.rb_step_host(ctypes.byref(args), two, 2, none, 0, None) == 1     # null pointer
+    assert L.rb_step_host(ctypes.byref(args), none, 0, two, 2, None) == 1
+    two[1] = lib.rb_host_copy(None, None, 0)                 # empty copies need no pointers
+    assert L.rb_step_host(ctypes.byref(args), two, 2, two, 2, None) == 1      # no metadata buffers

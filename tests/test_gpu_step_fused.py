@@ -1,6 +1,7 @@
 """rb_step (one memset and two launches) against the four separate calls: every output bit for
 bit — metadata, phase flags, both caches, attention output, gathered rows, error word — and,
-on a few cases, directly against the oracle."""
+on a few cases, directly against the oracle; rb_step_host (host buffers in and out) against
+rb_step."""
 import numpy as np
 import pytest
 import torch
@@ -108,4 +109,30 @@ def test_fused_step_error_bits(rb):
     rb.run_step_fused(b)
     torch.cuda.synchronize()
     assert int(a.meta["scalars"][3].item()) & 0x010
+    _same(a, b)
+
+
+@pytest.mark.parametrize("name", ["cfg1_pad24", "cfg2", "mix_step57"])
+def test_step_host_equals_device_step(rb, name):
+    """rb_step_host (inputs copied in from pinned host memory, results copied back) against
+    rb_step on inputs already on the device: the same outputs, bit for bit."""
+    spec = CASES[name]()
+    a, b, _ = _twins(rb, spec)
+    rb.run_step_fused(a)
+    host_in = []
+    for t in (b.token_table, b.block_table, b.num_computed, b.num_scheduled, b.q, b.k, b.v,
+              b.hidden):
+        h = t.cpu().pin_memory()
+        t.zero_()  # the copies must bring the inputs
+        host_in.append((t, h))
+    got = {k: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+           for k, t in (("attn", b.attn_out), ("rows", b.rows_out), ("scalars", b.meta["scalars"]))}
+    host_out = [(got["attn"], b.attn_out), (got["rows"], b.rows_out),
+                (got["scalars"], b.meta["scalars"])]
+    rb.run_step_host(b, host_in, host_out)
+    torch.cuda.synchronize()
+    assert int(got["scalars"][3]) == 0
+    assert torch.equal(got["attn"], a.attn_out.cpu())
+    assert torch.equal(got["rows"], a.rows_out.cpu())
+    assert torch.equal(got["scalars"], a.meta["scalars"].cpu())
     _same(a, b)
