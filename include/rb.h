@@ -21,7 +21,9 @@
  *    allocates it and keeps it alive until the work queued on `stream` has finished.  The
  *    library allocates no device memory and never synchronises: each call only enqueues
  *    kernels (and, for rb_prepare_inputs, one 4-byte memset) on `stream`, a cudaStream_t passed
- *    as void* (NULL = the legacy default stream).
+ *    as void* (NULL = the legacy default stream).  The one exception to "no device memory" is
+ *    the 64 MiB scratch array of rb_paged_attention_static_ws: a static device array of the
+ *    library's module, so every GPU that loads the library holds it until the process exits.
  *  - All index arrays are int32.  bf16 tensors are passed as void* holding IEEE bfloat16 bits.
  *  - Host-side checks (null pointers, sizes, alignment, unsupported shapes) run before anything
  *    is enqueued and return a status other than RB_OK; nothing is enqueued then.
@@ -242,9 +244,13 @@ rb_status rb_paged_attention_profiled(const rb_dims* dims, int32_t num_reqs, int
  * Errors: RB_ERR_CAPACITY when rb_paged_attention_workspace_size(dims, num_reqs, num_tokens)
  * exceeds 64 MiB (at 8 kv heads and head_dim 128: more than 991 requests); RB_ERR_CUDA if the
  * array's device address cannot be obtained.  The first call on a device looks that address
- * up with the device current; make it before any stream capture.  All calls on a device share
+ * up with the device current and keeps it for later calls; make it before any stream capture.
+ * The kept address belongs to the device's primary context (the one the CUDA runtime uses):
+ * after cudaDeviceReset, or from a context the caller made itself with the driver API, it is
+ * not valid, so such callers must not use this entry point.  All calls on a device share
  * the array: calls whose work overlaps on the GPU (e.g. two streams at once) race on it, so
- * serialise them.  Nothing in the array needs clearing between calls.
+ * serialise them.  Nothing in the array needs clearing between calls: the planner launch
+ * rewrites every field the later launches read.
  */
 rb_status rb_paged_attention_static_ws(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
                                        int32_t num_tokens_padded, const void* d_q,

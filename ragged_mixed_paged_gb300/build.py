@@ -48,8 +48,13 @@ def _compile(nvcc, src, extra):
 
 
 def build(verbose: bool = False, extra_flags=()) -> str:
-    """Compile every .cu under csrc/ and link librb.so; returns the library path."""
+    """Compile every .cu under csrc/ and link librb.so; returns the library path.
+
+    ``RB_NVTX=1`` in the environment compiles an NVTX range around every C-ABI call (the
+    objects are then rebuilt: remove ``_build/`` when switching it on or off)."""
     nvcc = _nvcc()
+    if os.environ.get("RB_NVTX", "0") not in ("", "0"):
+        extra_flags = list(extra_flags) + ["-DRB_NVTX"]
     os.makedirs(OBJ, exist_ok=True)
     srcs = sources()
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(srcs), os.cpu_count() or 4))) as ex:

@@ -291,6 +291,7 @@ extern "C" rb_status rb_paged_attention(const rb_dims* dims, int32_t num_reqs, i
                                         const int32_t* d_seq_lens, float softmax_scale,
                                         void* d_out, void* d_workspace, size_t workspace_bytes,
                                         int32_t* d_error_word, void* stream) {
+  rb::CallRange range_("rb_paged_attention");
   return paged_attention_impl(dims, num_reqs, num_tokens, num_tokens_padded, d_q, d_k_cache,
                               d_v_cache, d_block_table, d_query_start_loc, d_seq_lens,
                               softmax_scale, d_out, d_workspace, workspace_bytes, d_error_word,
@@ -303,6 +304,7 @@ extern "C" rb_status rb_paged_attention_profiled(
     const int32_t* d_query_start_loc, const int32_t* d_seq_lens, float softmax_scale, void* d_out,
     void* d_workspace, size_t workspace_bytes, int32_t* d_error_word, void* stream,
     void* const* events, int32_t num_events) {
+  rb::CallRange range_("rb_paged_attention_profiled");
   if (num_events < 0 || (num_events > 0 && events == nullptr)) return RB_ERR_INVALID_ARG;
   return paged_attention_impl(dims, num_reqs, num_tokens, num_tokens_padded, d_q, d_k_cache,
                               d_v_cache, d_block_table, d_query_start_loc, d_seq_lens,
@@ -327,6 +329,7 @@ extern "C" rb_status rb_paged_attention_cascade(
     const int32_t* d_block_table, const int32_t* d_query_start_loc, const int32_t* d_seq_lens,
     float softmax_scale, void* d_out, void* d_workspace, size_t workspace_bytes,
     int32_t* d_error_word, void* stream) {
+  rb::CallRange range_("rb_paged_attention_cascade");
   return paged_attention_impl(dims, num_reqs, num_tokens, num_tokens_padded, d_q, d_k_cache,
                               d_v_cache, d_block_table, d_query_start_loc, d_seq_lens,
                               softmax_scale, d_out, d_workspace, workspace_bytes, d_error_word,

@@ -21,6 +21,9 @@ static __device__ __align__(256) unsigned char g_attention_scratch[kStaticScratc
 
 // Device address of the array on the current device.  Looked up once per device, on the first
 // call made with that device current; that first call should come before any stream capture.
+// A symbol's address belongs to a CUDA context: the one kept here is the device's primary
+// context's (the runtime's), so it does not survive cudaDeviceReset and does not hold in a
+// context the caller created with the driver API.
 void* scratch_for_current_device() {
   static std::mutex mu;
   static void* addr[64] = {nullptr};
@@ -42,6 +45,7 @@ extern "C" rb_status rb_paged_attention_static_ws(
     const void* d_q, const void* d_k_cache, const void* d_v_cache, const int32_t* d_block_table,
     const int32_t* d_query_start_loc, const int32_t* d_seq_lens, float softmax_scale,
     void* d_out, int32_t* d_error_word, void* stream) {
+  rb::CallRange range_("rb_paged_attention_static_ws");
   if (dims == nullptr || num_reqs < 0 || num_tokens < 0) return RB_ERR_INVALID_ARG;
   const size_t need = rb_paged_attention_workspace_size(dims, num_reqs, num_tokens);
   if (need == 0) return RB_ERR_INVALID_ARG;

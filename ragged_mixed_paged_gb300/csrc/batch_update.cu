@@ -441,6 +441,7 @@ extern "C" rb_status rb_batch_apply_update(const rb_batch* batch, const rb_batch
                                            int32_t* d_num_scheduled, int32_t* d_row_of_sched,
                                            void* d_workspace, size_t workspace_bytes,
                                            int32_t* d_error_word, void* stream) {
+  rb::CallRange range_("rb_batch_apply_update");
   using namespace rb;
   if (batch == nullptr || update == nullptr) return RB_ERR_INVALID_ARG;
   const rb_batch& b = *batch;

@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(kThreads)
 extern "C" rb_status rb_gather_rows(int32_t num_rows, int32_t hidden_size, int32_t num_hidden_rows,
                                     const void* d_hidden, const int32_t* d_indices, void* d_out,
                                     int32_t* d_error_word, void* stream) {
+  rb::CallRange range_("rb_gather_rows");
   using namespace rb;
   if (num_rows < 0 || hidden_size < 1 || num_hidden_rows < 0) return RB_ERR_INVALID_ARG;
   if ((2LL * hidden_size) % 16 != 0) return RB_ERR_UNSUPPORTED;

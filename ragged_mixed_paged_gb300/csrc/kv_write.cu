@@ -45,6 +45,7 @@ __global__ void __launch_bounds__(kThreads)
 extern "C" rb_status rb_kv_write(const rb_dims* dims, int32_t num_tokens_padded, const void* d_k,
                                  const void* d_v, const int32_t* d_slot_mapping, void* d_k_cache,
                                  void* d_v_cache, int32_t* d_error_word, void* stream) {
+  rb::CallRange range_("rb_kv_write");
   using namespace rb;
   if (dims == nullptr || num_tokens_padded < 0) return RB_ERR_INVALID_ARG;
   const rb_dims& d = *dims;

@@ -117,6 +117,7 @@ extern "C" rb_status rb_prepare_inputs(const rb_dims* dims, int32_t num_reqs,
                                        int32_t* d_logits_indices, int32_t* d_scalars,
                                        const int32_t* d_num_prompt, int32_t* d_is_prefilling,
                                        int32_t* d_discard_request_mask, void* stream) {
+  rb::CallRange range_("rb_prepare_inputs");
   using namespace rb;
   using namespace rb::prep;
   if (dims == nullptr) return RB_ERR_INVALID_ARG;

@@ -10,7 +10,24 @@
 
 #include "rb.h"
 
+#ifdef RB_NVTX
+#include <nvtx3/nvToolsExt.h>
+#endif
+
 namespace rb {
+
+// One NVTX range around each C-ABI call, for timelines in a profiler.  Compiled in only with
+// -DRB_NVTX (build.py: RB_NVTX=1 in the environment); otherwise it costs nothing.
+struct CallRange {
+#ifdef RB_NVTX
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+#else
+  explicit CallRange(const char*) {}
+#endif
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
 
 // ---------------------------------------------------------------------------------------------
 // host side

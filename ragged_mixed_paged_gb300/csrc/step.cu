@@ -210,6 +210,7 @@ rb_status step_enqueue(const rb_step_args& x, const StepArgs& sa, const attn::At
 }  // namespace rb
 
 extern "C" rb_status rb_step(const rb_step_args* args, void* stream) {
+  rb::CallRange range_("rb_step");
   using namespace rb;
   if (args == nullptr || args->dims == nullptr) return RB_ERR_INVALID_ARG;
   StepArgs sa;
@@ -222,6 +223,7 @@ extern "C" rb_status rb_step(const rb_step_args* args, void* stream) {
 extern "C" rb_status rb_step_host(const rb_step_args* args, const rb_host_copy* in,
                                   int32_t num_in, const rb_host_copy* out, int32_t num_out,
                                   void* stream) {
+  rb::CallRange range_("rb_step_host");
   using namespace rb;
   if (args == nullptr || args->dims == nullptr || num_in < 0 || num_out < 0 ||
       (num_in > 0 && in == nullptr) || (num_out > 0 && out == nullptr))

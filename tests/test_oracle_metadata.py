@@ -263,3 +263,29 @@ def test_manager_table_slots_equal_one_big_page(ratio, seed):
     # every real slot lies in a manager block the request owns, never in the null one
     for s in want:
         assert s // big != d.null_block // ratio
+
+
+def test_batch_maxima_on_worked_examples():
+    """max_query_len / max_seq_len (the scalars the attention metadata carries, nano-vLLM's
+    max_seqlen_q / max_seqlen_k) on the printed examples: A/B/C of '布局与元数据' has query
+    lengths 7, 1, 12 and sequence lengths 7, 6, 22, so 12 and 22 (both from C); the runner's
+    example of '2. 模型位置与完整序列长度' has query lengths 1, 3, 2 and sequence lengths 6, 3, 10,
+    so 3 (from B) and 10 (from C) -- a maximum over num_computed would give 8 there."""
+    g = load_golden("batch_layout_abc.json")
+    out = _run(g["inputs"]["num_computed"], g["inputs"]["num_scheduled"], num_reqs_padded=5,
+               num_tokens_padded=24)
+    assert (out["max_query_len"], out["max_seq_len"]) == (12, 22)
+    g = load_golden("runner_flatten_example.json")
+    i = g["inputs"]
+    out = _run(i["num_computed"], i["num_scheduled"], i["block_size"],
+               block_rows=i["block_table"], token_rows=i["token_rows"], num_reqs_padded=4)
+    assert (out["max_query_len"], out["max_seq_len"]) == (3, 10)
+    # nano-vLLM's flattening example (question 8): Seq_0 4 tokens, Seq_1 6 tokens -> max q 6;
+    # scheduled again with 4 cached and 4 new -> seqlen_k 8
+    out = _run([0, 0], [4, 6])
+    assert (out["max_query_len"], out["max_seq_len"]) == (6, 6)
+    out = _run([4], [4])
+    assert (out["max_query_len"], out["max_seq_len"]) == (4, 8)
+    # padded requests (q = 0, seq_len 0) never raise either maximum
+    out = _run([100, 3], [1, 2], num_reqs_padded=8, num_tokens_padded=16)
+    assert (out["max_query_len"], out["max_seq_len"]) == (2, 101)
