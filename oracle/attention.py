@@ -35,6 +35,13 @@ def paged_attention(q: np.ndarray, hist_k: Sequence[np.ndarray], hist_v: Sequenc
     ``q [N_pad, nh, hd]``, ``k_new/v_new [N_pad, nkv, hd]``: this step's rows (flat order).
     ``hist_k[i]/hist_v[i] [c_i, nkv, hd]``: request i's cached keys/values, contiguous.
     ``rows``: if given, only these flat token indices are computed; the other real rows are NaN.
+
+    For request i and kv head kv the selected queries of the head group are stacked: the scores
+    of query j against every key of the request are one matrix product, the keys past its
+    visible length ``c_i + j + 1`` get weight exp(-inf) = 0, each row is normalised by its own
+    maximum and sum, and the output is the weights times V.  Every query row is computed on its
+    own (stacking rows only batches independent products), so the result of a row does not
+    depend on which other rows are asked for.
     """
     q = np.asarray(q, np.float64)
     k_new = np.asarray(k_new, np.float64)
@@ -55,18 +62,31 @@ def paged_attention(q: np.ndarray, hist_k: Sequence[np.ndarray], hist_v: Sequenc
         n_new = e - s
         c = int(seq_lens[i]) - n_new
         assert c == hist_k[i].shape[0], "seq_len - query_len must equal the cached length"
-        js = [j for j in range(n_new) if wanted is None or (s + j) in wanted]
-        if not js:
+        js = np.array([j for j in range(n_new) if wanted is None or (s + j) in wanted], np.int64)
+        if js.size == 0:
             continue
-        K = np.concatenate([np.asarray(hist_k[i], np.float64), k_new[s:e]], axis=0)  # [L, nkv, hd]
-        V = np.concatenate([np.asarray(hist_v[i], np.float64), v_new[s:e]], axis=0)
-        for h in range(nh):
-            kv = h // group
-            for j in js:
-                visible = c + j + 1                       # keys 0 .. c + j
-                scores = K[:visible, kv, :] @ q[s + j, h, :] * scale
-                scores = scores - scores.max()
+        L = c + n_new
+        key = np.arange(L)
+        # rows per product: bounds the [rows, group, L] score array (~32M values)
+        step = max(1, (1 << 25) // (group * L))
+        for kv in range(nkv):
+            # keys and values of this kv head: the cached history, then this step's rows
+            Kh = np.empty((L, hd), np.float64)
+            Vh = np.empty((L, hd), np.float64)
+            Kh[:c] = hist_k[i][:, kv, :]
+            Vh[:c] = hist_v[i][:, kv, :]
+            Kh[c:] = k_new[s:e, kv, :]
+            Vh[c:] = v_new[s:e, kv, :]
+            heads = slice(kv * group, (kv + 1) * group)      # query heads reading this kv head
+            for b in range(0, js.size, step):
+                jb = js[b:b + step]
+                Qb = q[s + jb, heads, :]                       # [J, group, hd]
+                scores = np.matmul(Qb, Kh.T) * scale           # [J, group, L]
+                visible = c + jb + 1                           # keys 0 .. c + j
+                hidden = key[None, :] >= visible[:, None]      # [J, L]
+                scores = np.where(hidden[:, None, :], -np.inf, scores)
+                scores = scores - scores.max(axis=-1, keepdims=True)
                 p = np.exp(scores)
-                p = p / p.sum()
-                out[s + j, h, :] = p @ V[:visible, kv, :]
+                p = p / p.sum(axis=-1, keepdims=True)
+                out[s + jb, heads, :] = np.matmul(p, Vh)
     return out

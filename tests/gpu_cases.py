@@ -33,11 +33,12 @@ def i32(a, device="cuda"):
 
 
 def to64(t):
-    return t.float().cpu().numpy().astype(np.float64)
+    return t.detach().cpu().to(torch.float64).numpy()
 
 
 class _Lazy:
-    """A history tensor converted to float64 only when the oracle reads it."""
+    """A bf16 history tensor widened only when the oracle reads it (whole, or one kv head's
+    slice as float32, which widens to float64 exactly on assignment)."""
 
     def __init__(self, t):
         self.t = t
@@ -46,6 +47,79 @@ class _Lazy:
     def __array__(self, dtype=None, copy=None):
         a = to64(self.t)
         return a if dtype is None else a.astype(dtype)
+
+    def __getitem__(self, idx):
+        return self.t[idx].float().cpu().numpy()
+
+
+# --------------------------------------------------------------------------- oracle threads
+def _openblas_thread_setters():
+    """(get, set) of the OpenBLAS that numpy loaded, or None: the oracle's per-request calls run
+    in threads, and a BLAS that also spawns threads per call oversubscribes the cores."""
+    import ctypes
+    import glob
+    import os
+
+    paths = glob.glob(os.path.join(os.path.dirname(np.__file__), os.pardir, "numpy.libs",
+                                   "*openblas*"))
+    try:
+        with open("/proc/self/maps") as f:
+            paths += sorted({ln.split()[-1] for ln in f if "openblas" in ln and "/" in ln})
+    except OSError:
+        pass
+    for path in paths:
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for pre, suf in (("scipy_openblas_", "64_"), ("scipy_openblas_", ""), ("openblas_", "64_"),
+                         ("openblas_", "")):
+            get = getattr(lib, f"{pre}get_num_threads{suf}", None)
+            put = getattr(lib, f"{pre}set_num_threads{suf}", None)
+            if get is not None and put is not None:
+                get.restype = ctypes.c_int
+                put.argtypes = [ctypes.c_int]
+                return get, put
+    return None
+
+
+def oracle_attention_threads(q64, hist_k, hist_v, k64, v64, qsl, seq_lens, R, rows,
+                             workers=None):
+    """The oracle's attention for the flat rows ``rows``: one oracle call per request that has
+    any, on that request's own rows (a mixed step gives each request what it gets alone, a pinned
+    property of the oracle), spread over host threads (numpy releases the GIL inside its loops).
+    Falls back to one call over the whole batch when BLAS cannot be pinned to one thread per
+    call."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    qsl = np.asarray(qsl)
+    rows = np.asarray(sorted(set(int(r) for r in rows)), np.int64)
+    owner = np.searchsorted(qsl[1:R + 1], rows, side="right")
+    blas = _openblas_thread_setters()
+    workers = workers or max(1, min(32, (os.cpu_count() or 2) - 1))
+    if blas is None or workers == 1:
+        return oracle.paged_attention(q64, hist_k, hist_v, k64, v64, qsl[:R + 1], seq_lens[:R],
+                                      R, rows=rows.tolist())
+    out = np.full_like(q64, np.nan)
+    out[int(qsl[R]):] = 0.0
+
+    def one(i):  # request i alone (the oracle's result for a request does not depend on others)
+        s, e = int(qsl[i]), int(qsl[i + 1])
+        sel = rows[owner == i]
+        res = oracle.paged_attention(q64[s:e], [hist_k[i]], [hist_v[i]], k64[s:e], v64[s:e],
+                                     [0, e - s], [int(seq_lens[i])], 1, rows=(sel - s).tolist())
+        out[sel] = res[sel - s]
+
+    get, put = blas
+    before = get()
+    put(1)
+    try:
+        with ThreadPoolExecutor(workers) as ex:
+            list(ex.map(one, np.unique(owner).tolist()))
+    finally:
+        put(before)
+    return out
 
 
 def config4_layouts(num_steps):
@@ -113,11 +187,13 @@ def run_attention(rb, spec, tens, meta, error_word=None):
 
 
 def oracle_attention(spec, tens, meta, rows=None):
+    """The oracle's attention of a step (rows not asked for are NaN, padding rows 0)."""
     R = spec.num_reqs
-    return oracle.paged_attention(to64(tens.q), [_Lazy(h) for h in tens.hist_k],
-                                  [_Lazy(h) for h in tens.hist_v], to64(tens.k), to64(tens.v),
-                                  meta["query_start_loc"][:R + 1], meta["seq_lens"][:R], R,
-                                  rows=rows)
+    rows = range(spec.num_tokens) if rows is None else rows
+    return oracle_attention_threads(to64(tens.q), [_Lazy(h) for h in tens.hist_k],
+                                    [_Lazy(h) for h in tens.hist_v], to64(tens.k), to64(tens.v),
+                                    meta["query_start_loc"][:R + 1], meta["seq_lens"][:R], R,
+                                    rows)
 
 
 def compare_attention(got, ref, N, rows=None):
@@ -130,3 +206,21 @@ def compare_attention(got, ref, N, rows=None):
     assert mean_abs <= ATTN_MEAN_ABS, f"mean abs {mean_abs}"
     assert np.all(g[N:] == 0.0), "padding rows must be zero"
     return max_abs, mean_abs
+
+
+def check_kv_write(spec, k_before, v_before, tens, slot_mapping):
+    """The paged KV write of one step, checked on the device: ``cache[slot[t]] = kv[t]`` for
+    every real token t and nothing else changes, except padding tokens' writes, which land in
+    the null page (any winner: its contents are not state)."""
+    d = spec.dims
+    N = spec.num_tokens
+    slots = torch.as_tensor(np.asarray(slot_mapping[:N], np.int64), device=tens.k_cache.device)
+    changed = ((tens.k_cache != k_before).flatten(1).any(1) |
+               (tens.v_cache != v_before).flatten(1).any(1))
+    changed = torch.nonzero(changed).flatten()
+    null_rows = (changed // d.block_size) == d.null_block
+    assert bool(torch.isin(changed[~null_rows], slots).all()), "a row outside the slots changed"
+    assert not bool(((slots // d.block_size) == d.null_block).any()), "a real token in the null page"
+    assert torch.equal(tens.k_cache[slots], tens.k[:N])
+    assert torch.equal(tens.v_cache[slots], tens.v[:N])
+

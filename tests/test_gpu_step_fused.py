@@ -8,7 +8,8 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_cases import compare_attention, config4_specs, oracle_attention, oracle_meta
+from gpu_cases import (check_kv_write, compare_attention, config4_specs, oracle_attention,
+                       oracle_meta, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -80,11 +81,26 @@ def test_fused_step_fuzz(rb, seed):
     _same(a, b)
 
 
-@pytest.mark.parametrize("name", ["cfg1_pad24", "fuzz"])
+ORACLE_CASES = {
+    "cfg1_pad24": (lambda: wl.config1(num_tokens_padded=24), None),
+    "fuzz": (lambda: wl.random_batch(9, num_q_heads=8, num_kv_heads=2, head_dim=128,
+                                     pad_tokens=3), None),
+    "cfg2": (lambda: wl.config2(), None),
+    "cfg3_pad": (lambda: wl.config3(num_real=250), None),
+    "cfg5": (lambda: wl.config5(), 96),   # every decode row + a sample of the chunk's rows
+}
+
+
+@pytest.mark.parametrize("name", sorted(ORACLE_CASES))
 def test_fused_step_vs_oracle(rb, name):
-    spec = (wl.config1(num_tokens_padded=24) if name == "cfg1_pad24" else
-            wl.random_batch(9, num_q_heads=8, num_kv_heads=2, head_dim=128, pad_tokens=3))
+    """rb_step (the entry point bench.py times) against the oracle directly: metadata, phase
+    flags and scalars bit for bit, the KV write (changed rows = the oracle's real slots plus
+    the null page, each real slot holding its token's K and V), attention element-wise, the
+    gathered rows bit for bit."""
+    make, n_random = ORACLE_CASES[name]
+    spec = make()
     buf, tens = _buffers(rb, spec)
+    kc0, vc0 = tens.k_cache.clone(), tens.v_cache.clone()
     rb.run_step_fused(buf)
     torch.cuda.synchronize()
     assert int(buf.meta["scalars"][3].item()) == 0
@@ -92,11 +108,14 @@ def test_fused_step_vs_oracle(rb, name):
     for k in ("input_ids", "positions", "query_start_loc", "seq_lens", "slot_mapping",
               "logits_indices"):
         assert np.array_equal(buf.meta[k].cpu().numpy(), want[k]), k
-    ref = oracle_attention(spec, tens, want)
-    compare_attention(buf.attn_out, ref, spec.num_tokens)
-    hid = tens.hidden.float().cpu().numpy()
-    rows = oracle.gather_rows(hid, want["logits_indices"])
-    assert np.array_equal(buf.rows_out.float().cpu().numpy(), rows)
+    assert buf.meta["scalars"][:3].tolist() == [want["max_query_len"], want["max_seq_len"],
+                                                want["num_actual_tokens"]]
+    check_kv_write(spec, kc0, vc0, tens, want["slot_mapping"])
+    rows = None if n_random is None else sample_rows(spec, n_random=n_random, seed=5)
+    ref = oracle_attention(spec, tens, want, rows=rows)
+    compare_attention(buf.attn_out, ref, spec.num_tokens, rows=rows)
+    li = torch.as_tensor(want["logits_indices"], device="cuda")
+    assert torch.equal(buf.rows_out, tens.hidden[li])
 
 
 def test_fused_step_error_bits(rb):
