@@ -1,26 +1,46 @@
 #!/usr/bin/env python
-"""Throughput of one flattened mixed-batch step on GB300 (prepare_inputs -> kv_write ->
-paged_attention -> gather_rows, one attention layer, synthetic bf16 activations).
+"""Throughput of the flattened mixed-batch step on GB300, one attention layer, synthetic data.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config C]
 
-Prints ONE JSON line on rank 0.  The headline workload is the pages' padding example
-(query lens [2000, 512, 1 x 6]; 32 q / 8 kv heads, head_dim 128, block 16, hidden 4096).
-``--config`` selects another workload for local study (1 worked example, 3 pure decode,
-4 chunked-prefill mix step 0, 5 long context); those lines are not the headline.
+Prints ONE JSON line on rank 0.
 
-Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events on the launching
-stream with a 512 MiB write between steps (outside the events) so every step starts with a
-cold L2; barrier + synchronize around the whole region; max over ranks.  Under torchrun every
-rank runs its own independent batch (data parallel, no collective on the data path).
+Headline workload (``--config 4``, the default): the chunked-prefill mix as a seeded request
+stream with an 8192-token budget -- 4 chunked prefills of U[1024, 2048] tokens on U[0, 16384]
+cached tokens and 128 decodes on U[256, 32768] cached tokens, 32 q / 8 kv heads, head_dim 128,
+pages of 16 tokens, requests finishing, arriving, being preempted and having their page rows
+replaced -- over max(100, W + K) scheduler steps.  One step is the whole hot path on the
+device: ``rb_batch_apply_update`` (the scheduler's deltas merged into the device-resident
+persistent batch, its packet staged in device memory before the timed region) and one
+``rb_step`` (metadata, KV write, paged attention, last-token row gather).  Steps 0..W-1 warm
+up; steps W..W+K-1 are timed; the rest of the stream runs after the timed region and is
+reported as ``stream_all``.  ``value`` = real tokens of the timed steps / their device time.
+
+In the same line, ``configs`` carries the other single-GPU workloads, each timed as a captured
+``rb_step`` graph replayed with a cold L2 (median of its steps): ``2`` the pages' padding
+example, ``3`` pure decode (256 x U[512, 8192]), ``5`` long context (8 decodes at 131072 plus a
+4096-token chunk on 65536, 64 q heads); each with the roofline of its dominant kernel.
+``--config 2|3|5`` makes one of them the headline instead.
+
+Timing: CUDA events on the launching stream around each step, a 512 MiB write between steps
+(outside the events) so every step starts with a cold L2, barrier + synchronize around the
+whole region, max over ranks.  Under torchrun every rank runs its own independent stream
+(data parallel: no collective on the data path).  ``e2e``: the same steps through the public
+API with host buffers (the scheduler packet and q / k / v / hidden copied in from pinned host
+memory, the attention output, gathered rows and scalars copied back, every step synchronised),
+wall clock.  ``cpu_baseline``: the CPU oracle (float64) on a bounded row sample of the same
+workload, on all host cores (one request per thread).  ``--impl reference`` times that oracle
+alone on the headline workload.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
 import os
+import platform
 import statistics
 import subprocess
 import sys
@@ -33,54 +53,25 @@ if ROOT not in sys.path:
 METRIC = "mixed-step tokens/s; decode-attn HBM GB/s & prefill TFLOPS vs peak"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+STREAM_STEPS = 100
+HIDDEN = 4096
+FLUSH_BYTES = 512 << 20
 
-# DRAM bytes (read + write) per launch measured by ncu (dram__bytes_read.sum +
-# dram__bytes_write.sum), keyed by (kernel, workload, hash of the kernel's sources): a figure is
-# reported only while the kernel's sources are the ones it was measured on (profiles/).
+# DRAM bytes (read + write) per launch of the fused attention kernel measured by ncu
+# (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (workload, hash of the kernel's
+# sources): a figure is reported only while the sources are the ones it was measured on.
 KNOWN_TRAFFIC = {
-    ("fused", 2, "3b1b6221124298e8"): 79013632 + 4368640,
-    ("fused", 3, "3b1b6221124298e8"): 4546843904 + 26761472,
-    ("fused", 4, "3b1b6221124298e8"): 10085929472 + 99310336,
+    (2, "3b1b6221124298e8"): 79013632 + 4368640,
+    (3, "3b1b6221124298e8"): 4546843904 + 26761472,
 }
+
+WORKLOAD_NAMES = {1: "pages' worked example A/B/C", 2: "pages' padding example",
+                  3: "pure decode x256", 4: "chunked-prefill mix stream (8192-token budget)",
+                  5: "long-context 70B-like step"}
 
 
 # ----------------------------------------------------------------------------- workloads
-def chunked_mix_step0(rank: int, oracle_layout: bool = False):
-    """Step 0 of the chunked-prefill request stream, laid out into batch rows by the library's
-    own device-side batch update (the oracle's InputBatch on the reference leg)."""
-    import workloads as wl
-
-    stream = wl.MixedChunkStream(seed=4000 + 7919 * rank)
-    step, d = stream.next_step(), stream.dims
-    if oracle_layout:
-        from oracle.persistent_batch import InputBatch
-
-        batch = InputBatch(d.max_num_reqs, d.max_model_len, d.max_blocks_per_req)
-        batch.apply(step)
-        cols = batch.columns(step.scheduled)
-        tok, blk = batch.tables()
-        computed, sched, prompt = cols["num_computed"], cols["num_scheduled"], cols["num_prompt"]
-    else:
-        import torch
-
-        import ragged_mixed_paged_gb300 as rb
-
-        batch = rb.PersistentBatch(d.max_num_reqs, d.max_model_len, d.max_blocks_per_req)
-        batch.apply(step)
-        torch.cuda.synchronize()
-        if int(batch.error_word.item()) != 0:
-            raise SystemExit(f"batch update error word {int(batch.error_word.item()):#x}")
-        R = batch.num_reqs
-        computed = batch.num_computed[:R].cpu().numpy()
-        sched = batch.num_scheduled[:R].cpu().numpy()
-        prompt = batch.num_prompt[:R].cpu().numpy()
-        tok, blk = batch.token_table.cpu().numpy(), batch.block_table.cpu().numpy()
-        del batch
-    return wl.spec_from_columns("chunked-prefill mix step 0", d, computed, sched, prompt, tok, blk,
-                                seed=(4000 + 7919 * rank) * 1000)
-
-
-def make_spec(config: int, rank: int = 0, oracle_layout: bool = False, manager_ratio: int = 1):
+def make_spec(config: int, rank: int = 0, manager_ratio: int = 1):
     import workloads as wl
 
     if config == 1:
@@ -89,20 +80,63 @@ def make_spec(config: int, rank: int = 0, oracle_layout: bool = False, manager_r
         return wl.config2(step=rank, manager_ratio=manager_ratio)
     if config == 3:
         return wl.config3(step=rank, manager_ratio=manager_ratio)
-    if config == 4:
-        return chunked_mix_step0(rank, oracle_layout)
     if config == 5:
         return wl.config5(step=rank)
-    raise SystemExit(f"unknown config {config}")
+    raise SystemExit(f"config {config} is not a single fixed batch")
 
 
-def workload_name(spec, config):
+def stream_seed(rank: int) -> int:
+    return 4000 + 7919 * rank
+
+
+def stream_steps(rank: int, n: int):
+    """The first n scheduler outputs of this rank's chunked-prefill request stream."""
+    import workloads as wl
+
+    stream = wl.MixedChunkStream(seed=stream_seed(rank))
+    return stream, [stream.next_step() for _ in range(n)]
+
+
+def step_cq(step):
+    """(cached, scheduled) token counts of every request of a scheduler step, in schedule
+    order (the counts the scheduler hands the runner)."""
+    computed = {n.req_id: int(n.num_computed) for n in step.new}
+    computed.update({c.req_id: int(c.num_computed) for c in step.cached})
+    return [(computed[i], int(q)) for i, q in step.scheduled.items()]
+
+
+def work_of(cq, nh, nkv, hd, block_size, N, Np, R, Rp, hidden):
+    """Algorithmic work of a step (what the pages define, not what the kernels do)."""
+    g = nh // nkv
+    dec_bytes = pre_flops = dec_flops = 0
+    for c, q in cq:
+        visible = q * c + q * (q + 1) // 2                 # sum over j of (c + j + 1)
+        flops = 4 * nh * hd * visible
+        if q * g <= 8:  # decode-like: bound by reading the request's K/V once per kv head
+            L = c + q
+            dec_bytes += L * 2 * nkv * hd * 2 + 2 * q * nh * hd * 2 + -(-L // block_size) * 4
+            dec_flops += flops
+        else:
+            pre_flops += flops
+    row = nkv * hd * 2
+    return dict(prefill_flops=pre_flops, decode_flops=dec_flops, decode_bytes=dec_bytes,
+                kv_write_bytes=2 * 2 * Np * row,
+                meta_bytes=Np * (4 + 4 + 3 * 4) + R * (2 * 4 + 3 * 4),
+                gather_bytes=2 * Rp * hidden * 2)
+
+
+def spec_work(spec):
+    d = spec.dims
+    cq = list(zip(spec.num_computed.tolist(), spec.num_scheduled.tolist()))
+    return work_of(cq, d.num_q_heads, d.num_kv_heads, d.head_dim, d.block_size, spec.num_tokens,
+                   spec.num_tokens_padded, spec.num_reqs, spec.num_reqs_padded, spec.hidden_size)
+
+
+def fixed_config_desc(spec, config):
     d = spec.dims
     return {
-        "workload": {1: "pages' worked example A/B/C", 2: "pages' padding example",
-                     3: "pure decode x256", 4: "chunked-prefill mix (step 0)",
-                     5: "long-context 70B-like"}[config],
-        "query_lens": (spec.num_scheduled.tolist() if spec.num_reqs <= 8
+        "workload": WORKLOAD_NAMES[config],
+        "query_lens": (spec.num_scheduled.tolist() if spec.num_reqs <= 9
                        else f"{spec.num_reqs} requests"),
         "num_reqs": spec.num_reqs, "num_tokens": spec.num_tokens,
         "num_tokens_padded": spec.num_tokens_padded, "q_heads": d.num_q_heads,
@@ -113,29 +147,20 @@ def workload_name(spec, config):
     }
 
 
-def work_counts(spec):
-    """Algorithmic work of the step (what the pages define, not what the kernels do)."""
-    d = spec.dims
-    g = d.num_q_heads // d.num_kv_heads
-    dec_bytes = pre_flops = dec_flops = 0
-    for c, q in zip(spec.num_computed.tolist(), spec.num_scheduled.tolist()):
-        visible = q * c + q * (q + 1) // 2                 # sum over j of (c + j + 1)
-        flops = 4 * d.num_q_heads * d.head_dim * visible
-        if q * g <= 8:  # decode-like: bound by reading the request's K/V once per kv head
-            L = c + q
-            dec_bytes += L * 2 * d.num_kv_heads * d.head_dim * 2 \
-                + 2 * q * d.num_q_heads * d.head_dim * 2 + -(-L // d.block_size) * 4
-            dec_flops += flops
-        else:
-            pre_flops += flops
-    N, Np, R = spec.num_tokens, spec.num_tokens_padded, spec.num_reqs
-    row = d.num_kv_heads * d.head_dim * 2
-    return dict(
-        attn_flops=pre_flops + dec_flops, prefill_flops=pre_flops, decode_flops=dec_flops,
-        decode_bytes=dec_bytes,
-        kv_write_bytes=2 * 2 * Np * row,                       # K and V, read + write
-        meta_bytes=Np * (4 + 4 + 3 * 4) + R * (2 * 4 + 3 * 4),
-        gather_bytes=2 * spec.num_reqs_padded * spec.hidden_size * 2)
+def stream_config_desc(dims, warmup, steps, total):
+    return {
+        "workload": WORKLOAD_NAMES[4],
+        "stream": f"{total} seeded scheduler steps (seed {stream_seed(0)} + 7919 x rank); "
+                  f"steps {warmup}..{warmup + steps - 1} timed",
+        "mix": "4 chunks U[1024, 2048] on U[0, 16384] cached + 128 decodes on U[256, 32768] "
+               "cached, budget 8192 tokens; 5% finish / 1% preempt / 1% page-row replace "
+               "per step",
+        "q_heads": dims.num_q_heads, "kv_heads": dims.num_kv_heads, "head_dim": dims.head_dim,
+        "block_size": dims.block_size, "hidden": HIDDEN, "kv_pages": dims.num_blocks,
+        "max_num_reqs": dims.max_num_reqs, "max_model_len": dims.max_model_len,
+        "step": "rb_batch_apply_update (packet pre-staged in HBM) + rb_step, eager",
+        "l2": "flushed before every timed step (512 MiB write, outside the events)",
+    }
 
 
 def peaks():
@@ -146,22 +171,45 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-KERNEL_SOURCES = {
-    "fused": ("attn_prefill_tc.cu", "attn_decode_warp.cuh", "tc_ptx.cuh", "attn_common.cuh",
-              "rb_internal.cuh"),
-    "prefill": ("attn_prefill.cu", "attn_common.cuh", "rb_internal.cuh"),
-    "decode": ("attn_decode.cu", "attn_decode_warp.cuh", "attn_common.cuh", "rb_internal.cuh"),
-}
+FUSED_SOURCES = ("attn_prefill_tc.cu", "attn_decode_warp.cuh", "tc_ptx.cuh", "attn_common.cuh",
+                 "rb_internal.cuh")
 
 
-def kernel_sources_hash(kind):
-    """Hash of the sources a kernel is built from (traffic figures are valid for one hash)."""
+def kernel_sources_hash():
+    """Hash of the sources the fused attention kernel is built from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ragged_mixed_paged_gb300", "csrc")
-    for f in KERNEL_SOURCES[kind]:
+    for f in FUSED_SOURCES:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
+
+
+def roofline(work, launch_s, config, launches=1):
+    """Roofline of the fused attention launch: the dominant resource's algorithmic work (prefill
+    FLOPs or decode bytes, whichever takes longer at peak) over the measured launch time."""
+    pk, pk_kind = peaks()
+    t_tensor = work["prefill_flops"] / (pk["bf16_tflops"] * 1e12)
+    t_hbm = work["decode_bytes"] / (pk["hbm_gbs"] * 1e9)
+    tensor_bound = t_tensor >= t_hbm
+    tflops = work["prefill_flops"] / launch_s / 1e12
+    gbs = work["decode_bytes"] / launch_s / 1e9
+    achieved = tflops if tensor_bound else gbs
+    peak = pk["bf16_tflops"] if tensor_bound else pk["hbm_gbs"]
+    traffic = KNOWN_TRAFFIC.get((config, kernel_sources_hash()))
+    return {"bound": "tensor" if tensor_bound else "hbm", "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s" if tensor_bound else "GB/s", "frac": achieved / peak,
+            "traffic": traffic,
+            "kernel": "attn_prefill_tc_kernel (fused launch: split-KV decode units + tcgen05 "
+                      "prefill units)",
+            "launch_ms": launch_s * 1000.0 / launches,
+            "tensor_frac": tflops / pk["bf16_tflops"],
+            "tensor_frac_sustained": tflops / pk["bf16_tflops_sustained"],
+            "hbm_frac": gbs / pk["hbm_gbs"],
+            "overlap_frac": max(t_tensor, t_hbm) / launch_s,
+            "peak_kind": f"{'bf16 dense burst' if tensor_bound else 'HBM copy'}, {pk_kind}",
+            "work_per_launch": {"prefill_gflop": work["prefill_flops"] / 1e9 / launches,
+                                "decode_kv_gb": work["decode_bytes"] / 1e9 / launches}}
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -255,449 +303,568 @@ def barrier(world: int):
         dist.barrier()
 
 
-# ----------------------------------------------------------------------------- oracle arm
-def oracle_step_sample(spec, tens, rows):
-    """The CPU oracle on a row sample of the step: metadata, KV write, attention for `rows`,
-    gather.  Returns seconds."""
+# ----------------------------------------------------------------------------- oracle (CPU)
+def host_cpu():
+    """CPU model and the cores this process may use."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if model is None:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith(("model name", "cpu part")):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    return {"model": model or platform.processor() or platform.machine(),
+            "arch": platform.machine(), "host_cores": len(os.sched_getaffinity(0))}
+
+
+class OracleStream:
+    """The oracle's side of the chunked-prefill stream on the host: its persistent batch, one
+    layer's K/V pool (bf16 bit patterns, lazily zero), and random float32 activations and
+    histories (a request's history is a prefix of one shared random array: the oracle reads
+    histories, never the pool, and any values will do)."""
+
+    def __init__(self, rank):
+        import numpy as np
+
+        from oracle.persistent_batch import InputBatch
+
+        self.stream, _ = stream_steps(rank, 0)
+        d = self.dims = self.stream.dims
+        self.batch = InputBatch(d.max_num_reqs, d.max_model_len, d.max_blocks_per_req)
+        self.k_pool = np.zeros((d.num_slots, d.num_kv_heads, d.head_dim), np.int16)
+        self.v_pool = np.zeros_like(self.k_pool)
+        rng = np.random.default_rng(stream_seed(rank) + 99)
+        shape = (d.max_model_len, d.num_kv_heads, d.head_dim)
+        self.hist_k = rng.standard_normal(shape, np.float32)
+        self.hist_v = rng.standard_normal(shape, np.float32)
+        n = self.stream.BUDGET
+        self.q = rng.standard_normal((n, d.num_q_heads, d.head_dim)).astype(np.float64)
+        self.k = rng.standard_normal((n, d.num_kv_heads, d.head_dim)).astype(np.float64)
+        self.v = rng.standard_normal((n, d.num_kv_heads, d.head_dim)).astype(np.float64)
+        bits = lambda a: (a.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        self.k16, self.v16 = bits(self.k).view(np.int16), bits(self.v).view(np.int16)
+        self.hidden = np.zeros((n, HIDDEN), np.int16)
+
+    def advance(self):
+        """The next scheduler step (not yet merged into the oracle's batch)."""
+        return self.stream.next_step()
+
+    def timed_step(self, step, row_stride, offset):
+        """The oracle's whole step: the batch merge, metadata for every token, the KV write,
+        attention for every ``row_stride``-th query row (all heads), the row gather.  Returns
+        (seconds, rows evaluated, process CPU seconds)."""
+        import numpy as np
+
+        import oracle
+        from oracle.threads import oracle_attention_threads
+
+        d = self.dims
+        N = step.num_tokens
+        rows = list(range(offset % row_stride, N, row_stride))
+        c0, w0 = time.process_time(), time.perf_counter()
+        self.batch.apply(step)
+        cols = self.batch.columns(step.scheduled)
+        tok, blk = self.batch.tables()
+        meta = oracle.prepare_inputs(block_size=d.block_size, null_block=d.null_block,
+                                     token_table=tok, block_table=blk,
+                                     num_computed=cols["num_computed"],
+                                     num_scheduled=cols["num_scheduled"],
+                                     num_prompt=cols["num_prompt"])
+        oracle.kv_write(self.k_pool, self.v_pool, meta["slot_mapping"], self.k16[:N],
+                        self.v16[:N])
+        c = cols["num_computed"].tolist()
+        a0 = time.perf_counter()
+        oracle_attention_threads(self.q[:N], [self.hist_k[:x] for x in c],
+                                 [self.hist_v[:x] for x in c], self.k[:N], self.v[:N],
+                                 meta["query_start_loc"], meta["seq_lens"], len(c), rows)
+        attn = time.perf_counter() - a0
+        oracle.gather_rows(self.hidden[:N], meta["logits_indices"])
+        wall = time.perf_counter() - w0
+        return {"wall": wall, "attn": attn, "rows": len(rows), "cpu": time.process_time() - c0}
+
+
+def oracle_stream_run(rank, warmup, steps, budget_s):
+    """The oracle over the stream: W warm-up steps (the last one a full step with a small row
+    sample, the others only merged into the batch), then K timed steps whose row sample is
+    sized so they take about ``budget_s`` together (the probe step's attention time per row
+    and its time outside attention)."""
+    os_ = OracleStream(rank)
+    probe = None
+    for w in range(warmup):
+        step = os_.advance()
+        if w < warmup - 1:
+            os_.batch.apply(step)
+            continue
+        probe = os_.timed_step(step, 64, w)
+    per_row = probe["attn"] / max(probe["rows"], 1) if probe else 0.1
+    fixed = probe["wall"] - probe["attn"] if probe else 5.0
+    rows_budget = max(1.0, (budget_s / max(steps, 1) - fixed) / max(per_row, 1e-6))
+    stride = max(1, math.ceil(6000 / rows_budget))
+    times, rows, cpu = [], 0, 0.0
+    for k in range(steps):
+        step = os_.advance()
+        r = os_.timed_step(step, stride, k)
+        times.append(r["wall"])
+        rows += r["rows"]
+        cpu += r["cpu"]
+    total = sum(times)
+    return {"value": rows / total, "wall_s": total, "rows": rows, "stride": stride,
+            "cores": round(cpu / max(total, 1e-9), 1), "times": times}
+
+
+def fixed_oracle_run(spec, target_s):
+    """The oracle on one fixed batch: full metadata, KV write and gather, attention for a row
+    sample sized to about ``target_s``.  Returns (rows/s, rows, stride, cores, seconds)."""
     import numpy as np
     import torch
 
     import oracle
-
-    d = spec.dims
-    f64 = lambda t: t.float().numpy().astype(np.float64)
-    u16 = lambda t: t.view(torch.int16).numpy()
-    t0 = time.perf_counter()
-    meta = oracle.prepare_inputs(block_size=d.block_size, null_block=d.null_block,
-                                 token_table=spec.token_table, block_table=spec.block_table,
-                                 num_computed=spec.num_computed,
-                                 num_scheduled=spec.num_scheduled,
-                                 num_reqs_padded=spec.num_reqs_padded,
-                                 num_tokens_padded=spec.num_tokens_padded)
-    oracle.kv_write(u16(tens.k_cache), u16(tens.v_cache), meta["slot_mapping"], u16(tens.k),
-                    u16(tens.v))
-    oracle.paged_attention(f64(tens.q), [f64(h) for h in tens.hist_k],
-                           [f64(h) for h in tens.hist_v], f64(tens.k), f64(tens.v),
-                           meta["query_start_loc"], meta["seq_lens"], spec.num_reqs, rows=rows)
-    oracle.gather_rows(u16(tens.hidden), meta["logits_indices"])
-    return time.perf_counter() - t0
-
-
-def row_sample(spec, stride, offset=0):
-    return list(range(offset % stride, spec.num_tokens, stride))
-
-
-def cpu_baseline(spec, target_s=12.0):
-    """Oracle timed on this host's cores on a bounded row sample of the same workload."""
     import workloads as wl
+    from oracle.threads import oracle_attention_threads
 
     tens = wl.make_tensors(spec, device="cpu")
-    probe = max(1, spec.num_tokens // 40)
-    t = oracle_step_sample(spec, tens, row_sample(spec, probe))
-    per_row = t / len(row_sample(spec, probe))
-    stride = max(1, math.ceil(spec.num_tokens * per_row / target_s))
-    rows = row_sample(spec, stride)
-    c0, w0 = time.process_time(), time.perf_counter()
-    t = oracle_step_sample(spec, tens, rows)
-    cores = (time.process_time() - c0) / max(time.perf_counter() - w0, 1e-9)
-    return {"value": len(rows) / t, "unit": UNIT, "cores": round(cores, 1),
-            "host_cores": len(os.sched_getaffinity(0)), "kind": "oracle",
-            "sample": f"every {stride}th of {spec.num_tokens} query rows (all heads) with the "
-                      f"full metadata, KV write and gather; {t:.1f} s"}
+    d = spec.dims
+    f64 = lambda t: t.to(torch.float64).numpy()
+    u16 = lambda t: t.view(torch.int16).numpy()
+    q64, k64, v64 = f64(tens.q), f64(tens.k), f64(tens.v)
+    hk = [f64(h) for h in tens.hist_k]
+    hv = [f64(h) for h in tens.hist_v]
+
+    def run(rows):
+        c0, w0 = time.process_time(), time.perf_counter()
+        meta = oracle.prepare_inputs(block_size=d.block_size, null_block=d.null_block,
+                                     token_table=spec.token_table, block_table=spec.block_table,
+                                     num_computed=spec.num_computed,
+                                     num_scheduled=spec.num_scheduled,
+                                     num_reqs_padded=spec.num_reqs_padded,
+                                     num_tokens_padded=spec.num_tokens_padded)
+        oracle.kv_write(u16(tens.k_cache), u16(tens.v_cache), meta["slot_mapping"], u16(tens.k),
+                        u16(tens.v))
+        R = spec.num_reqs
+        oracle_attention_threads(q64, hk, hv, k64, v64, meta["query_start_loc"][:R + 1],
+                                 meta["seq_lens"][:R], R, rows)
+        oracle.gather_rows(u16(tens.hidden), meta["logits_indices"])
+        return time.perf_counter() - w0, time.process_time() - c0
+
+    N = spec.num_tokens
+    probe = list(range(0, N, max(1, N // 48)))
+    t, _ = run(probe)
+    stride = max(1, math.ceil(N * t / len(probe) / target_s))
+    rows = list(range(0, N, stride))
+    t, c = run(rows)
+    return len(rows) / t, len(rows), stride, round(c / max(t, 1e-9), 1), t
 
 
 def run_reference(args, rank, world):
+    """--impl reference: the CPU oracle (float64) on the headline workload, on this host's
+    cores; rank 0 only."""
     if rank != 0:
         return
-    spec = make_spec(args.config, oracle_layout=True)
-    import workloads as wl
+    cpu = host_cpu()
+    budget = 150.0
+    if args.config == 4:
+        r = oracle_stream_run(rank, args.warmup, args.steps, budget)
+        import workloads as wl
 
-    tens = wl.make_tensors(spec, device="cpu")
-    budget = 150.0 / max(1, args.steps + args.warmup)      # seconds per step
-    probe = max(1, spec.num_tokens // 40)
-    t = oracle_step_sample(spec, tens, row_sample(spec, probe))
-    per_row = t / len(row_sample(spec, probe))
-    stride = max(1, math.ceil(spec.num_tokens * per_row / budget))
-    for w in range(max(0, args.warmup - 1)):
-        oracle_step_sample(spec, tens, row_sample(spec, stride, w))
-    times, nrows = [], 0
-    c0, w0 = time.process_time(), time.perf_counter()
-    for k in range(args.steps):
-        rows = row_sample(spec, stride, k)
-        times.append(oracle_step_sample(spec, tens, rows))
-        nrows += len(rows)
-    cores = (time.process_time() - c0) / max(time.perf_counter() - w0, 1e-9)
-    total = sum(times)
-    value = nrows / total
-    sample = (f"each step: the oracle's metadata, KV write and gather in full plus attention "
-              f"for every {stride}th query row (all heads), rotating the offset per step")
+        value, total = r["value"], r["wall_s"]
+        config = stream_config_desc(wl.MixedChunkStream().dims, args.warmup, args.steps,
+                                    args.warmup + args.steps)
+        sample = (f"each step: the oracle's batch merge, metadata for every token, KV write and "
+                  f"row gather in full, attention (all heads) for every {r['stride']}th query "
+                  f"row, one request per thread; {r['rows']} rows over {args.steps} steps")
+        cores = r["cores"]
+    else:
+        spec = make_spec(args.config)
+        per = budget / max(1, args.steps + args.warmup)
+        value, nrows, stride, cores, t = fixed_oracle_run(spec, per)
+        total = t * args.steps
+        config = fixed_config_desc(spec, args.config)
+        sample = f"every {stride}th of {spec.num_tokens} query rows per step"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000 * total / max(1, args.steps), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_name(spec, args.config),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": round(cores, 1),
-                             "kind": "oracle", "sample": sample},
+            "config": config,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample, **cpu},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+def cpu_baseline(config, rank):
+    """The oracle on this host's cores, on a bounded sample of the headline workload."""
+    cpu = host_cpu()
+    if config == 4:
+        r = oracle_stream_run(rank, 1, 1, 20.0)
+        return {"value": r["value"], "unit": UNIT, "cores": r["cores"], "kind": "oracle",
+                "sample": (f"stream step 1 (after a probe of step 0): the oracle's batch "
+                           f"merge, metadata, KV write (a copy of the whole pool) and gather in "
+                           f"full, attention for every {r['stride']}th query row (all heads), "
+                           f"one request per thread; {r['rows']} rows in "
+                           f"{r['wall_s']:.1f} s"), **cpu}
+    spec = make_spec(config, rank)
+    value, nrows, stride, cores, t = fixed_oracle_run(spec, 12.0)
+    return {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"every {stride}th of {spec.num_tokens} query rows with the full "
+                      f"metadata, KV write and gather; {t:.1f} s", **cpu}
+
+
 # ----------------------------------------------------------------------------- our arm
-def run_ours(args, rank, world, local):
+def _events(n):
     import torch
 
-    import workloads as wl
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+def _recorded_events(n):
+    """Events the library re-records (rb_step_profiled): torch creates the handle lazily."""
+    import torch
+
+    ev = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(n)]
+    for e in ev:
+        e.record()
+    return ev
+
+
+def measure_stream(args, rank, world, local):
+    """The headline: the chunked-prefill stream, each step rb_batch_apply_update + rb_step."""
+    import torch
+
     import ragged_mixed_paged_gb300 as rb
 
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device for --impl ours")
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream()
-    spec = make_spec(args.config, rank, manager_ratio=args.manager_ratio)
-    d = spec.dims
-    tens = wl.make_tensors(spec, device=dev)
-    tables = wl.device_tables(spec, dev)
-    buf = rb.StepBuffers.allocate(rb.Dims.of(d), spec.num_reqs, spec.num_reqs_padded,
-                                  spec.num_tokens, spec.num_tokens_padded, tables, tens.q,
-                                  tens.k, tens.v, tens.hidden, tens.k_cache, tens.v_cache)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    E = lambda: torch.cuda.Event(enable_timing=True)
+    total = max(STREAM_STEPS, args.warmup + args.steps)
+    stream, steps = stream_steps(rank, total)
+    d = stream.dims
+    dims = rb.Dims.of(d)
+    nmax, rmax = stream.BUDGET, d.max_num_reqs
+    g = torch.Generator(device=dev).manual_seed(stream_seed(rank))
+    bf = torch.bfloat16
 
-    # the product's step is one rb_step call (one memset, two launches); --four-calls times the
-    # four separate entry points instead
-    step_fn = rb.run_step if args.four_calls else rb.run_step_fused
-    for _ in range(args.warmup):
+    def rnd(*shape):
+        return torch.randn(*shape, generator=g, device=dev, dtype=torch.float32).to(bf)
+
+    q, k, v = rnd(nmax, d.num_q_heads, d.head_dim), rnd(nmax, d.num_kv_heads, d.head_dim), \
+        rnd(nmax, d.num_kv_heads, d.head_dim)
+    hidden = rnd(nmax, HIDDEN)
+    k_cache = torch.empty((d.num_slots, d.num_kv_heads, d.head_dim), dtype=bf,
+                          device=dev).normal_(generator=g)
+    v_cache = torch.empty_like(k_cache).normal_(generator=g)
+    batch = rb.PersistentBatch(d.max_num_reqs, d.max_model_len, d.max_blocks_per_req, device=dev)
+    staged = [batch.stage(s) for s in steps]             # every step's packet in HBM
+    buf = rb.StepBuffers.allocate(dims, rmax, rmax, nmax, nmax, batch.tables(), q, k, v, hidden,
+                                  k_cache, v_cache)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    cq = [step_cq(s) for s in steps]
+    works = [work_of(x, d.num_q_heads, d.num_kv_heads, d.head_dim, d.block_size,
+                     sum(qq for _, qq in x), sum(qq for _, qq in x), len(x), len(x), HIDDEN)
+             for x in cq]
+    tokens = [s.num_tokens for s in steps]
+    # per step: start | after the update | after the preparation launch | after attention
+    marks = [(_events(2), _recorded_events(2)) for _ in steps]
+
+    def run(i):
+        st = staged[i]
+        R, N = st.num_scheduled, st.num_tokens
+        b = dataclasses.replace(buf, num_reqs=R, num_reqs_padded=R, num_tokens=N,
+                                num_tokens_padded=N, q=q[:N], k=k[:N], v=v[:N],
+                                hidden=hidden[:N], attn_out=buf.attn_out[:N],
+                                rows_out=buf.rows_out[:R])
+        (a, u), inner = marks[i]
         flush.zero_()
-        step_fn(buf)
-        rb.run_step(buf)
-    torch.cuda.synchronize()
-    if int(buf.meta["scalars"][3].item()) != 0:
-        raise SystemExit(f"device error word {int(buf.meta['scalars'][3].item()):#x}")
+        a.record()
+        batch.apply_staged(st)
+        u.record()
+        rb.run_step_fused(b, events=inner)
 
-    # events recorded inside the step: 5 around the four calls, 3 inside the attention call
-    EX = lambda: torch.cuda.Event(enable_timing=True, external=True)
-    marks, attn_marks = [EX() for _ in range(5)], [EX() for _ in range(3)]
-    for ev in marks + attn_marks:
-        ev.record()  # torch creates the handle lazily; the library re-records it in the step
     torch.cuda.synchronize()
-    graph = graph_marked = None
-    launches_per_step = None
-    if not args.eager:
-        # the step has only scalar host inputs and fixed-address buffers: capture it once and
-        # replay it, as a serving loop would, so host launch latency does not enter the step.
-        # The timed graph holds the library's launches only: an event-record node inside a
-        # graph costs ~3.5 us, so the per-call and per-kernel events live in a second graph of
-        # the same step, replayed after the timed region
-        launches0 = rb.launch_count()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            step_fn(buf)
-        launches_per_step = rb.launch_count() - launches0
-        graph_marked = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph_marked):
-            rb.run_step(buf, marks=marks, attn_marks=attn_marks)
-        graph.replay()
-        graph_marked.replay()
-        torch.cuda.synchronize()
-    E = lambda: torch.cuda.Event(enable_timing=True)
-    step_events = [(E(), E()) for _ in range(args.steps)]
-    samples = []  # per step of the breakdown pass: the 8 event timestamps
+    for i in range(args.warmup):
+        run(i)
+    torch.cuda.synchronize()
     sampler = ClockSampler(local)
     barrier(world)
     torch.cuda.synchronize()
     sampler.start()
     launches0 = rb.launch_count()
     w0 = time.perf_counter()
-    for k in range(args.steps):
-        flush.zero_()
-        a, b = step_events[k]
-        a.record()
-        if graph is not None:
-            graph.replay()
-        elif args.four_calls:
-            rb.run_step(buf, marks=marks, attn_marks=attn_marks)
-        else:
-            step_fn(buf)
-        b.record()
-        torch.cuda.synchronize()
-        if graph is None and args.four_calls:
-            pts = [marks[0], marks[1], marks[2], attn_marks[0], attn_marks[1], attn_marks[2],
-                   marks[3], marks[4]]
-            samples.append([pts[0].elapsed_time(p) for p in pts])
+    timed = range(args.warmup, args.warmup + args.steps)
+    for i in timed:
+        run(i)
     torch.cuda.synchronize()
     barrier(world)
     wall = time.perf_counter() - w0
-    launches = (launches_per_step * args.steps if graph is not None
-                else rb.launch_count() - launches0)
-    step_times = [a.elapsed_time(b) for a, b in step_events]
-    if not samples:  # breakdown pass: the same steps, four calls with events between launches
-        for k in range(args.steps):
-            flush.zero_()
-            if graph_marked is not None:
-                graph_marked.replay()
-            else:
-                rb.run_step(buf, marks=marks, attn_marks=attn_marks)
-            torch.cuda.synchronize()
-            pts = [marks[0], marks[1], marks[2], attn_marks[0], attn_marks[1], attn_marks[2],
-                   marks[3], marks[4]]
-            samples.append([pts[0].elapsed_time(p) for p in pts])
+    launches = rb.launch_count() - launches0
     clocks = sampler.stop()
+    for i in range(args.warmup + args.steps, total):  # the rest of the stream
+        run(i)
+    torch.cuda.synchronize()
+    err = int(buf.meta["scalars"][3].item()) | int(batch.error_word.item())
+    if err:
+        raise SystemExit(f"device error word {err:#x}")
 
-    # timestamps: 0 start | 1 after prepare | 2 after kv_write | 3 after plan | 4 after decode |
-    # 5 after prefill | 6 after attention | 7 after gather
-    def span(a, b):
-        idx = {0: 0, 1: 1, 2: 2, 3: 6, 4: 7}
-        return [s[idx[b]] - s[idx[a]] for s in samples]
+    def spans(i):
+        (a, u), (p, z) = marks[i]
+        return a.elapsed_time(u), u.elapsed_time(p), p.elapsed_time(z), a.elapsed_time(z)
 
-    def kspan(a, b):  # inside the attention call: planner | decode kernel | prefill kernel
-        return [s[2 + b] - s[2 + a] for s in samples]
+    sp = [spans(i) for i in range(total)]
+    step_ms = [x[3] for x in sp]
+    t_timed = sum(step_ms[i] for i in timed)
+    tok_timed = sum(tokens[i] for i in timed)
+    t_max = reduce_over_ranks(t_timed, "max", world, dev)
+    tok_sum = reduce_over_ranks(float(tok_timed), "sum", world, dev)
+    value = tok_sum / (t_max / 1000.0)
 
-    step_ms = statistics.mean(step_times)
-    marked_step_ms = statistics.mean(span(0, 4))
-    parts = {"prepare_inputs": span(0, 1), "kv_write": span(1, 2),
-             "paged_attention": span(2, 3), "gather_rows": span(3, 4)}
-    parts_ms = {k: statistics.mean(v) for k, v in parts.items()}
-    kernels_ms = {"attn_plan": statistics.mean(kspan(0, 1)),
-                  "attn_decode": statistics.mean(kspan(1, 2)),
-                  "attn_prefill": statistics.mean(kspan(2, 3))}
-    step_ms_max = reduce_over_ranks(step_ms, "max", world, dev)
-    total_tokens = reduce_over_ranks(float(spec.num_tokens), "sum", world, dev)
-    value = total_tokens / (step_ms_max / 1000.0)
+    def agg(idx):
+        w = {k2: sum(works[i][k2] for i in idx) for k2 in works[0]}
+        launch_s = sum(sp[i][2] for i in idx) / 1000.0
+        return w, launch_s
 
-    w = work_counts(spec)
-    pk, pk_kind = peaks()
-    attn_s = parts_ms["paged_attention"] / 1000.0
-    dec_s = kernels_ms["attn_decode"] / 1000.0
-    pre_s = kernels_ms["attn_prefill"] / 1000.0
-    # decode and prefill units share one launch (timed as the prefill span) when the head group
-    # is a power of two and head_dim is 64 or 128 (the tcgen05 path)
-    fused = (d.num_q_heads // d.num_kv_heads) in (1, 2, 4, 8, 16) and d.head_dim in (64, 128)
-    t_tensor = w["prefill_flops"] / (pk["bf16_tflops"] * 1e12)
-    t_hbm = w["decode_bytes"] / (pk["hbm_gbs"] * 1e9)
-    if fused:
-        kernels_ms = {"attn_plan": kernels_ms["attn_plan"],
-                      "attn_fused": kernels_ms["attn_prefill"]}
-        tensor_bound = t_tensor >= t_hbm
-        achieved = (w["prefill_flops"] / pre_s / 1e12 if tensor_bound
-                    else w["decode_bytes"] / pre_s / 1e9)
-        peak = pk["bf16_tflops"] if tensor_bound else pk["hbm_gbs"]
-        roof = {"bound": "tensor" if tensor_bound else "hbm", "achieved": achieved,
-                "peak": peak, "unit": "TFLOP/s" if tensor_bound else "GB/s",
-                "frac": achieved / peak,
-                "traffic": KNOWN_TRAFFIC.get(("fused", args.config, kernel_sources_hash("fused"))),
-                "kernel": "attn_fused (split-KV decode + tcgen05 prefill units, one launch)",
-                "launch_ms": pre_s * 1000.0,
-                "overlap_frac": max(t_tensor, t_hbm) / pre_s,
-                "tensor_frac": w["prefill_flops"] / pre_s / 1e12 / pk["bf16_tflops"],
-                "hbm_frac": w["decode_bytes"] / pre_s / 1e9 / pk["hbm_gbs"],
-                "peak_kind": f"{'bf16 dense burst' if tensor_bound else 'HBM copy'}, {pk_kind}"}
-    # otherwise the dominant kernel: the one with the larger measured share of the step
-    elif pre_s >= dec_s:
-        achieved = w["prefill_flops"] / pre_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops"],
-                "traffic": KNOWN_TRAFFIC.get(("prefill", args.config, kernel_sources_hash("prefill"))),
-                "kernel": "attn_prefill (tcgen05 tiles)", "launch_ms": kernels_ms["attn_prefill"],
-                "peak_kind": f"bf16 dense burst, {pk_kind}"}
-    else:
-        achieved = w["decode_bytes"] / dec_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / pk["hbm_gbs"],
-                "traffic": KNOWN_TRAFFIC.get(("decode", args.config, kernel_sources_hash("decode"))),
-                "kernel": "attn_decode (split-KV)", "launch_ms": kernels_ms["attn_decode"],
-                "peak_kind": f"HBM copy, {pk_kind}"}
-
-    e2e = measure_e2e(spec, tens, buf, dev, args, flush, world)
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms_max,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic (seeded N(0,1) bf16 Q/K/V/hidden, random page ids; no weights)",
-            "config": workload_name(spec, args.config), "roofline": roof,
-            "components_ms": parts_ms, "attention_kernels_ms": kernels_ms,
-            "step_entry": "four calls" if args.four_calls else "rb_step (one memset, two launches)",
-            "breakdown": ("per-call and per-kernel spans from a second pass of the same steps "
-                          "through the four separate calls with events recorded between the "
-                          f"launches (step {marked_step_ms:.4f} ms there; an event node in a "
-                          "graph adds ~3.5 us, so these spans overstate the kernels slightly)"),
-            "work": {"prefill_tflop": w["prefill_flops"] / 1e12,
-                     "decode_kv_gb": w["decode_bytes"] / 1e9,
-                     "attention_call_tflops": w["attn_flops"] / attn_s / 1e12,
-                     "prefill_tflops_over_kernel": w["prefill_flops"] / pre_s / 1e12 if pre_s else None,
-                     "decode_gbs_over_kernel": (w["decode_bytes"] / (pre_s if fused else dec_s) / 1e9
-                                                if (pre_s if fused else dec_s) else None)},
-            "gpu_launches": launches, "launch": "eager" if args.eager else "cuda_graph_replay",
-            "wall_s": wall, "clocks": clocks, "e2e": e2e,
-            "kernel_source_hashes": {k: kernel_sources_hash(k) for k in KERNEL_SOURCES}}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(spec)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    w, launch_s = agg(timed)
+    roof = roofline(w, launch_s, 4, launches=len(timed))
+    all_idx = range(total)
+    w_all, launch_all = agg(all_idx)
+    roof_all = roofline(w_all, launch_all, 4, launches=total)
+    comp = {"batch_update": statistics.mean(sp[i][0] for i in timed),
+            "prep_launch": statistics.mean(sp[i][1] for i in timed),
+            "attention_launch": statistics.mean(sp[i][2] for i in timed)}
+    result = {
+        "value": value, "ms_per_step": t_max / len(timed), "tokens_timed": tok_timed,
+        "median_step_tokens_per_s": statistics.median(tokens[i] / (step_ms[i] / 1000.0)
+                                                      for i in timed),
+        "config": stream_config_desc(d, args.warmup, args.steps, total),
+        "roofline": roof, "components_ms": comp, "gpu_launches": launches,
+        "clocks": clocks, "wall_s": wall,
+        "stream_all": {"steps": total, "tokens": sum(tokens),
+                       "value": sum(tokens) / (sum(step_ms) / 1000.0),
+                       "ms_per_step": sum(step_ms) / total,
+                       "hbm_frac": roof_all["hbm_frac"], "tensor_frac": roof_all["tensor_frac"],
+                       "attention_launch_ms": roof_all["launch_ms"]},
+    }
+    e2e = stream_e2e(args, rank, world, dev, steps, buf, q, k, v, hidden, k_cache, v_cache,
+                     flush)
+    del batch, staged, buf, k_cache, v_cache, flush
+    torch.cuda.empty_cache()
+    return result, e2e
 
 
-def measure_e2e(spec, tens, buf, dev, args, flush, world):
-    """Same step through the C ABI with host buffers (``rb_step_host``): inputs copied from
-    pinned host memory and the results read back inside the timed region."""
+def stream_e2e(args, rank, world, dev, steps, buf, q, k, v, hidden, k_cache, v_cache, flush):
+    """The stream end to end through the public API: per step PersistentBatch.apply (host
+    packing, one packet copy from pinned memory, the update) and rb_step_host (q / k / v /
+    hidden in from pinned host memory, the step, attention output, gathered rows and scalars
+    back), synchronised; wall clock per step, L2 flushed outside it."""
     import torch
 
     import ragged_mixed_paged_gb300 as rb
 
-    host_in = {
-        "token_table": buf.token_table.cpu().pin_memory(),
-        "block_table": buf.block_table.cpu().pin_memory(),
-        "num_computed": buf.num_computed.cpu().pin_memory(),
-        "num_scheduled": buf.num_scheduled.cpu().pin_memory(),
-        "q": buf.q.cpu().pin_memory(), "k": buf.k.cpu().pin_memory(),
-        "v": buf.v.cpu().pin_memory(), "hidden": buf.hidden.cpu().pin_memory(),
-    }
-    dst = {"token_table": buf.token_table, "block_table": buf.block_table,
-           "num_computed": buf.num_computed, "num_scheduled": buf.num_scheduled,
-           "q": buf.q, "k": buf.k, "v": buf.v, "hidden": buf.hidden}
-    host_out = {"attn_out": torch.empty_like(buf.attn_out, device="cpu").pin_memory(),
-                "rows_out": torch.empty_like(buf.rows_out, device="cpu").pin_memory(),
-                "scalars": torch.empty(4, dtype=torch.int32).pin_memory()}
-    src_out = {"attn_out": buf.attn_out, "rows_out": buf.rows_out,
-               "scalars": buf.meta["scalars"]}
-    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
-    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
-
-    # one rb_step_host call: the C ABI enqueues the host-to-device copies of the step's inputs,
-    # the step and the device-to-host copies of its results
-    ins = [(dst[k], t) for k, t in host_in.items()]
-    outs = [(t, src_out[k]) for k, t in host_out.items()]
-
-    def step():
-        rb.run_step_host(buf, ins, outs)
-
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    n = max(3, min(args.steps, 50))
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(n)]
-    for a, b in ev:
+    d = buf.dims
+    batch = rb.PersistentBatch(d.max_num_reqs, d.max_model_len, d.max_blocks_per_req, device=dev)
+    b0 = dataclasses.replace(buf, token_table=batch.token_table, block_table=batch.block_table,
+                             num_computed=batch.num_computed, num_scheduled=batch.num_scheduled,
+                             num_prompt=batch.num_prompt, _step_args=None)
+    nmax = q.shape[0]
+    pin = lambda t: t.cpu().pin_memory()
+    hq, hk, hv, hh = pin(q), pin(k), pin(v), pin(hidden)
+    out_attn = torch.empty(tuple(buf.attn_out.shape), dtype=buf.attn_out.dtype).pin_memory()
+    out_rows = torch.empty(tuple(buf.rows_out.shape), dtype=buf.rows_out.dtype).pin_memory()
+    out_sc = torch.empty(4, dtype=torch.int32).pin_memory()
+    times, h2d, d2h, tok = [], 0, 0, 0
+    for i in range(args.warmup + args.steps):
+        step = steps[i]
         flush.zero_()
-        a.record()
-        step()
-        b.record()
-    torch.cuda.synchronize()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    ms = reduce_over_ranks(ms, "max", world, dev)
-    return {"value": world * spec.num_tokens / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "entry": "rb_step_host (C ABI, host buffers)"}
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        nbytes = batch.apply(step)
+        R, N = batch.num_reqs, batch.num_tokens_scheduled
+        b = dataclasses.replace(b0, num_reqs=R, num_reqs_padded=R, num_tokens=N,
+                                num_tokens_padded=N, q=q[:N], k=k[:N], v=v[:N],
+                                hidden=hidden[:N], attn_out=buf.attn_out[:N],
+                                rows_out=buf.rows_out[:R], _step_args=None)
+        ins = [(b.q, hq[:N]), (b.k, hk[:N]), (b.v, hv[:N]), (b.hidden, hh[:N])]
+        outs = [(out_attn[:N], b.attn_out), (out_rows[:R], b.rows_out), (out_sc, b.meta["scalars"])]
+        rb.run_step_host(b, ins, outs)
+        torch.cuda.synchronize()
+        t1 = time.perf_counter()
+        if int(out_sc[3]) != 0:
+            raise SystemExit(f"e2e step {i}: device error word {int(out_sc[3]):#x}")
+        if i >= args.warmup:
+            times.append(t1 - t0)
+            tok += N
+            h2d += nbytes + sum(t.numel() * t.element_size() for _, t in ins)
+            d2h += sum(t.numel() * t.element_size() for t, _ in outs)
+    K = max(1, args.steps)
+    total = reduce_over_ranks(sum(times), "max", world, dev)
+    toks = reduce_over_ranks(float(tok), "sum", world, dev)
+    del batch
+    return {"value": toks / total, "unit": UNIT, "ms_per_step": 1000.0 * total / K,
+            "h2d_bytes_per_step": h2d / K, "d2h_bytes_per_step": d2h / K,
+            "entry": "PersistentBatch.apply (packet copy + rb_batch_apply_update) + rb_step_host "
+                     "(C ABI, host buffers), wall clock, synchronised every step",
+            "timed_steps": f"{args.warmup}..{args.warmup + args.steps - 1}"}
 
 
-def run_trajectory(args, rank, world, local):
-    """The chunked-prefill mix as a stream: every step merges the scheduler's deltas into the
-    device-resident persistent batch (packet copy + rb_batch_apply_update), then runs the step
-    on the rows it produced.  Eager launches (the shapes change every step)."""
-    import dataclasses
-
+def measure_fixed(config, rank, world, local, steps, warmup, manager_ratio=1, want_e2e=False):
+    """One fixed batch: rb_step captured once as a CUDA graph and replayed with a cold L2; the
+    fused launch timed in a second graph of rb_step_profiled (event nodes between launches)."""
     import torch
 
     import workloads as wl
     import ragged_mixed_paged_gb300 as rb
 
+    dev = torch.device("cuda", local)
+    spec = make_spec(config, rank, manager_ratio)
+    d = spec.dims
+    tens = wl.make_tensors(spec, device=dev)
+    tables = wl.device_tables(spec, dev)
+    buf = rb.StepBuffers.allocate(rb.Dims.of(d), spec.num_reqs, spec.num_reqs_padded,
+                                  spec.num_tokens, spec.num_tokens_padded, tables, tens.q,
+                                  tens.k, tens.v, tens.hidden, tens.k_cache, tens.v_cache)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    for _ in range(warmup):
+        flush.zero_()
+        rb.run_step_fused(buf)
+    torch.cuda.synchronize()
+    if int(buf.meta["scalars"][3].item()) != 0:
+        raise SystemExit(f"device error word {int(buf.meta['scalars'][3].item()):#x}")
+    inner = _recorded_events(2)
+    torch.cuda.synchronize()
+    launches0 = rb.launch_count()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        rb.run_step_fused(buf)
+    per_step = rb.launch_count() - launches0
+    marked = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(marked):
+        rb.run_step_fused(buf, events=inner)
+    graph.replay()
+    marked.replay()
+    torch.cuda.synchronize()
+    ev = [_events(2) for _ in range(steps)]
+    sampler = ClockSampler(local)
+    barrier(world)
+    torch.cuda.synchronize()
+    sampler.start()
+    w0 = time.perf_counter()
+    for a, b in ev:
+        flush.zero_()
+        a.record()
+        graph.replay()
+        b.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - w0
+    clocks = sampler.stop()
+    step_times = [a.elapsed_time(b) for a, b in ev]
+    # breakdown pass: the same step with the library's events between its two launches
+    pre, att = [], []
+    for _ in range(steps):
+        flush.zero_()
+        a = _events(1)[0]
+        a.record()
+        marked.replay()
+        torch.cuda.synchronize()
+        pre.append(a.elapsed_time(inner[0]))
+        att.append(inner[0].elapsed_time(inner[1]))
+    med = statistics.median(step_times)
+    med_max = reduce_over_ranks(med, "max", world, dev)
+    toks = reduce_over_ranks(float(spec.num_tokens), "sum", world, dev)
+    launch_s = statistics.median(att) / 1000.0
+    out = {"value": toks / (med_max / 1000.0), "ms_per_step": med_max,
+           "ms_per_step_mean": statistics.mean(step_times), "steps": steps, "warmup": warmup,
+           "config": fixed_config_desc(spec, config),
+           "roofline": roofline(spec_work(spec), launch_s, config),
+           "components_ms": {"prep_launch": statistics.median(pre),
+                             "attention_launch": statistics.median(att)},
+           "gpu_launches": per_step * steps, "launch": "cuda_graph_replay", "wall_s": wall,
+           "clocks": clocks}
+    e2e = fixed_e2e(spec, buf, flush, steps, warmup, world, dev) if want_e2e else None
+    del buf, tens, tables, flush, graph, marked
+    torch.cuda.empty_cache()
+    return out, e2e
+
+
+def fixed_e2e(spec, buf, flush, steps, warmup, world, dev):
+    """A fixed batch through rb_step_host with host buffers (inputs in from pinned memory,
+    results back), every step synchronised; wall clock."""
+    import torch
+
+    import ragged_mixed_paged_gb300 as rb
+
+    host_in = [(t, t.cpu().pin_memory()) for t in (
+        buf.token_table, buf.block_table, buf.num_computed, buf.num_scheduled, buf.q, buf.k,
+        buf.v, buf.hidden)]
+    host_out = [(torch.empty_like(t, device="cpu").pin_memory(), t) for t in (
+        buf.attn_out, buf.rows_out, buf.meta["scalars"])]
+    h2d = sum(t.numel() * t.element_size() for _, t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t, _ in host_out)
+    times = []
+    for i in range(warmup + steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        rb.run_step_host(buf, host_in, host_out)
+        torch.cuda.synchronize()
+        if i >= warmup:
+            times.append(time.perf_counter() - t0)
+    ms = reduce_over_ranks(1000.0 * statistics.median(times), "max", world, dev)
+    return {"value": world * spec.num_tokens / (ms / 1000.0), "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "entry": "rb_step_host (C ABI, host buffers), wall clock, median"}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device for --impl ours")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    stream = wl.MixedChunkStream(seed=4000 + 7919 * rank)
-    d = stream.dims
-    dims = rb.Dims.of(d)
-    steps = [stream.next_step() for _ in range(args.warmup + args.steps)]
-    nmax, rmax = stream.BUDGET, d.max_num_reqs
-    g = torch.Generator(device=dev).manual_seed(4000 + rank)
-    bf = torch.bfloat16
-    rnd = lambda *shape: torch.randn(*shape, generator=g, device=dev, dtype=torch.float32).to(bf)
-    q, k, v = (rnd(nmax, d.num_q_heads, d.head_dim), rnd(nmax, d.num_kv_heads, d.head_dim),
-               rnd(nmax, d.num_kv_heads, d.head_dim))
-    hidden = rnd(nmax, 4096)
-    k_cache = torch.empty((d.num_blocks * d.block_size, d.num_kv_heads, d.head_dim), dtype=bf,
-                          device=dev).normal_(generator=g)
-    v_cache = torch.empty_like(k_cache).normal_(generator=g)
-    batch = rb.PersistentBatch(d.max_num_reqs, d.max_model_len, d.max_blocks_per_req, device=dev)
-    buf = rb.StepBuffers.allocate(dims, rmax, rmax, nmax, nmax, batch.tables(), q, k, v, hidden,
-                                  k_cache, v_cache)
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    E = lambda: torch.cuda.Event(enable_timing=True)
-    host_rows = torch.empty((rmax, 4096), dtype=bf).pin_memory()
-    host_scalars = torch.empty(4, dtype=torch.int32).pin_memory()
-    rec, tokens, h2d, d2h = [], 0, 0, 0
-    sampler = ClockSampler(local)
-    launches0 = None
-    barrier(world)
-    for i, step in enumerate(steps):
-        if i == args.warmup:
-            torch.cuda.synchronize()
-            sampler.start()
-            launches0 = rb.launch_count()
-        flush.zero_()
-        ev = [E() for _ in range(5)]
-        ev[0].record()
-        nbytes = batch.apply(step, copied_event=ev[1])
-        ev[2].record()
-        R, N = batch.num_reqs, batch.num_tokens_scheduled
-        b = dataclasses.replace(buf, num_reqs=R, num_reqs_padded=R, num_tokens=N,
-                                num_tokens_padded=N, q=q[:N], k=k[:N], v=v[:N], hidden=hidden[:N],
-                                attn_out=buf.attn_out[:N])
-        rb.run_step_fused(b)
-        ev[3].record()
-        host_rows[:R].copy_(b.rows_out[:R], non_blocking=True)
-        host_scalars.copy_(b.meta["scalars"], non_blocking=True)
-        ev[4].record()
-        torch.cuda.synchronize()
-        if int(host_scalars[3]) != 0 or int(batch.error_word.item()) != 0:
-            raise SystemExit(f"step {i}: error words {int(host_scalars[3]):#x} "
-                             f"{int(batch.error_word.item()):#x}")
-        if i >= args.warmup:
-            rec.append([ev[0].elapsed_time(e) for e in ev[1:]])
-            tokens += N
-            h2d += nbytes
-            d2h += R * 4096 * 2 + 16
-    launches = rb.launch_count() - launches0
-    clocks = sampler.stop()
-    barrier(world)
-    rec = list(zip(*rec))  # per mark: copy done | update done | step done | results read
-    pack_copy = statistics.mean(rec[0])
-    update = statistics.mean(b2 - b1 for b1, b2 in zip(rec[0], rec[1]))
-    step_ms = statistics.mean(b3 - b2 for b2, b3 in zip(rec[1], rec[2]))
-    e2e_ms = statistics.mean(rec[3])
-    dev_ms = update + step_ms
-    total = reduce_over_ranks(float(tokens), "sum", world, dev)
-    dev_ms = reduce_over_ranks(dev_ms, "max", world, dev)
-    e2e_ms = reduce_over_ranks(e2e_ms, "max", world, dev)
-    K = args.steps
-    # what the update replaces: uploading the whole token and page tables every step
-    tt = torch.empty((rmax, d.max_model_len), dtype=torch.int32).pin_memory()
-    bt = torch.empty((rmax, d.max_blocks_per_req), dtype=torch.int32).pin_memory()
-    gt, gb = torch.empty_like(tt, device=dev), torch.empty_like(bt, device=dev)
-    a, z = E(), E()
-    a.record()
-    for _ in range(5):
-        gt.copy_(tt, non_blocking=True)
-        gb.copy_(bt, non_blocking=True)
-    z.record()
-    torch.cuda.synchronize()
+    side_steps = max(3, min(args.steps, 10))
+    if args.config == 4:
+        head, e2e = measure_stream(args, rank, world, local)
+    else:
+        head, e2e = measure_fixed(args.config, rank, world, local, args.steps, args.warmup,
+                                  args.manager_ratio, want_e2e=True)
+    line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded N(0,1) bf16 Q/K/V/hidden and KV pool, seeded request "
+                    "stream and page ids; no weights)",
+            "config": head["config"], "roofline": head["roofline"],
+            "gpu_launches": head["gpu_launches"], "clocks": head["clocks"], "e2e": e2e,
+            "components_ms": head["components_ms"],
+            "kernel_source_hash": kernel_sources_hash()}
+    for key in ("stream_all", "median_step_tokens_per_s", "tokens_timed", "launch", "wall_s"):
+        if key in head:
+            line[key] = head[key]
+    if not args.no_side_configs:
+        side = {}
+        for c in (2, 3, 5):
+            if c == args.config:
+                continue
+            out, _ = measure_fixed(c, rank, world, local, side_steps, 3)
+            side[str(c)] = {k2: out[k2] for k2 in ("value", "ms_per_step", "roofline",
+                                                    "components_ms", "config", "clocks")}
+            side[str(c)]["unit"] = UNIT
+            side[str(c)]["timing"] = (f"median of {side_steps} graph replays of rb_step after "
+                                      "3 warm-ups, L2 flushed before each")
+        line["configs"] = side
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config, rank)
     if rank == 0:
-        print(json.dumps({
-            "metric": METRIC + " (stream of steps with the batch update)",
-            "value": total / (dev_ms * K / 1000.0),
-            "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-            "ms_per_step": dev_ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic request stream",
-            "config": {"workload": f"chunked-prefill mix stream, steps {args.warmup}.."
-                                   f"{args.warmup + K - 1}", "l2": "512 MiB flush per step",
-                       "launch": "eager"},
-            "components_ms": {"pack_and_packet_h2d": pack_copy, "batch_update": update,
-                              "step": step_ms},
-            "e2e": {"value": total / (e2e_ms * K / 1000.0), "unit": UNIT, "ms_per_step": e2e_ms,
-                    "h2d_bytes_per_step": h2d / K, "d2h_bytes_per_step": d2h / K},
-            "full_table_h2d_ms": a.elapsed_time(z) / 5,
-            "full_table_bytes": tt.numel() * 4 + bt.numel() * 4,
-            "gpu_launches": launches, "clocks": clocks}), flush=True)
+        print(json.dumps(line), flush=True)
+
 
 def run_cascade_compare(args, rank, world, local):
     """Shared system prompt (256 decodes after a common 4096-token prefix, own suffixes
@@ -733,8 +900,7 @@ def run_cascade_compare(args, rank, world, local):
                                                       tens.v_cache, bt, qsl, sl, out=out,
                                                       workspace=ws, error_word=err),
     }
-    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
-    E = lambda: torch.cuda.Event(enable_timing=True)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
     res = {}
     sampler = ClockSampler(local)
     sampler.start()
@@ -748,13 +914,13 @@ def run_cascade_compare(args, rank, world, local):
         times = []
         for _ in range(args.steps):
             flush.zero_()
-            a, b = E(), E()
+            a, b = _events(2)
             a.record()
             g.replay()
             b.record()
             torch.cuda.synchronize()
             times.append(a.elapsed_time(b))
-        res[name] = statistics.mean(times)
+        res[name] = statistics.median(times)
     clocks = sampler.stop()
     if int(err.item()) != 0:
         raise SystemExit(f"device error word {int(err.item()):#x}")
@@ -781,33 +947,27 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=95)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--config", type=int, default=4, choices=[2, 3, 4, 5])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--eager", action="store_true",
-                    help="launch every step from Python instead of replaying a captured graph")
-    ap.add_argument("--four-calls", action="store_true",
-                    help="time the four separate entry points instead of the one rb_step call")
+    ap.add_argument("--no-side-configs", action="store_true",
+                    help="skip the configs 2/3/5 entries of the line")
     ap.add_argument("--manager-ratio", type=int, default=1,
                     help="--config 2/3: page tables of manager blocks of this many kernel pages")
     ap.add_argument("--cascade", action="store_true",
                     help="time one attention call on a shared-prefix batch, plain vs cascade")
-    ap.add_argument("--trajectory", action="store_true",
-                    help="--config 4 only: time a stream of steps, each with its batch update")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
+    if args.steps < 1:
+        raise SystemExit("--steps must be >= 1")
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
     elif args.cascade:
         run_cascade_compare(args, rank, world, local)
-    elif args.trajectory:
-        if args.config != 4:
-            raise SystemExit("--trajectory needs --config 4")
-        run_trajectory(args, rank, world, local)
     else:
         run_ours(args, rank, world, local)
     if world > 1:

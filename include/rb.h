@@ -371,6 +371,17 @@ typedef struct rb_step_args {
 rb_status rb_step(const rb_step_args* args, void* stream);
 
 /*
+ * rb_step_profiled — rb_step with caller-owned CUDA events recorded between its launches, for
+ * per-kernel timing of a step: events[0] after the preparation launch, events[1] after the
+ * attention launch (cudaEvent_t passed as void*, created by the caller; null slots and slots
+ * past num_events are skipped).  Inside a stream capture the records become external event
+ * nodes.  Sources, arguments, results and errors are those of rb_step, plus RB_ERR_INVALID_ARG
+ * for num_events < 0 or a null `events` with num_events > 0, and RB_ERR_CUDA if a record fails.
+ */
+rb_status rb_step_profiled(const rb_step_args* args, void* const* events, int32_t num_events,
+                           void* stream);
+
+/*
  * rb_host_copy — one contiguous copy between caller-owned host memory and caller-owned device
  * memory: `bytes` bytes from `src` to `dst` (both null only when `bytes` is 0).  Page-locked
  * host memory makes the copy asynchronous; pageable memory works but the copy then blocks the

@@ -110,6 +110,8 @@ def _load():
         "rb_batch_update_workspace_size": (I32, [I32, ctypes.POINTER(ctypes.c_size_t)]),
         "rb_cascade_prefix_len": (I32, [I32, P, I32, I32]),
         "rb_step": (I32, [ctypes.POINTER(rb_step_args), P]),
+        "rb_step_profiled": (I32, [ctypes.POINTER(rb_step_args), ctypes.POINTER(ctypes.c_void_p),
+                                   I32, P]),
         "rb_step_host": (I32, [ctypes.POINTER(rb_step_args), ctypes.POINTER(rb_host_copy), I32,
                                ctypes.POINTER(rb_host_copy), I32, P]),
         "rb_paged_attention_cascade_workspace_size": (ctypes.c_size_t, [PD, I32, I32]),

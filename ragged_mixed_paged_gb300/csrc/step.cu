@@ -188,9 +188,26 @@ rb_status step_build(const rb_step_args& x, StepArgs* out_sa, attn::AttnSetup* o
   return RB_OK;
 }
 
-// The step's memset and two launches on stream `s`.
+// Records event i of a profiled call (none when i >= n or the slot is null); inside a stream
+// capture the record becomes a graph node.
+struct StepMarks {
+  void* const* events;
+  int n;
+  bool record(int i, cudaStream_t s) const {
+    if (i >= n || events[i] == nullptr) return true;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) return false;
+    return cudaEventRecordWithFlags(static_cast<cudaEvent_t>(events[i]), s,
+                                    cap == cudaStreamCaptureStatusActive
+                                        ? cudaEventRecordExternal
+                                        : cudaEventRecordDefault) == cudaSuccess;
+  }
+};
+
+// The step's memset and two launches on stream `s`; `marks` (optional) records its events
+// after the preparation launch and after the attention launch.
 rb_status step_enqueue(const rb_step_args& x, const StepArgs& sa, const attn::AttnSetup& su,
-                       cudaStream_t s) {
+                       cudaStream_t s, const StepMarks& marks = StepMarks{nullptr, 0}) {
   if (cudaMemsetAsync(x.d_scalars + 3, 0, sizeof(int32_t), s) != cudaSuccess) return RB_ERR_CUDA;
   const size_t smem = static_cast<size_t>(x.num_reqs + 1) * sizeof(int32_t);
   if (smem > 48 * 1024 &&
@@ -203,7 +220,10 @@ rb_status step_enqueue(const rb_step_args& x, const StepArgs& sa, const attn::At
   step_prep_kernel<<<grid, prep::kThreads, smem, s>>>(sa);
   if (last_launch_status() != RB_OK) return RB_ERR_CUDA;
   note_launches(1);
-  return attn::attn_main(su, s);
+  if (!marks.record(0, s)) return RB_ERR_CUDA;
+  const rb_status st = attn::attn_main(su, s);
+  if (st != RB_OK) return st;
+  return marks.record(1, s) ? RB_OK : RB_ERR_CUDA;
 }
 
 }  // namespace
@@ -218,6 +238,21 @@ extern "C" rb_status rb_step(const rb_step_args* args, void* stream) {
   const rb_status st = step_build(*args, &sa, &su);
   if (st != RB_OK) return st;
   return step_enqueue(*args, sa, su, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" rb_status rb_step_profiled(const rb_step_args* args, void* const* events,
+                                      int32_t num_events, void* stream) {
+  rb::CallRange range_("rb_step_profiled");
+  using namespace rb;
+  if (args == nullptr || args->dims == nullptr || num_events < 0 ||
+      (num_events > 0 && events == nullptr))
+    return RB_ERR_INVALID_ARG;
+  StepArgs sa;
+  attn::AttnSetup su;
+  const rb_status st = step_build(*args, &sa, &su);
+  if (st != RB_OK) return st;
+  return step_enqueue(*args, sa, su, static_cast<cudaStream_t>(stream),
+                      StepMarks{events, num_events});
 }
 
 extern "C" rb_status rb_step_host(const rb_step_args* args, const rb_host_copy* in,

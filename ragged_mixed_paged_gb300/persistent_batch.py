@@ -64,6 +64,19 @@ class _Staging:
         return slot
 
 
+class StagedStep:
+    """One step's packed scheduler output, already in device memory."""
+
+    def __init__(self, packet, offsets, num_scheduled, num_new, num_cached, num_tokens, nbytes):
+        self.packet = packet
+        self.offsets = offsets
+        self.num_scheduled = num_scheduled
+        self.num_new = num_new
+        self.num_cached = num_cached
+        self.num_tokens = num_tokens
+        self.nbytes = nbytes
+
+
 class PersistentBatch:
     """One row per resident request; the live rows are always [0, num_reqs)."""
 
@@ -127,17 +140,34 @@ class PersistentBatch:
             ("cached_blocks", cat([c.new_blocks for c in cached])),
         ], len(sched_ids), len(new), len(cached)
 
+    @classmethod
+    def _layout(cls, step):
+        sections, S, NN, NC = cls.pack(step)
+        offsets, n = {}, 0
+        for name, arr in sections:
+            offsets[name] = n
+            n += -(-arr.size // _ALIGN) * _ALIGN
+        return sections, offsets, n, S, NN, NC
+
+    def _launch(self, base: int, offsets: dict, S: int, NN: int, NC: int, stream) -> None:
+        import torch
+
+        ptr = {name: base + 4 * off for name, off in offsets.items()}
+        u = rb.rb_batch_update(S, NN, NC, 0, *(ptr[f[0][2:]] for f in rb.rb_batch_update._fields_[4:]))
+        st = rb.lib.rb_batch_apply_update(
+            ctypes.byref(self._c), ctypes.byref(u), rb._ptr(self.num_scheduled, torch.int32),
+            rb._ptr(self.row_of_sched, torch.int32), rb._ptr(self.workspace),
+            self.workspace.numel(), rb._ptr(self.error_word, torch.int32), rb._stream(stream))
+        rb._check("rb_batch_apply_update", st)
+        self.num_reqs = S
+
     def apply(self, step, stream=None, copied_event=None) -> int:
         """Merge one step's scheduler output into the batch (enqueued on ``stream``); returns
         the bytes copied host -> device.  Sets ``num_reqs`` / ``num_tokens_scheduled``.
         ``copied_event``, if given, is recorded between the packet copy and the kernels."""
         import torch
 
-        sections, S, NN, NC = self.pack(step)
-        offsets, n = {}, 0
-        for name, arr in sections:
-            offsets[name] = n
-            n += -(-arr.size // _ALIGN) * _ALIGN
+        sections, offsets, n, S, NN, NC = self._layout(step)
         host, dev, _ = slot = self._staging.get(n)
         view = host.numpy()
         for name, arr in sections:
@@ -150,18 +180,34 @@ class PersistentBatch:
         slot[2] = ev
         if copied_event is not None:
             copied_event.record(s)
-        base = dev.data_ptr()
-        ptr = {name: base + 4 * off for name, off in offsets.items()}
-        u = rb.rb_batch_update(S, NN, NC, 0, *(ptr[f[0][2:]] for f in rb.rb_batch_update._fields_[4:]))
-        st = rb.lib.rb_batch_apply_update(
-            ctypes.byref(self._c), ctypes.byref(u), rb._ptr(self.num_scheduled, torch.int32),
-            rb._ptr(self.row_of_sched, torch.int32), rb._ptr(self.workspace),
-            self.workspace.numel(), rb._ptr(self.error_word, torch.int32), rb._stream(s))
-        rb._check("rb_batch_apply_update", st)
-        self.num_reqs = S
+        self._launch(dev.data_ptr(), offsets, S, NN, NC, s)
         self.num_tokens_scheduled = int(sum(step.scheduled.values()))
         self.last_h2d_bytes = 4 * n
         return self.last_h2d_bytes
+
+    def stage(self, step, device=None) -> "StagedStep":
+        """Pack one step's scheduler output and copy it into a device buffer of its own, ahead
+        of time (a caller that has the step before it runs, e.g. a benchmark); the copy is
+        complete when this returns.  ``apply_staged`` then merges it with no host work."""
+        import torch
+
+        sections, offsets, n, S, NN, NC = self._layout(step)
+        host = np.zeros(max(n, 1), np.int32)
+        for name, arr in sections:
+            host[offsets[name]:offsets[name] + arr.size] = arr
+        dev = torch.from_numpy(host).to(device or self.req_id.device)
+        return StagedStep(dev, offsets, S, NN, NC, int(sum(step.scheduled.values())), 4 * n)
+
+    def apply_staged(self, staged: "StagedStep", stream=None) -> None:
+        """``apply`` for a packet already on the device (``stage``): only the update's
+        launches are enqueued on ``stream``."""
+        import torch
+
+        s = stream if stream is not None else torch.cuda.current_stream()
+        self._launch(staged.packet.data_ptr(), staged.offsets, staged.num_scheduled,
+                     staged.num_new, staged.num_cached, s)
+        self.num_tokens_scheduled = staged.num_tokens
+        self.last_h2d_bytes = 0
 
     # ------------------------------------------------------------------------------ views
     def tables(self) -> dict:

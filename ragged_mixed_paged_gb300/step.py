@@ -133,11 +133,23 @@ def _step_args(b: StepBuffers, softmax_scale: Optional[float]):
         p(b.rows_out, bf), p(b.workspace, torch.uint8), b.workspace.numel())
 
 
-def run_step_fused(b: StepBuffers, stream=None, softmax_scale: Optional[float] = None) -> None:
-    """Enqueue the whole step as one ``rb_step`` call (one memset and two launches)."""
+def run_step_fused(b: StepBuffers, stream=None, softmax_scale: Optional[float] = None,
+                   events=None) -> None:
+    """Enqueue the whole step as one ``rb_step`` call (one memset and two launches).
+
+    ``events``: optional recorded-once torch.cuda.Event objects that the library re-records
+    after its preparation launch and after its attention launch (``rb_step_profiled``)."""
     if b._step_args is None or softmax_scale is not None:
         b._step_args = _step_args(b, softmax_scale)
-    rb._check("rb_step", rb.lib.rb_step(ctypes.byref(b._step_args), rb._stream(stream)))
+    if events is None:
+        rb._check("rb_step", rb.lib.rb_step(ctypes.byref(b._step_args), rb._stream(stream)))
+        return
+    handles = [e.cuda_event for e in events]
+    if not all(handles):
+        raise ValueError("record each event once before passing it (torch creates them lazily)")
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    rb._check("rb_step_profiled", rb.lib.rb_step_profiled(ctypes.byref(b._step_args), arr,
+                                                          len(handles), rb._stream(stream)))
 
 
 def _copies(pairs):

@@ -236,6 +236,11 @@ def test_step_host_checks(lib):
     args.num_reqs = args.num_reqs_padded = 1
     args.num_tokens = args.num_tokens_padded = 1
     assert L.rb_step(ctypes.byref(args), None) == 1            # no metadata buffers
+    none = ctypes.POINTER(ctypes.c_void_p)()
+    assert L.rb_step_profiled(None, none, 0, None) == 1
+    assert L.rb_step_profiled(ctypes.byref(args), none, 2, None) == 1   # null events array
+    assert L.rb_step_profiled(ctypes.byref(args), none, -1, None) == 1
+    assert L.rb_step_profiled(ctypes.byref(args), none, 0, None) == 1   # no metadata buffers
 
 
 def test_step_host_copy_checks(lib):

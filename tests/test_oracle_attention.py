@@ -133,3 +133,20 @@ def test_row_subset_matches_full():
     for r in (0, 5, 10):
         np.testing.assert_array_equal(part[r], full[r])
     assert np.isnan(part[1]).all()
+
+
+def test_threaded_evaluation_equals_one_call():
+    """oracle.threads evaluates each request on its own rows in a thread pool: the same rows as
+    one call over the whole batch (up to BLAS summation order), NaN elsewhere, padding zero."""
+    from oracle.threads import oracle_attention_threads
+
+    rng = np.random.default_rng(6)
+    c, qn = [30, 0, 12, 7], [1, 9, 5, 1]
+    q, k, v, hk, hv = _rand_batch(rng, c, qn, 8, 2, 16, pad=2)
+    qsl, sl = _meta(c, qn)
+    rows = [0, 1, 4, 9, 10, 12, 15]
+    full = oracle.paged_attention(q, hk, hv, k, v, qsl, sl, 4)
+    got = oracle_attention_threads(q, hk, hv, k, v, qsl, sl, 4, rows, workers=3)
+    np.testing.assert_allclose(got[rows], full[rows], rtol=0, atol=1e-13)
+    others = [r for r in range(16) if r not in rows]
+    assert np.isnan(got[others]).all() and np.all(got[16:] == 0)
