@@ -71,7 +71,7 @@ WORKLOAD_NAMES = {1: "pages' worked example A/B/C", 2: "pages' padding example",
 
 
 # ----------------------------------------------------------------------------- workloads
-def make_spec(config: int, rank: int = 0, manager_ratio: int = 1):
+def make_spec(config: int, rank: int = 0, manager_ratio: int = 1, context_scale: float = 1.0):
     import workloads as wl
 
     if config == 1:
@@ -81,7 +81,7 @@ def make_spec(config: int, rank: int = 0, manager_ratio: int = 1):
     if config == 3:
         return wl.config3(step=rank, manager_ratio=manager_ratio)
     if config == 5:
-        return wl.config5(step=rank)
+        return wl.config5(step=rank, context_scale=context_scale)
     raise SystemExit(f"config {config} is not a single fixed batch")
 
 
@@ -714,7 +714,8 @@ def stream_e2e(args, rank, world, dev, steps, buf, q, k, v, hidden, k_cache, v_c
             "timed_steps": f"{args.warmup}..{args.warmup + args.steps - 1}"}
 
 
-def measure_fixed(config, rank, world, local, steps, warmup, manager_ratio=1, want_e2e=False):
+def measure_fixed(config, rank, world, local, steps, warmup, manager_ratio=1, want_e2e=False,
+                  context_scale=1.0):
     """One fixed batch: rb_step captured once as a CUDA graph and replayed with a cold L2; the
     fused launch timed in a second graph of rb_step_profiled (event nodes between launches)."""
     import torch
@@ -723,7 +724,7 @@ def measure_fixed(config, rank, world, local, steps, warmup, manager_ratio=1, wa
     import ragged_mixed_paged_gb300 as rb
 
     dev = torch.device("cuda", local)
-    spec = make_spec(config, rank, manager_ratio)
+    spec = make_spec(config, rank, manager_ratio, context_scale)
     d = spec.dims
     tens = wl.make_tensors(spec, device=dev)
     tables = wl.device_tables(spec, dev)
@@ -835,7 +836,8 @@ def run_ours(args, rank, world, local):
         head, e2e = measure_stream(args, rank, world, local)
     else:
         head, e2e = measure_fixed(args.config, rank, world, local, args.steps, args.warmup,
-                                  args.manager_ratio, want_e2e=True)
+                                  args.manager_ratio, want_e2e=True,
+                                  context_scale=args.context_scale)
     line = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
@@ -956,6 +958,9 @@ def main(argv=None):
                     help="skip the configs 2/3/5 entries of the line")
     ap.add_argument("--manager-ratio", type=int, default=1,
                     help="--config 2/3: page tables of manager blocks of this many kernel pages")
+    ap.add_argument("--context-scale", type=float, default=1.0,
+                    help="--config 5: cached lengths times this factor (a smaller case, e.g. "
+                         "for a profiler; not a headline)")
     ap.add_argument("--cascade", action="store_true",
                     help="time one attention call on a shared-prefix batch, plain vs cascade")
     args = ap.parse_args(argv)

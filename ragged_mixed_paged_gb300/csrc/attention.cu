@@ -11,11 +11,10 @@
 //   1. plan     (1 CTA)  validates the metadata, classifies requests (decode-like when
 //                        query_len * group <= 8), splits the CTAs between decode and prefill
 //                        work, sizes KV splits, writes per-request unit offsets, zeroes padding;
-//   2. one persistent launch (head groups that are powers of two): every CTA runs decode units
-//      (split-KV, one warp per (request, kv head, split); the last split of a (request, kv head)
-//      merges the partials) and prefill units (tcgen05 tiles), starting with the kind the
-//      planner assigned it and then helping with the other, so HBM-bound and tensor-bound work
-//      overlap; other groups run a decode launch and an mma.sync prefill launch instead.
+//   2. one persistent launch: every CTA runs decode units (split-KV, one warp per (request, kv
+//      head, split); the last split of a (request, kv head) merges the partials) and prefill
+//      units (tcgen05 tiles of 128 / group whole tokens), starting with the kind the planner
+//      assigned it and then helping with the other, so HBM-bound and tensor-bound work overlap.
 #include "attn_plan.cuh"
 
 namespace rb {
@@ -50,7 +49,8 @@ __global__ void __launch_bounds__(kPlanThreads)
   }
   if (tid == 0) {
     a.header[kHNumDecodeUnits] = 0;
-    a.header[kHNumPrefillUnits] = a.nkv * ((a.N * a.group + 255) / 256) * a.prefix_splits;
+    a.header[kHNumPrefillUnits] =
+        a.nkv * ((a.N + 2 * a.tile_tokens - 1) / (2 * a.tile_tokens)) * a.prefix_splits;
     a.header[kHDecodeNext] = 0;
     a.header[kHPrefillNext] = 0;
     a.header[kHSplitPages] = kMinSplitPages;
@@ -108,7 +108,6 @@ rb_status attn_setup(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
   const int group = d.num_q_heads / d.num_kv_heads;
   su->g = g;
   su->head_dim = d.head_dim;
-  su->use_tc = prefill_tc_supported(d.head_dim, group);
   su->k_cache = d_k_cache;
   su->v_cache = d_v_cache;
   su->num_kv_heads = d.num_kv_heads;
@@ -141,8 +140,8 @@ rb_status attn_setup(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
   a.kp_cap = static_cast<long long>(d.max_blocks_per_req) * g.ratio;
   const int sms = max(1, device_sm_count());
   a.target_units = min(kMaxTargetUnits, 32 * sms);
-  a.tile_m = su->use_tc ? 256 : kPrefillTileM;  // tcgen05 units are pairs of 128-row tiles
-  a.fused_ctas = su->use_tc ? sms : 0;
+  a.tile_tokens = 128 / group;  // a tcgen05 unit is a pair of 128-row tiles of whole tokens
+  a.fused_ctas = sms;
   a.decode_warps_per_cta = 8;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.err = d_error_word;
@@ -156,8 +155,7 @@ rb_status attn_encode_maps(AttnSetup* su) {
       !encode_kv_tensor_map(&su->vmap, su->v_cache, su->head_dim, su->num_kv_heads,
                             su->num_slots))
     return RB_ERR_CUDA;
-  if (su->use_tc && a.N_pad > 0 &&
-      !encode_q_tensor_map(&su->qmap, a.q, su->head_dim, a.nh, a.N_pad, a.group))
+  if (a.N_pad > 0 && !encode_q_tensor_map(&su->qmap, a.q, su->head_dim, a.nh, a.N_pad, a.group))
     return RB_ERR_CUDA;
   return RB_OK;
 }
@@ -166,17 +164,9 @@ template <class Mark>
 rb_status attn_main_impl(const AttnSetup& su, cudaStream_t s, const Mark& mark) {
   const AttnArgs& a = su.a;
   rb_status st = RB_OK;
-  if (su.use_tc) {  // one launch runs decode and prefill units side by side
-    if (!mark(1)) return RB_ERR_CUDA;
-    if (a.R > 0) st = launch_prefill_tc(a, su.head_dim, su.qmap, su.kmap, su.vmap, s);
-    if (st != RB_OK) return st;
-    if (!mark(2)) return RB_ERR_CUDA;
-    return RB_OK;
-  }
-  if (a.R > 0) st = launch_decode(a, su.head_dim, su.kmap, su.vmap, s);
-  if (st != RB_OK) return st;
+  // one launch runs decode and prefill units side by side
   if (!mark(1)) return RB_ERR_CUDA;
-  if (a.R > 0) st = launch_prefill(a, su.head_dim, su.kmap, su.vmap, s);
+  if (a.R > 0) st = launch_prefill_tc(a, su.head_dim, su.qmap, su.kmap, su.vmap, s);
   if (st != RB_OK) return st;
   if (!mark(2)) return RB_ERR_CUDA;
   return RB_OK;
@@ -233,7 +223,6 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
   const CascadeLayout cl =
       cascade_layout(d.head_dim, d.num_q_heads, d.num_kv_heads, num_reqs, num_tokens);
   if (prefix_len > 0 && workspace_bytes < cl.total) return RB_ERR_CAPACITY;
-  if (prefix_len > 0 && !su.use_tc) return RB_ERR_UNSUPPORTED;
   st = attn_encode_maps(&su);
   if (st != RB_OK) return st;
 
@@ -242,7 +231,6 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
   if (prefix_len > 0) {
     // "8.3.2.5 Cascade Attention": the shared prefix once for every query row, then the
     // ordinary causal pass over each request's own keys [P, seq_len), merged per row
-    const int group = a.group;
     const int entries = prefix_len / (kPage * g.ratio);
     int32_t* lens = reinterpret_cast<int32_t*>(ws + cl.lens);
     a.pre_lse = reinterpret_cast<float*>(ws + cl.lse);
@@ -250,7 +238,8 @@ rb_status paged_attention_impl(const rb_dims* dims, int32_t num_reqs, int32_t nu
     // cut the prefix keys into ranges so the prefix pass has a few units per SM (each range
     // at least 4 key tiles); the suffix epilogues merge one partial per range
     const int tiles = (prefix_len + 127) / 128;
-    const int base_units = d.num_kv_heads * ((num_tokens * group + 255) / 256);
+    const int base_units = d.num_kv_heads * ((num_tokens + 2 * a.tile_tokens - 1) /
+                                             (2 * a.tile_tokens));
     const int sms = max(1, device_sm_count());
     int splits = (4 * sms + base_units - 1) / base_units;
     splits = max(1, min(splits, min(kMaxPrefixSplits, tiles / 4)));

@@ -8,7 +8,6 @@ namespace rb {
 namespace attn {
 
 constexpr int kMaxCols = 8;          // decode columns: (query token, head of the group) pairs
-constexpr int kPrefillTileM = 64;    // query rows per mma.sync prefill tile
 constexpr int kMaxTargetUnits = 8192;
 constexpr int kMinSplitPages = 8;
 constexpr int kPage = 16;            // tokens per KV page (the only page size these kernels take)
@@ -31,8 +30,9 @@ struct WsLayout {
   long long max_units;
 };
 
-// Prefill (request, 256-row pair) entries a batch can have: sum over requests of
-// ceil(q_i * group / 256) <= N * 16 / 256 + R for groups up to 16.
+// Prefill (request, tile pair) entries a batch can have: a pair covers 2 * (128 / group) >= 16
+// query tokens for groups up to 16, so sum over requests of ceil(q_i / pair tokens)
+// <= N / 16 + R.
 __host__ __device__ inline long long max_prefill_pairs(int num_reqs, int num_tokens) {
   return static_cast<long long>(num_tokens) / 16 + num_reqs + 1;
 }
@@ -104,7 +104,7 @@ struct AttnArgs {
   int R, N, N_pad, nh, nkv, group, MB, num_blocks, null_block;
   int ratio;  // kernel pages per page-table entry (manager block)
   int target_units;
-  int tile_m;  // query rows per prefill unit (256 on the tcgen05 path, 64 on the mma.sync path)
+  int tile_tokens;  // query tokens per 128-row tcgen05 tile: 128 / group (whole tokens only)
   int fused_ctas;  // > 0: decode and prefill share one launch of this many CTAs (one per SM)
   int decode_warps_per_cta;  // decode warps per CTA in the launch that runs decode units
   float scale_log2;
@@ -165,7 +165,6 @@ struct AttnSetup {
   AttnArgs a;
   PageGeom g;
   int head_dim, num_kv_heads;
-  bool use_tc;  // decode and prefill units in one tcgen05 launch
   const void* k_cache;
   const void* v_cache;
   long long num_slots;
@@ -181,14 +180,9 @@ rb_status attn_setup(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
                      int32_t* d_error_word, AttnSetup* su);
 // Encodes the TMA descriptors of a set-up call.
 rb_status attn_encode_maps(AttnSetup* su);
-// Enqueues what follows the planner: the fused launch, or the decode and prefill launches.
+// Enqueues what follows the planner: the fused decode + prefill launch.
 rb_status attn_main(const AttnSetup& su, cudaStream_t s);
 
-rb_status launch_decode(const AttnArgs& a, int head_dim, const CUtensorMap& kmap,
-                        const CUtensorMap& vmap, cudaStream_t s);
-rb_status launch_prefill(const AttnArgs& a, int head_dim, const CUtensorMap& kmap,
-                         const CUtensorMap& vmap, cudaStream_t s);
-bool prefill_tc_supported(int head_dim, int group);
 rb_status launch_prefill_tc(const AttnArgs& a, int head_dim, const CUtensorMap& qmap,
                             const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t s);
 

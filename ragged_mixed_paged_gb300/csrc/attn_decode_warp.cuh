@@ -1,5 +1,21 @@
-// Split-KV decode warp shared by the standalone decode kernel and the fused attention kernel.
-// Not part of the C ABI.
+// Split-KV decode warp of the fused attention kernel (its decode units).  Not part of the C ABI.
+//
+// Work unit = (request, kv head, split of pages); one warp per unit, units pulled from an atomic
+// counter (or handed out statically to decode-first CTAs).  Each warp owns a ring of
+// shared-memory stages; lane 0 issues TMA loads (3-D tensor map, one {64 dims x 16 slots} box
+// per 128-byte half of a page, 128B swizzle) and the warp waits on the stage's mbarrier with a
+// bounded wait.
+//
+// The contraction runs transposed so a 16-token page is one MMA tile:
+//   S^T[16 keys, 8 cols] = K[16, hd] . Q^T[hd, 8]     cols = (query token, head of the group)
+//   O^T[hd, 8 cols]     += V^T[hd, 16] . P^T[16, 8]
+// with mma.sync m16n8k16 (bf16 in, fp32 accumulate): its contraction per page is 16 keys by at
+// most 8 columns, far below a tcgen05 tile, and the unit is bound by HBM, not by the tensor
+// pipe.  P^T's fragments come from S^T's with a register transpose (movmatrix), so each page
+// costs 2 x hd/16 MMAs and every K/V byte is read once per kv head, shared by the whole
+// query-head group.  Softmax statistics are per column, reduced with warp shuffles; a unit with
+// several splits leaves (m, l, o) partials and the last split of its (request, kv head) to
+// finish merges them; a single-split unit writes the normalised bf16 output directly.
 #pragma once
 
 #include "attn_common.cuh"
@@ -9,13 +25,11 @@ namespace attn {
 
 template <int HD>
 struct DecCfg {
-  static constexpr int kWarps = 4;   // per CTA of the standalone decode kernel
   static constexpr int kStages = 3;  // per warp
   static constexpr int kBoxes = HD / 64;                 // 128-byte halves of a token row
   static constexpr int kBoxBytes = kPage * 128;          // one TMA box: 16 rows x 128 bytes
   static constexpr int kPageBytes = kBoxes * kBoxBytes;  // one page of one kv head (K or V)
   static constexpr int kStageBytes = 2 * kPageBytes;
-  static constexpr int kSmemBytes = kWarps * kStages * kStageBytes + 1024;
   static constexpr int kKS = HD / 16;
 };
 

@@ -65,12 +65,18 @@ __device__ __forceinline__ ReqInfo req_info(const AttnArgs& a, const ReqSrc& src
   return x;
 }
 
-// Key tiles (128 keys) of tcgen05 prefill unit `pair` (query rows [256 pair, 256 pair + 256)
-// of a request with c cached tokens and q new ones): the larger of its two 128-row tiles.
-__device__ __forceinline__ int pair_key_tiles(int c, int q, int group, int pair) {
-  const int rows = q * group, row0 = pair * 256;
-  const int last_row = min(row0 + (row0 + 128 < rows ? 256 : 128), rows) - 1;
-  return (c + last_row / group + 1 + 127) / 128;
+// Query-token pairs of tiles a prefill request of q tokens is cut into (tile_tokens tokens per
+// 128-row tile, two tiles per unit).
+__device__ __forceinline__ int prefill_pairs(int q, int tile_tokens) {
+  return (q + 2 * tile_tokens - 1) / (2 * tile_tokens);
+}
+
+// Key tiles (128 keys) of tcgen05 prefill unit `pair` (query tokens [2 T pair, 2 T pair + 2 T)
+// of a request with c cached tokens and q new ones, T = tile_tokens): the tiles its last query
+// token sees, the larger of its two tiles' counts.
+__device__ __forceinline__ int pair_key_tiles(int c, int q, int tile_tokens, int pair) {
+  const int last_tok = min((pair + 1) * 2 * tile_tokens, q) - 1;
+  return (c + last_tok + 1 + 127) / 128;
 }
 
 // Finish-time model of the fused launch (microseconds, this GPU, cold caches; fitted to per-unit
@@ -134,7 +140,7 @@ __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim, ReqSr
   auto units_of = [&](const ReqInfo& x, int* d, int* p) {
     if (!x.ok || x.q == 0) return;
     if (is_decode_class(x.q, a.group)) *d += (x.pages + sp - 1) / sp * a.nkv;
-    else *p += (x.q * a.group + a.tile_m - 1) / a.tile_m * a.nkv;
+    else *p += prefill_pairs(x.q, a.tile_tokens) * a.nkv;
   };
   int my_d = 0, my_p = 0;
   each([&](int, const ReqInfo& x) { units_of(x, &my_d, &my_p); });
@@ -156,7 +162,7 @@ __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim, ReqSr
   auto warp_pairs = [&](auto&& body) {  // body(r, c, q, pair) for every pair, warp-cooperative
     auto one = [&](int r, const ReqInfo& x, bool has) {
       const bool pre = has && x.ok && x.q > 0 && !is_decode_class(x.q, a.group);
-      const int pairs = pre ? (x.q * a.group + 255) / 256 : 0;
+      const int pairs = pre ? prefill_pairs(x.q, a.tile_tokens) : 0;
       unsigned m = __ballot_sync(0xffffffffu, pairs > 0);
       while (m) {
         const int src = __ffs(m) - 1;
@@ -184,7 +190,7 @@ __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim, ReqSr
     float my_us = 0.f;
     int my_max = 0;
     warp_pairs([&](int, int c, int q, int p) {
-      const int n = pair_key_tiles(c, q, a.group, p);
+      const int n = pair_key_tiles(c, q, a.tile_tokens, p);
       atomicAdd(&s_bin[min(n, kTileBins - 1)], 1);
       my_us += kPreUnitUs + kPreTileUs * n;
       my_max = max(my_max, n);
@@ -215,7 +221,7 @@ __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim, ReqSr
     }
     __syncthreads();
     warp_pairs([&](int r, int c, int q, int p) {
-      const int n = pair_key_tiles(c, q, a.group, p);
+      const int n = pair_key_tiles(c, q, a.tile_tokens, p);
       a.pre_list[atomicAdd(&s_bin[min(n, kTileBins - 1)], 1)] = r * 65536 + p;
     });
   }

@@ -6,12 +6,13 @@
 //
 // Prefill unit = (request, kv head, pair of 128-row query tiles A and B); rows are (query token,
 // head of the group) pairs, token-major, so every K/V tile serves the whole query-head group
-// and both tiles of the pair.  One CTA per SM (persistent; units pulled from an atomic
+// and both tiles of the pair.  A tile holds T = 128 / group whole tokens (T * group rows; for a
+// group that does not divide 128 the last rows hold no query and are masked out).  One CTA per SM (persistent; units pulled from an atomic
 // counter, the most expensive pair of each request first), 12 warps with fixed roles (the
 // single-thread MMA issuer is warp 0, the oldest warp of its SM sub-partition, which shares that
 // scheduler with one softmax warp of each tile):
 //   warp 1     TMA producer: fetches units into a 4-entry ring, loads Q_A and Q_B once per unit
-//              (3-D boxes {64 dims, group heads, 128/group tokens}) and each 128-key K and V
+//              (3-D boxes {64 dims, group heads, T tokens}) and each 128-key K and V
 //              tile (8 pages x 128-byte boxes, 128B swizzle, one page per lane) into a 3-stage
 //              K ring and a 2-stage V ring, V one tile behind K (K is freed once S is done);
 //   warp 0     allocates all 512 TMEM columns (S_A, S_B, O_A, O_B); one thread issues the MMAs
@@ -72,11 +73,12 @@ struct TcCfg {
   __device__ static constexpr uint32_t col_o(int x) { return kColO0 + static_cast<uint32_t>(HD) * x; }
 };
 
-// A unit of work.  In a cascade prefix pass `r` holds the unit's prefix key range (the pages
-// are row 0's), key indices are relative to the range's first key and no row is masked
-// causally: every row sees keys [0, c].
+// A unit of work: query tokens [tok0, tok0 + 2T) of the request's q (tile A the first T, tile
+// B the next T), T = tile_tokens.  In a cascade prefix pass `r` holds the unit's prefix key
+// range (the pages are row 0's), the tokens are the whole batch's, key indices are relative to
+// the range's first key and no row is masked causally: every row sees keys [0, c].
 struct TcUnit {
-  int r, h, row0, t0, q, L, c, rows_total, n[2], n_kt, pages, valid;
+  int r, h, tok0, t0, q, L, c, n[2], n_kt, pages, valid;
 };
 
 // First page of a unit's keys and the page-table row they are read from.
@@ -129,24 +131,24 @@ constexpr int kKeysPerTile = 128;  // keys per K/V tile
 
 __device__ __forceinline__ TcUnit decode_unit(const AttnArgs& a, int u) {
   TcUnit un{};
+  const int T = a.tile_tokens;
   if (a.cascade == kPrefixPass) {
-    // (key range, kv head, 256 query rows of the whole batch) against one range of the shared
+    // (key range, kv head, 2T query tokens of the whole batch) against one range of the shared
     // keys [0, P) of row 0; key indices are relative to the range's first key
-    const int per_split = a.nkv * ((a.N * a.group + 255) / 256);
+    const int per_split = a.nkv * ((a.N + 2 * T - 1) / (2 * T));
     const int split = u / per_split, rem = u - split * per_split;
     const int k0 = split * a.prefix_split_keys;
     const int k1 = min(a.prefix_len, k0 + a.prefix_split_keys);
     un.r = split;
     un.h = rem % a.nkv;
-    un.row0 = (rem / a.nkv) * 256;
+    un.tok0 = (rem / a.nkv) * 2 * T;
     un.t0 = 0;
     un.q = a.N;
     un.L = k1 - k0;
     un.c = un.L - 1;
-    un.rows_total = a.N * a.group;
     const int nk = (un.L + kKeysPerTile - 1) / kKeysPerTile;
     un.n[0] = nk;
-    un.n[1] = un.row0 + 128 < un.rows_total ? nk : 0;
+    un.n[1] = un.tok0 + T < un.q ? nk : 0;
     un.n_kt = nk;
     un.pages = (un.L + kPage - 1) / kPage;
     un.valid = 1;
@@ -162,12 +164,9 @@ __device__ __forceinline__ TcUnit decode_unit(const AttnArgs& a, int u) {
   un.q = a.qsl[r + 1] - un.t0;
   un.L = a.seq_lens[r];
   un.c = un.L - un.q;
-  un.rows_total = un.q * a.group;
-  un.row0 = pair * 256;
-  un.n[0] = tiles_for(un.c, (min(un.row0 + 128, un.rows_total) - 1) / a.group);
-  un.n[1] = un.row0 + 128 < un.rows_total
-                ? tiles_for(un.c, (min(un.row0 + 256, un.rows_total) - 1) / a.group)
-                : 0;
+  un.tok0 = pair * 2 * T;
+  un.n[0] = tiles_for(un.c, min(un.tok0 + T, un.q) - 1);
+  un.n[1] = un.tok0 + T < un.q ? tiles_for(un.c, min(un.tok0 + 2 * T, un.q) - 1) : 0;
   un.n_kt = max(un.n[0], un.n[1]);
   un.pages = (un.L + kPage - 1) / kPage;
   un.valid = 1;
@@ -205,14 +204,15 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
     if (!un.valid) break;
     if (!lane0_wait(&sh.q_empty, (k & 1) ^ 1)) break;
     if (lane == 0) {
+      // one box per 64-dim half of a tile: T tokens x group heads = T * group rows of 128 bytes
       const int nq = un.n[1] > 0 ? 2 : 1;
-      mbar_arrive_expect_tx(&sh.q_full, nq * C::kQBytes);
+      mbar_arrive_expect_tx(&sh.q_full, nq * C::kHalves * a.tile_tokens * a.group * 128);
       ++q_armed;
       for (int x = 0; x < nq; ++x)
 #pragma unroll
         for (int hf = 0; hf < C::kHalves; ++hf)
           tma_load_3d(smem_base + C::kQOffset + x * C::kQBytes + hf * C::kQHalfBytes, qmap,
-                      &sh.q_full, hf * 64, un.h * a.group, un.t0 + (un.row0 + 128 * x) / a.group);
+                      &sh.q_full, hf * 64, un.h * a.group, un.t0 + un.tok0 + a.tile_tokens * x);
     }
     const int32_t* bt_row =
         a.block_table + static_cast<size_t>(unit_table_row(a, un)) * a.MB;
@@ -438,14 +438,19 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
     const TcUnit un = sh.units[slot];
     if (!un.valid) break;
     const int n = un.n[x];
-    const int row0 = un.row0 + 128 * x;
-    const int row = row0 + t;
-    const bool valid = row < un.rows_total;
-    const int jt = valid ? row / a.group : 0;
-    const int hh = valid ? row - jt * a.group : 0;
+    // row t of this tile: token tok_base + t / group, head t % group of the kv head's group;
+    // rows past T * group (a group that does not divide 128) or past the last token hold no
+    // query: every key is masked for them and they are never stored
+    const int tok_base = un.tok0 + a.tile_tokens * x;
+    const int rows_used = a.tile_tokens * a.group;
+    const int jt_in = t / a.group;
+    const bool valid = t < rows_used && tok_base + jt_in < un.q;
+    const int jt = valid ? tok_base + jt_in : 0;
+    const int hh = valid ? t - jt_in * a.group : 0;
     const bool causal = a.cascade != kPrefixPass;
-    const int lim = causal ? un.c + jt : un.c;
-    const int lim_min = causal ? un.c + row0 / a.group : un.c;
+    const int lim = !valid ? -1 : (causal ? un.c + jt : un.c);
+    const int lim_min = causal ? un.c + tok_base : un.c;
+    const bool partial = rows_used < C::kM || tok_base + a.tile_tokens > un.q;
     float m_ref = -INFINITY, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
@@ -469,7 +474,7 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
         }
       }
       const int kv_base = j * C::kN;
-      if (kv_base + C::kN - 1 > lim_min) {
+      if (partial || kv_base + C::kN - 1 > lim_min) {
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = (kv_base + i <= lim) ? s[i] : -INFINITY;
       }
@@ -744,11 +749,6 @@ rb_status launch_hd(const AttnArgs& a, const CUtensorMap& qmap, const CUtensorMa
 }
 
 }  // namespace
-
-bool prefill_tc_supported(int head_dim, int group) {
-  return (head_dim == 64 || head_dim == 128) &&
-         (group == 1 || group == 2 || group == 4 || group == 8 || group == 16);
-}
 
 rb_status launch_prefill_tc(const AttnArgs& a, int head_dim, const CUtensorMap& qmap,
                             const CUtensorMap& kmap, const CUtensorMap& vmap, cudaStream_t s) {

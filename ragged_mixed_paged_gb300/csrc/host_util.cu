@@ -77,7 +77,7 @@ bool encode_kv_tensor_map(CUtensorMap* map, const void* base, int head_dim, int 
 bool encode_q_tensor_map(CUtensorMap* map, const void* base, int head_dim, int num_q_heads,
                          long long num_tokens, int group) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (enc == nullptr || group < 1 || 128 % group != 0) return false;
+  if (enc == nullptr || group < 1 || group > 128) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim),
                               static_cast<cuuint64_t>(num_q_heads),
                               static_cast<cuuint64_t>(num_tokens)};

@@ -55,7 +55,8 @@ __host__ __device__ inline bool aligned16(const void* p) {
 bool encode_kv_tensor_map(CUtensorMap* map, const void* base, int head_dim, int num_kv_heads,
                           long long num_slots);
 // 3-D TMA descriptor over queries [num_tokens, nh, hd] bf16 with a box of {64 dims, `group`
-// heads, 128/group tokens} and 128-byte swizzle: one box = 128 (token, head) rows x 128 bytes.
+// heads, 128 / group (rounded down) tokens} and 128-byte swizzle: one box = up to 128 (token,
+// head) rows x 128 bytes.
 bool encode_q_tensor_map(CUtensorMap* map, const void* base, int head_dim, int num_q_heads,
                          long long num_tokens, int group);
 

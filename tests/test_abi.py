@@ -217,7 +217,7 @@ def test_cascade_attention_host_checks(lib):
     assert call(d, 8) == 1                                  # not a whole page
     assert call(d, 16 * 257) == 1                           # more entries than a row has
     assert call(d, -16) == 1
-    assert call(_dims(lib, num_q_heads=24), 16) == 5        # group 3: no tcgen05 path
+    assert call(_dims(lib, num_q_heads=64, num_kv_heads=2), 16) == 5   # group 32
     r2 = _dims(lib, kernel_blocks_per_manager_block=2)
     assert call(r2, 16) == 1                                # half a manager block
     need = L.rb_paged_attention_cascade_workspace_size(ctypes.byref(d), 2, 4)

@@ -43,9 +43,12 @@ def test_long_context_sampled(rb):
     _case(rb, spec, rows=sample_rows(spec, n_random=96, seed=5))
 
 
-@pytest.mark.parametrize("seed", range(32))
+@pytest.mark.parametrize("seed", range(48))
 def test_fuzzed_mixes(rb, seed):
-    nh, nkv = [(4, 4), (4, 2), (8, 2), (16, 2), (32, 8), (16, 1), (6, 2), (12, 2)][seed % 8]
+    """Head groups 1-16, powers of two and not (a 128-row tile then holds 128 // group whole
+    tokens and masks its last rows)."""
+    nh, nkv = [(4, 4), (4, 2), (8, 2), (16, 2), (32, 8), (16, 1), (6, 2), (12, 2), (28, 4),
+               (10, 1), (14, 2), (15, 1)][seed % 12]
     hd = 64 if seed % 2 else 128
     spec = wl.random_batch(seed, num_q_heads=nh, num_kv_heads=nkv, head_dim=hd, max_reqs=7,
                            max_q=150, max_c=400, pad_tokens=seed % 4, decode_frac=0.5)
@@ -56,7 +59,7 @@ def test_fuzzed_mixes(rb, seed):
                                  (9, 40), (63, 1), (64, 0), (65, 64), (200, 0), (1, 1000)])
 def test_edge_lengths(rb, q, c):
     """Page and tile edges: sequence lengths at and around multiples of 16 and 64."""
-    for nh, nkv in ((8, 1), (4, 2), (8, 8)):
+    for nh, nkv in ((8, 1), (4, 2), (8, 8), (6, 2), (7, 1)):
         spec = wl.batch_from_lists([c, 3], [q, 1], num_q_heads=nh, num_kv_heads=nkv,
                                    head_dim=128, seed=q * 1000 + c)
         _case(rb, spec)

@@ -1,5 +1,6 @@
 """rb_paged_attention_cascade vs the one-pass float64 oracle ("8.3.2.5 Cascade Attention"):
-shared-prefix batches of decodes and chunks, several head groups, manager blocks, the prefix
+shared-prefix batches of decodes and chunks, head groups 1-10 (powers of two and not),
+manager blocks, the prefix
 length the rule allows and shorter ones; P = 0 is the plain call bit for bit; a broken
 contract sets ATTN_META."""
 import numpy as np
@@ -42,9 +43,9 @@ def _check(rb, spec, P=None, rows=None):
     return P
 
 
-@pytest.mark.parametrize("seed", range(12))
+@pytest.mark.parametrize("seed", range(16))
 def test_shared_prefix_mixes(rb, seed):
-    nh, nkv = [(32, 8), (8, 1), (4, 4), (16, 2)][seed % 4]
+    nh, nkv = [(32, 8), (8, 1), (4, 4), (16, 2), (6, 2), (12, 2), (28, 4), (10, 1)][seed % 8]
     spec = wl.shared_prefix_batch(seed, num_decodes=3 + seed, prefix_tokens=[64, 160, 512][seed % 3],
                                   suffix_range=(0, 200), num_chunks=seed % 3, chunk_q=[7, 130][seed % 2],
                                   num_q_heads=nh, num_kv_heads=nkv,

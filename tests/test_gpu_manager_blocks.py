@@ -49,9 +49,9 @@ def test_workloads_attention(rb, name, make):
 
 @pytest.mark.parametrize("seed", range(16))
 def test_fuzzed_attention(rb, seed):
-    """Both attention paths: the fused tcgen05 launch (power-of-two groups) and the separate
-    decode + mma.sync prefill launches (group 3)."""
-    nh, nkv = [(32, 8), (8, 1), (6, 2), (4, 4)][seed % 4]
+    """Manager blocks of 2 and 4 kernel pages under head groups that are powers of two and
+    not (decode units and tcgen05 prefill units both walk the expanded pages)."""
+    nh, nkv = [(32, 8), (8, 1), (6, 2), (4, 4), (12, 2), (7, 1)][seed % 6]
     spec = wl.random_batch(seed, num_q_heads=nh, num_kv_heads=nkv, head_dim=128 if seed % 2 else 64,
                            manager_ratio=[2, 4][seed % 2], max_reqs=6, max_q=140, max_c=500,
                            decode_frac=0.5)

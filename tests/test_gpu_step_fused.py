@@ -69,8 +69,9 @@ def test_fused_step_equals_four_calls(rb, name):
 
 @pytest.mark.parametrize("seed", range(16))
 def test_fused_step_fuzz(rb, seed):
-    """Both attention paths (power-of-two groups fused, group 3 in two launches), padding."""
-    nh, nkv = [(32, 8), (6, 2), (8, 1), (4, 4)][seed % 4]
+    """Head groups that are powers of two and not, head_dim 64 and 128, padding, manager
+    blocks."""
+    nh, nkv = [(32, 8), (6, 2), (8, 1), (4, 4), (28, 4), (12, 1)][seed % 6]
     spec = wl.random_batch(seed, num_q_heads=nh, num_kv_heads=nkv, head_dim=[64, 128][seed % 2],
                            max_reqs=9, max_q=150, max_c=300, pad_tokens=seed % 5,
                            pad_reqs=seed % 3, manager_ratio=[1, 2, 4, 1][seed % 4])

@@ -211,17 +211,19 @@ def config3(step: int = 0, num_real: int = 256, manager_ratio: int = 1) -> Batch
                        4096, seed, num_reqs_padded=256, num_tokens_padded=256)
 
 
-def config5(step: int = 0, pool_gb: float = 0.0) -> BatchSpec:
+def config5(step: int = 0, pool_gb: float = 0.0, context_scale: float = 1.0) -> BatchSpec:
     """Long context: 8 decodes at 131072 cached + one 4096-token chunk with 65536 cached.
 
     64 q heads / 8 kv heads, head_dim 128, block_size 16.  One layer of the KV cache is
     materialised; ``pool_gb`` > 0 spreads the pages over a larger pool of that many GB (K+V).
+    ``context_scale`` < 1 shrinks every cached length by that factor (a smaller case of the
+    same shape, e.g. for a profiler).
     """
     seed = 1000 * 5 + step
     rng = np.random.default_rng(seed)
-    computed = [131072] * 8 + [65536]
+    computed = [int(131072 * context_scale)] * 8 + [int(65536 * context_scale)]
     scheduled = [1] * 8 + [4096]
-    M = 131072 + 16
+    M = _round_up(max(c + q for c, q in zip(computed, scheduled)), 16) + 16
     nb = _pool_blocks_for(computed, scheduled, 16)
     if pool_gb > 0:
         page_bytes = 2 * 16 * 8 * 128 * 2
