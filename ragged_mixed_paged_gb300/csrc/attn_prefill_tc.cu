@@ -478,14 +478,20 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = (kv_base + i <= lim) ? s[i] : -INFINITY;
       }
+      // row maximum: eight running maxima over the 16 groups of 8 columns, three-input max
+      // instructions (two columns per instruction)
       float mx[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx[i] = s[i];
+      for (int k = 0; k < 8; ++k) mx[k] = fmax3(s[k], s[8 + k], s[16 + k]);
 #pragma unroll
-      for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], s[i]);
+      for (int g = 3; g + 1 < 16; g += 2)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[8 * g + k], s[8 * g + 8 + k]);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], s[120 + k]);
       // scores are scaled inside the exponent: max and mask commute with a positive scale
-      const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) *
+      const float m_tile = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                 fmaxf(mx[6], mx[7])) *
                            a.scale_log2;
       const bool need = m_tile > m_ref + 8.f;
       if (__any_sync(0xffffffffu, need)) {
@@ -524,17 +530,22 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
         }
       }
       const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-      const float sc = a.scale_log2;
-      float rs[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      // exponents and the row sum two columns at a time with the paired fp32 FMA / add
+      // instructions, so the softmax issues about two thirds of the instructions it would with
+      // scalar ones and stays inside the MMA work of the other tile
+      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nmu2 = make_float2(-mu, -mu);
+      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = fast_exp2(fmaf(s[c * 32 + 2 * i], sc, -mu));
-          const float p1 = fast_exp2(fmaf(s[c * 32 + 2 * i + 1], sc, -mu));
-          rs[i & 7] += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          const float2 e = __ffma2_rn(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sc2,
+                                      nmu2);
+          const float2 p = make_float2(fast_exp2(e.x), fast_exp2(e.y));
+          rs[i & 3] = __fadd2_rn(rs[i & 3], p);
+          pk[i] = pack_bf16x2(p.x, p.y);
         }
         tc::st16(col_s + c * 16, pk);
       }
@@ -543,7 +554,9 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
       // MMA after it) has landed
       tc::fence_before_sync();
       arrive_warp(&sh.p_full[x]);
-      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+      const float2 rs01 = __fadd2_rn(rs[0], rs[1]), rs23 = __fadd2_rn(rs[2], rs[3]);
+      const float2 rsum = __fadd2_rn(rs01, rs23);
+      l += rsum.x + rsum.y;
     }
     if (!ok) break;
     itk += un.n_kt;

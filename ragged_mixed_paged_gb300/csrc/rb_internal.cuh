@@ -223,6 +223,13 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// max(a, b, c) in one instruction (PTX three-input max.f32; a NaN input is ignored like fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float y;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+  return y;
+}
+
 // 2^x on the SFU (PTX ex2.approx.ftz.f32).
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
