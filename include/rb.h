@@ -104,6 +104,19 @@ const char* rb_status_string(int32_t status);
 uint64_t rb_kernel_launch_count(void);
 
 /*
+ * rb_debug_attention_wait_limit — test hook of the attention launch's bounded waits; the pages
+ * have no counterpart.  Every wait of the fused attention launch on an asynchronous copy, an
+ * MMA or another role gives up after `wait_limit_ns` (default 1 s; 0 restores it), sets
+ * RB_EBIT_TIMEOUT, lets the copies and MMAs it already issued complete, frees its tensor memory
+ * and returns.  With `withhold_first_unit` = 1 the producer of CTA 0 stops before handing its
+ * first prefill unit to the other roles (no copy or MMA of that unit is ever issued), so their
+ * waits for it run out: a test of the timeout path that faults nothing.  Process-wide, read at
+ * each attention call's set-up; not for production use.  RB_ERR_INVALID_ARG for a limit
+ * outside [100 us, 10 s] (other than 0) or a flag other than 0 / 1.
+ */
+rb_status rb_debug_attention_wait_limit(uint64_t wait_limit_ns, int32_t withhold_first_unit);
+
+/*
  * rb_pad_for_graph — host function; smallest entry of `capture_sizes` (sorted ascending,
  * `num_sizes` entries) that is >= num_tokens; num_tokens itself when it exceeds the largest size
  * (the step then runs unpadded), and -1 for invalid arguments (null sizes with num_sizes > 0,

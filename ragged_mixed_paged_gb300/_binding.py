@@ -96,6 +96,7 @@ def _load():
     sig = {
         "rb_status_string": (ctypes.c_char_p, [I32]),
         "rb_kernel_launch_count": (ctypes.c_uint64, []),
+        "rb_debug_attention_wait_limit": (I32, [ctypes.c_uint64, I32]),
         "rb_pad_for_graph": (I32, [P, I32, I32]),
         "rb_prepare_inputs": (I32, [PD, I32, I32, I32, I32, P, P, P, P, P, P, P, P, P, P, P, P,
                                     P, P, P]),

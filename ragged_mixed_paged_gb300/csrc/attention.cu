@@ -145,6 +145,7 @@ rb_status attn_setup(const rb_dims* dims, int32_t num_reqs, int32_t num_tokens,
   a.decode_warps_per_cta = 8;
   a.scale_log2 = softmax_scale * 1.4426950408889634f;
   a.err = d_error_word;
+  debug_wait_settings(&a.wait_limit_ns, &a.withhold_first_unit);
   return RB_OK;
 }
 

@@ -116,7 +116,15 @@ struct AttnArgs {
   int prefix_split_keys;  // keys per range (a multiple of 128)
   float* pre_o;       // [splits, N, nh, HD] prefix-pass outputs per key range, normalised
   float* pre_lse;     // [splits, N, nh] their log-sum-exp (log2 units of the scaled scores)
+  // limit of the fused launch's bounded waits, and (tests only) CTA 0's producer withholding
+  // the arrival of its first prefill unit so that the waits for it run out
+  unsigned long long wait_limit_ns;
+  int withhold_first_unit;
 };
+
+// Test hook behind rb_debug_attention_wait_limit: the wait limit and withhold flag of every
+// later attention call (process-wide).
+void debug_wait_settings(unsigned long long* limit_ns, int* withhold);
 
 // Weights that merge a suffix-pass row (accumulator relative to running max m, sum l; log2
 // units) with the prefix-pass rows of the same (token, head) (one per key range: log-sum-exp

@@ -103,13 +103,12 @@ struct TcShared {
   int role_rank;  // order in which this CTA took its role: decode-first CTAs are ranks 0..D-1
 };
 
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
-
-// Bounded wait that also gives up as soon as another role has aborted.  `Relaxed`: for the
-// MMA issuer (see mma_issuer).
+// Bounded wait (a.wait_limit_ns, 1 s unless a test shortened it) that also gives up as soon as
+// another role has aborted.  `Relaxed`: for the MMA issuer (see mma_issuer).
 template <bool Relaxed = false>
 __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t phase, volatile int* abort,
-                                        int32_t* err) {
+                                        const AttnArgs& a) {
+  int32_t* err = a.err;
   auto test = [&]() { return Relaxed ? mbar_try_wait_relaxed(bar, phase) : mbar_try_wait(bar, phase); };
 #pragma unroll 1
   for (int i = 0; i < 128; ++i)
@@ -119,7 +118,7 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t phase, volatile 
   while (true) {
     if (test()) return true;
     if (*abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > a.wait_limit_ns) {
       if (atomicExch(const_cast<int*>(abort), 1) == 0) raise_error(err, RB_EBIT_TIMEOUT);
       return false;
     }
@@ -186,19 +185,24 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
   uint32_t it = 0, q_armed = 0, k_armed[3] = {0, 0, 0}, v_armed[2] = {0, 0};
   auto lane0_wait = [&](uint64_t* bar, uint32_t phase) -> bool {
     int ok = 1;
-    if (lane == 0) ok = tc_wait(bar, phase, abort, a.err) ? 1 : 0;
+    if (lane == 0) ok = tc_wait(bar, phase, abort, a) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
   for (int k = 0;; ++k) {
     const int slot = k % C::kRing;
     if (!lane0_wait(&sh.unit_empty[slot], ((k / C::kRing) & 1) ^ 1)) break;
+    int withhold = 0;
     if (lane == 0) {
       const int u = atomicAdd(a.header + kHPrefillNext, 1);
       TcUnit un{};
       if (u < n_units) un = decode_unit(a, u);
       sh.units[slot] = un;
-      tc::mbar_arrive(&sh.unit_full[slot]);
+      // test hook: CTA 0 stops before its first unit reaches the other roles, so their waits
+      // for it run out while nothing of that unit has been issued
+      withhold = a.withhold_first_unit && blockIdx.x == 0 && k == 0 && un.valid;
+      if (!withhold) tc::mbar_arrive(&sh.unit_full[slot]);
     }
+    if (__shfl_sync(0xffffffffu, withhold, 0)) break;
     __syncwarp();
     const TcUnit un = sh.units[slot];
     if (!un.valid) break;
@@ -304,7 +308,7 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
   // acquiring try_wait behind queued MMAs left the tensor pipe idle ~140 cycles per wait on this
   // GPU, a relaxed one costs nothing.  The unit descriptor is plain shared memory written by the
   // producer warp: its barrier keeps the acquiring wait.
-  auto wait = [&](uint64_t* bar, uint32_t phase) { return tc_wait<true>(bar, phase, abort, a.err); };
+  auto wait = [&](uint64_t* bar, uint32_t phase) { return tc_wait<true>(bar, phase, abort, a); };
   // A wait whose result decides a branch costs the issuing thread a few hundred cycles even when
   // the phase is long complete; so every barrier of one step is first tested at once (the tests
   // issue back to back, one branch on their conjunction) and only a step that finds one not yet
@@ -350,7 +354,7 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
   };
   for (int k = 0;; ++k) {
     const int slot = k % C::kRing;
-    if (!tc_wait(&sh.unit_full[slot], (k / C::kRing) & 1, abort, a.err)) break;
+    if (!tc_wait(&sh.unit_full[slot], (k / C::kRing) & 1, abort, a)) break;
     const TcUnit un = sh.units[slot];
     if (!un.valid) break;
     const bool q_k = test(&sh.q_full, k & 1) & test(&sh.k_full[itk % C::kStagesK], (itk / C::kStagesK) & 1);
@@ -420,7 +424,7 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
   const uint32_t col_s = tmem + lane_off + C::col_s(x), col_o = tmem + lane_off + C::col_o(x);
   uint32_t tc_x = 0, itk = 0, uc_x = 0;  // S tiles, K/V tiles and units (with n > 0) of this side
   auto wait_all = [&](uint64_t* bar, uint32_t phase) -> bool {
-    const bool ok = tc_wait(bar, phase, abort, a.err);
+    const bool ok = tc_wait(bar, phase, abort, a);
     return !__any_sync(0xffffffffu, !ok);
   };
   // One lane of each warp arrives for the warp: 128 arrivals on one barrier load the barrier

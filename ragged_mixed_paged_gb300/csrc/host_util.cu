@@ -11,7 +11,19 @@ namespace rb {
 
 static std::atomic<uint64_t> g_launches{0};
 
+// rb_debug_attention_wait_limit's settings (defaults: 1 s, nothing withheld)
+constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
+static std::atomic<unsigned long long> g_wait_limit_ns{kDefaultWaitLimitNs};
+static std::atomic<int> g_withhold{0};
+
 void note_launches(int n) { g_launches.fetch_add(static_cast<uint64_t>(n)); }
+
+namespace attn {
+void debug_wait_settings(unsigned long long* limit_ns, int* withhold) {
+  *limit_ns = g_wait_limit_ns.load();
+  *withhold = g_withhold.load();
+}
+}  // namespace attn
 
 int device_sm_count() {
   static std::mutex mu;
@@ -108,6 +120,15 @@ const char* rb_status_string(int32_t status) {
 }
 
 uint64_t rb_kernel_launch_count(void) { return rb::g_launches.load(); }
+
+rb_status rb_debug_attention_wait_limit(uint64_t wait_limit_ns, int32_t withhold_first_unit) {
+  if (withhold_first_unit < 0 || withhold_first_unit > 1) return RB_ERR_INVALID_ARG;
+  if (wait_limit_ns != 0 && (wait_limit_ns < 100000ull || wait_limit_ns > 10000000000ull))
+    return RB_ERR_INVALID_ARG;
+  rb::g_wait_limit_ns.store(wait_limit_ns == 0 ? rb::kDefaultWaitLimitNs : wait_limit_ns);
+  rb::g_withhold.store(withhold_first_unit);
+  return RB_OK;
+}
 
 int32_t rb_pad_for_graph(const int32_t* capture_sizes, int32_t num_sizes, int32_t num_tokens) {
   if (num_sizes < 0 || num_tokens < 0 || (num_sizes > 0 && capture_sizes == nullptr)) return -1;

@@ -265,3 +265,14 @@ def test_step_host_copy_checks(lib):
     assert L.rb_step_host(ctypes.byref(args), none, 0, two, 2, None) == 1
     two[1] = lib.rb_host_copy(None, None, 0)                 # empty copies need no pointers
     assert L.rb_step_host(ctypes.byref(args), two, 2, two, 2, None) == 1      # no metadata buffers
+
+
+def test_wait_limit_hook_checks(lib):
+    """The attention wait-limit test hook rejects out-of-range settings and restores defaults
+    (host state only; no launch)."""
+    L = lib.lib
+    assert L.rb_debug_attention_wait_limit(10, 0) == 1             # below 100 us
+    assert L.rb_debug_attention_wait_limit(20_000_000_000, 0) == 1  # above 10 s
+    assert L.rb_debug_attention_wait_limit(0, 2) == 1
+    assert L.rb_debug_attention_wait_limit(5_000_000, 1) == 0
+    assert L.rb_debug_attention_wait_limit(0, 0) == 0               # back to the defaults
