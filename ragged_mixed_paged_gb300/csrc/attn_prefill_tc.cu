@@ -21,10 +21,12 @@
 //              O += P V:  M=128, N=hd,  K=128, P read from TMEM, V MN-major in shared memory;
 //              so one tile's softmax runs while the tensor core works on the other tile;
 //   warps 4-7  softmax of tile A, warps 8-11 softmax of tile B; thread t = query row t: reads its
-//              S row from TMEM, masks causally, keeps a running max and sum in the log2
-//              domain, writes P (bf16) back over the S columns, and rescales its O row in TMEM
-//              only when the max grows by more than 2^8 (exact either way: P and the sum share
-//              the same reference).  The epilogue reads O, divides by the sum, stores bf16 rows.
+//              S row from TMEM, masks causally, takes exponents against a running reference
+//              (log2 domain) and keeps their sum, writes P (bf16) back over the S columns.  The
+//              reference is the row's first-tile maximum and moves (O rescaled in TMEM, the
+//              tile's exponents taken again) only when a tile's sum exceeds 2^20 (exact either
+//              way: P and the sum share the reference), so a common tile takes no row maximum.
+//              The epilogue reads O, divides by the sum, stores bf16 rows.
 // All mbarrier waits are bounded; a timeout sets RB_EBIT_TIMEOUT, every role stops, in-flight
 // copies and MMAs are drained with bounded waits and TMEM is freed before the CTA exits.
 #include "attn_common.cuh"
@@ -92,7 +94,8 @@ __device__ __forceinline__ int unit_table_row(const AttnArgs& a, const TcUnit& u
 struct TcShared {
   uint64_t unit_full[4], unit_empty[4];
   uint64_t q_full, q_empty;
-  uint64_t k_full[3], k_empty[3], v_full[2], v_empty[2];
+  uint64_t k_full[TcCfg<128>::kStagesK], k_empty[TcCfg<128>::kStagesK];
+  uint64_t v_full[TcCfg<128>::kStagesV], v_empty[TcCfg<128>::kStagesV];
   uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint64_t drain;
   uint64_t dec_bars[8][DecCfg<128>::kStages];  // decode phase: one ring per warp 0..7
@@ -124,6 +127,10 @@ __device__ __forceinline__ bool tc_wait(uint64_t* bar, uint32_t phase, volatile 
     }
   }
 }
+
+// Largest sum of one tile's exponents (128 keys of one row) taken against a lagging reference:
+// P <= 2^20 keeps P V and the row sum far inside fp32 and bf16 range.
+constexpr float kSumLimit = 1048576.f;
 
 __device__ __forceinline__ int tiles_for(int c, int jmax) { return (c + jmax + 1 + 127) / 128; }
 constexpr int kKeysPerTile = 128;  // keys per K/V tile
@@ -182,7 +189,7 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
   volatile int* abort = &sh.abort;
   const int lane = threadIdx.x & 31;
   const int n_units = a.header[kHNumPrefillUnits];
-  uint32_t it = 0, q_armed = 0, k_armed[3] = {0, 0, 0}, v_armed[2] = {0, 0};
+  uint32_t it = 0, q_armed = 0, k_armed[C::kStagesK] = {}, v_armed[C::kStagesV] = {};
   auto lane0_wait = [&](uint64_t* bar, uint32_t phase) -> bool {
     int ok = 1;
     if (lane == 0) ok = tc_wait(bar, phase, abort, a) ? 1 : 0;
@@ -285,9 +292,9 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
   }
   if (lane == 0 && *abort) {  // let every copy already issued land before the CTA can exit
     if (q_armed) mbar_wait_bounded(&sh.q_full, (q_armed - 1) & 1, 100000000ull);
-    for (int b = 0; b < 3; ++b)
+    for (int b = 0; b < C::kStagesK; ++b)
       if (k_armed[b]) mbar_wait_bounded(&sh.k_full[b], (k_armed[b] - 1) & 1, 100000000ull);
-    for (int b = 0; b < 2; ++b)
+    for (int b = 0; b < C::kStagesV; ++b)
       if (v_armed[b]) mbar_wait_bounded(&sh.v_full[b], (v_armed[b] - 1) & 1, 100000000ull);
   }
 }
@@ -455,7 +462,9 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
     const int lim = !valid ? -1 : (causal ? un.c + jt : un.c);
     const int lim_min = causal ? un.c + tok_base : un.c;
     const bool partial = rows_used < C::kM || tok_base + a.tile_tokens > un.q;
-    float m_ref = -INFINITY, l = 0.f;
+    // running reference (log2 domain) and sum; a row without a query starts at 0, so that only
+    // rows with visible keys take the first tile's maximum
+    float m_ref = valid ? -INFINITY : 0.f, l = 0.f;
     bool ok = true;
     for (int j = 0; j < n; ++j) {
       const uint32_t tj = tc_x + j;
@@ -482,40 +491,49 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
 #pragma unroll
         for (int i = 0; i < 128; ++i) s[i] = (kv_base + i <= lim) ? s[i] : -INFINITY;
       }
-      // row maximum: eight running maxima over the 16 groups of 8 columns, three-input max
-      // instructions (two columns per instruction)
-      float mx[8];
+      // The exponents are taken against the running reference m_ref, not against this tile's
+      // maximum: any reference gives the same softmax, since P and the sum share it.  The row
+      // maximum is taken only (a) on the first tile of a row and (b) when the tile's sum of
+      // exponents shows the reference lagging the row's maximum by more than log2 of
+      // kSumLimit (or overflowing); then O and the sum are rescaled to the new reference and
+      // the tile's exponents are taken again.  So P <= kSumLimit always, and the common tile
+      // skips the maximum over its 128 columns.
+      auto take_tile_max = [&]() {
+        // eight running maxima over the 16 groups of 8 columns, three-input max instructions
+        float mx[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = fmax3(s[k], s[8 + k], s[16 + k]);
+        for (int k = 0; k < 8; ++k) mx[k] = fmax3(s[k], s[8 + k], s[16 + k]);
 #pragma unroll
-      for (int g = 3; g + 1 < 16; g += 2)
+        for (int g = 3; g + 1 < 16; g += 2)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[8 * g + k], s[8 * g + 8 + k]);
+          for (int k = 0; k < 8; ++k) mx[k] = fmax3(mx[k], s[8 * g + k], s[8 * g + 8 + k]);
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], s[120 + k]);
-      // scores are scaled inside the exponent: max and mask commute with a positive scale
-      const float m_tile = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
-                                 fmaxf(mx[6], mx[7])) *
-                           a.scale_log2;
-      const bool need = m_tile > m_ref + 8.f;
-      if (__any_sync(0xffffffffu, need)) {
-        const float m_new = need ? m_tile : m_ref;
-        const float alpha = fast_exp2(m_ref - m_new);
-        if (j > 0) {  // O holds P_{j-1} V_{j-1}: S_j, issued after it, has landed
-          uint32_t r[32];
+        for (int k = 0; k < 8; ++k) mx[k] = fmaxf(mx[k], s[120 + k]);
+        // scores are scaled inside the exponent: max and mask commute with a positive scale
+        const float m_tile = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]),
+                                   fmaxf(mx[6], mx[7])) *
+                             a.scale_log2;
+        const bool need = m_tile > m_ref;
+        if (__any_sync(0xffffffffu, need)) {
+          const float m_new = need ? m_tile : m_ref;
+          const float alpha = fast_exp2(m_ref - m_new);
+          if (j > 0) {  // O holds P_{j-1} V_{j-1}: S_j, issued after it, has landed
+            uint32_t r[32];
 #pragma unroll
-          for (int c = 0; c < HD / 32; ++c) {
-            tc::ld32(col_o + c * 32, r);
-            tc::wait_ld();
+            for (int c = 0; c < HD / 32; ++c) {
+              tc::ld32(col_o + c * 32, r);
+              tc::wait_ld();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
-            tc::st32(col_o + c * 32, r);
+              for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * alpha);
+              tc::st32(col_o + c * 32, r);
+            }
+            tc::wait_st();
           }
-          tc::wait_st();
+          l *= alpha;
+          m_ref = m_new;
         }
-        l *= alpha;
-        m_ref = m_new;
-      }
+      };
+      if (__any_sync(0xffffffffu, m_ref == -INFINITY)) take_tile_max();
       // keys at or past the end of the sequence may hold anything: zero their V rows (only the
       // unit's last K/V tile can reach them; tile A zeroes it when it uses that tile)
       if (kv_base + C::kN > un.L && (x == 0 || j >= un.n[0])) {
@@ -533,34 +551,42 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
           fence_proxy_async_smem();
         }
       }
-      const float mu = m_ref == -INFINITY ? 0.f : m_ref;
       // exponents and the row sum two columns at a time with the paired fp32 FMA / add
-      // instructions, so the softmax issues about two thirds of the instructions it would with
-      // scalar ones and stays inside the MMA work of the other tile
-      const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nmu2 = make_float2(-mu, -mu);
-      float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
-                      make_float2(0.f, 0.f)};
+      // instructions; P (bf16) goes over the S columns
+      auto exponents = [&]() -> float {
+        const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+        const float2 sc2 = make_float2(a.scale_log2, a.scale_log2), nmu2 = make_float2(-mu, -mu);
+        float2 rs[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t pk[16];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 e = __ffma2_rn(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]), sc2,
-                                      nmu2);
-          const float2 p = make_float2(fast_exp2(e.x), fast_exp2(e.y));
-          rs[i & 3] = __fadd2_rn(rs[i & 3], p);
-          pk[i] = pack_bf16x2(p.x, p.y);
+          for (int i = 0; i < 16; ++i) {
+            const float2 e = __ffma2_rn(make_float2(s[c * 32 + 2 * i], s[c * 32 + 2 * i + 1]),
+                                        sc2, nmu2);
+            const float2 p = make_float2(fast_exp2(e.x), fast_exp2(e.y));
+            rs[i & 3] = __fadd2_rn(rs[i & 3], p);
+            pk[i] = pack_bf16x2(p.x, p.y);
+          }
+          tc::st16(col_s + c * 16, pk);
         }
-        tc::st16(col_s + c * 16, pk);
+        const float2 rs01 = __fadd2_rn(rs[0], rs[1]), rs23 = __fadd2_rn(rs[2], rs[3]);
+        const float2 rsum = __fadd2_rn(rs01, rs23);
+        return rsum.x + rsum.y;
+      };
+      float rsum = exponents();
+      if (__any_sync(0xffffffffu, !(rsum <= kSumLimit))) {  // rare: re-reference this tile
+        tc::wait_st();
+        take_tile_max();
+        rsum = exponents();
       }
       tc::wait_st();
       // P_j overwrites the S columns P_{j-1} V_{j-1} read: that product is done, since S_j (the
       // MMA after it) has landed
       tc::fence_before_sync();
       arrive_warp(&sh.p_full[x]);
-      const float2 rs01 = __fadd2_rn(rs[0], rs[1]), rs23 = __fadd2_rn(rs[2], rs[3]);
-      const float2 rsum = __fadd2_rn(rs01, rs23);
-      l += rsum.x + rsum.y;
+      l += rsum;
     }
     if (!ok) break;
     itk += un.n_kt;
@@ -670,13 +696,15 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
     }
     mbar_init(&sh.q_full, 1);
     mbar_init(&sh.q_empty, 1);
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < C::kStagesK; ++i) {
       mbar_init(&sh.k_full[i], 1);
       mbar_init(&sh.k_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < C::kStagesV; ++i) {
       mbar_init(&sh.v_full[i], 1);
       mbar_init(&sh.v_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&sh.s_full[i], 1);
       mbar_init(&sh.p_full[i], 4);  // one lane of each softmax warp
       mbar_init(&sh.o_done[i], 1);
