@@ -11,10 +11,11 @@
 // counter, the most expensive pair of each request first), 12 warps with fixed roles (the
 // single-thread MMA issuer is warp 0, the oldest warp of its SM sub-partition, which shares that
 // scheduler with one softmax warp of each tile):
-//   warp 1     TMA producer: fetches units into a 4-entry ring, loads Q_A and Q_B once per unit
-//              (3-D boxes {64 dims, group heads, T tokens}) and each 128-key K and V
-//              tile (8 pages x 128-byte boxes, 128B swizzle, one page per lane) into a 3-stage
-//              K ring and a 2-stage V ring, V one tile behind K (K is freed once S is done);
+//   warp 1     TMA producer of units, Q and K: fetches units into a 4-entry ring, loads Q_A and
+//              Q_B once per unit (3-D boxes {64 dims, group heads, T tokens}) and each 128-key
+//              K tile (8 pages x 128-byte boxes, 128B swizzle, one page per lane) into a
+//              3-stage K ring (K is freed once S is done);
+//   warp 2     TMA producer of V: the same boxes into a 2-stage V ring;
 //   warp 0     allocates all 512 TMEM columns (S_A, S_B, O_A, O_B); one thread issues the MMAs
 //              in the order S_A(0) S_B(0) | PV_A(0) S_A(1) | PV_B(0) S_B(1) | PV_A(1) ...
 //              S = Q K^T: M=128, N=128, K=hd, both operands K-major in shared memory;
@@ -66,7 +67,8 @@ struct TcCfg {
   static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kThreads * kLaunchRegs,
                 "register split exceeds the launch allocation");
   static constexpr int kMmaWarp = 0;
-  static constexpr int kProducerWarp = 1;  // warps 2 and 3 only complete the first warpgroup
+  static constexpr int kProducerWarp = 1;   // units, Q and K
+  static constexpr int kProducerVWarp = 2;  // V (warp 3 only completes the first warpgroup)
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kColS0 = 0;                   // S_A at 0, S_B at 128
   static constexpr uint32_t kColO0 = 256;                 // O_A at 256, O_B at 256 + HD
@@ -179,20 +181,71 @@ __device__ __forceinline__ TcUnit decode_unit(const AttnArgs& a, int u) {
   return un;
 }
 
+// Page ids of a unit's K/V tiles for one warp: a 32-page window of the unit's block-table row
+// held one id per lane, the next window prefetched; lane l & 7 takes page l & 7 of a tile.
+struct PageWindow {
+  const AttnArgs& a;
+  const int32_t* bt_row;
+  int page0, pages, win, bid, bid_next, lane;
+  __device__ PageWindow(const AttnArgs& a_, const TcUnit& un, int lane_)
+      : a(a_),
+        bt_row(a_.block_table + static_cast<size_t>(unit_table_row(a_, un)) * a_.MB),
+        page0(unit_first_page(a_, un)),
+        pages(un.pages),
+        win(0),
+        lane(lane_) {
+    bid = page(lane);
+    bid_next = page(32 + lane);
+  }
+  __device__ int page(int pg) const {
+    return pg < pages ? kernel_page(bt_row, page0 + pg, a.ratio, a.num_blocks, a.null_block)
+                      : a.null_block;
+  }
+  // This lane's page id for tile j (tiles are taken in order).  Pages past the sequence read
+  // the null page (masked; V rows zeroed); an invalid id is reported when `report` and replaced
+  // by the null page.
+  __device__ int tile_page(int j, bool report) {
+    const int first = j * kKeysPerTile / kPage;
+    if (first - win >= 32) {
+      win += 32;
+      bid = bid_next;
+      bid_next = page(win + 32 + lane);
+    }
+    int id = __shfl_sync(0xffffffffu, bid, first + (lane & 7) - win);
+    const int pg = first + (lane & 7);
+    if (pg >= pages) {
+      id = a.null_block;
+    } else if (id < 0 || id >= a.num_blocks || id == a.null_block) {
+      if (report && lane < kKeysPerTile / kPage) raise_error(a.err, RB_EBIT_BLOCK_ID);
+      id = a.null_block;
+    }
+    return id;
+  }
+};
+
+// Producer of units, Q and K (warp 1, whole warp).  It takes units from the global counter
+// into the 4-entry unit ring, loads Q_A and Q_B once per unit and each K tile into the K
+// ring; lanes 0..7 each issue the boxes of one page of a tile.
 template <int HD>
-__device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
-                         const CUtensorMap* qmap, const CUtensorMap* kmap,
-                         const CUtensorMap* vmap) {
-  // The whole warp: page ids are held one per lane (a 32-page window, the next one prefetched)
-  // and lanes 0..7 each issue the boxes of one page of a tile.  V runs one tile behind K.
+__device__ void producer_qk(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
+                            const CUtensorMap* qmap, const CUtensorMap* kmap) {
   using C = TcCfg<HD>;
   volatile int* abort = &sh.abort;
   const int lane = threadIdx.x & 31;
   const int n_units = a.header[kHNumPrefillUnits];
-  uint32_t it = 0, q_armed = 0, k_armed[C::kStagesK] = {}, v_armed[C::kStagesV] = {};
+  uint32_t it = 0, q_armed = 0, k_armed[C::kStagesK] = {};
+  // the unit ring guards plain shared memory (the unit descriptors): acquiring wait
   auto lane0_wait = [&](uint64_t* bar, uint32_t phase) -> bool {
     int ok = 1;
     if (lane == 0) ok = tc_wait(bar, phase, abort, a) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  // Q and K slots are read only by tcgen05.mma and written only by TMA: a relaxed test first
+  // (an acquiring wait on a long-complete phase cost this warp a few hundred cycles per tile)
+  auto slot_wait = [&](uint64_t* bar, uint32_t phase) -> bool {
+    int ok = 1;
+    if (lane == 0)
+      ok = (mbar_test_relaxed(bar, phase) || tc_wait<true>(bar, phase, abort, a)) ? 1 : 0;
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
   for (int k = 0;; ++k) {
@@ -213,7 +266,7 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
     __syncwarp();
     const TcUnit un = sh.units[slot];
     if (!un.valid) break;
-    if (!lane0_wait(&sh.q_empty, (k & 1) ^ 1)) break;
+    if (!slot_wait(&sh.q_empty, (k & 1) ^ 1)) break;
     if (lane == 0) {
       // one box per 64-dim half of a tile: T tokens x group heads = T * group rows of 128 bytes
       const int nq = un.n[1] > 0 ? 2 : 1;
@@ -225,66 +278,22 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
           tma_load_3d(smem_base + C::kQOffset + x * C::kQBytes + hf * C::kQHalfBytes, qmap,
                       &sh.q_full, hf * 64, un.h * a.group, un.t0 + un.tok0 + a.tile_tokens * x);
     }
-    const int32_t* bt_row =
-        a.block_table + static_cast<size_t>(unit_table_row(a, un)) * a.MB;
-    const int page0 = unit_first_page(a, un);
-    int win = 0;
-    auto page = [&](int pg) {
-      return pg < un.pages
-                 ? kernel_page(bt_row, page0 + pg, a.ratio, a.num_blocks, a.null_block)
-                 : a.null_block;
-    };
-    int bid = page(lane);
-    int bid_next = page(32 + lane);
-    int ids[2] = {a.null_block, a.null_block};  // page id of this lane for tiles j and j-1
+    PageWindow pw(a, un, lane);
     bool ok = true;
-    for (int j = 0; j <= un.n_kt; ++j) {
-      if (j < un.n_kt) {  // K of tile j
-        const int first = j * C::kPagesPerTile;
-        if (first - win >= 32) {
-          win += 32;
-          bid = bid_next;
-          bid_next = page(win + 32 + lane);
-        }
-        int id = __shfl_sync(0xffffffffu, bid, first + (lane & 7) - win);
-        const int pg = first + (lane & 7);
-        if (pg >= un.pages) {
-          id = a.null_block;  // past the sequence: any valid page (masked, V zeroed)
-        } else if (id < 0 || id >= a.num_blocks || id == a.null_block) {
-          if (lane < C::kPagesPerTile) raise_error(a.err, RB_EBIT_BLOCK_ID);
-          id = a.null_block;
-        }
-        ids[j & 1] = id;
-        const uint32_t itk = it + j, st = itk % C::kStagesK;
-        if (!lane0_wait(&sh.k_empty[st], ((itk / C::kStagesK) & 1) ^ 1)) { ok = false; break; }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&sh.k_full[st], C::kTileBytes);
-          ++k_armed[st];
-        }
-        __syncwarp();
-        if (lane < C::kPagesPerTile) {
-#pragma unroll
-          for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_3d(smem_base + st * C::kTileBytes + hf * C::kHalfBytes + lane * (kPage * 128),
-                        kmap, &sh.k_full[st], hf * 64, un.h, id * kPage);
-        }
+    for (int j = 0; j < un.n_kt; ++j) {
+      const int id = pw.tile_page(j, true);
+      const uint32_t itk = it + j, st = itk % C::kStagesK;
+      if (!slot_wait(&sh.k_empty[st], ((itk / C::kStagesK) & 1) ^ 1)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&sh.k_full[st], C::kTileBytes);
+        ++k_armed[st];
       }
-      if (j >= 1) {  // V of tile j-1
-        const uint32_t itv = it + j - 1, st = itv % C::kStagesV;
-        if (!lane0_wait(&sh.v_empty[st], ((itv / C::kStagesV) & 1) ^ 1)) { ok = false; break; }
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&sh.v_full[st], C::kTileBytes);
-          ++v_armed[st];
-        }
-        __syncwarp();
-        if (lane < C::kPagesPerTile) {
-          const int id = ids[(j - 1) & 1];
+      __syncwarp();
+      if (lane < C::kPagesPerTile) {
 #pragma unroll
-          for (int hf = 0; hf < C::kHalves; ++hf)
-            tma_load_3d(smem_base + C::kVOffset + st * C::kTileBytes + hf * C::kHalfBytes +
-                            lane * (kPage * 128),
-                        vmap, &sh.v_full[st], hf * 64, un.h, id * kPage);
-        }
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem_base + st * C::kTileBytes + hf * C::kHalfBytes + lane * (kPage * 128),
+                      kmap, &sh.k_full[st], hf * 64, un.h, id * kPage);
       }
     }
     if (!ok) break;
@@ -294,6 +303,61 @@ __device__ void producer(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
     if (q_armed) mbar_wait_bounded(&sh.q_full, (q_armed - 1) & 1, 100000000ull);
     for (int b = 0; b < C::kStagesK; ++b)
       if (k_armed[b]) mbar_wait_bounded(&sh.k_full[b], (k_armed[b] - 1) & 1, 100000000ull);
+  }
+}
+
+// Producer of V (warp 2, whole warp): follows the unit ring like the other consumers and loads
+// each V tile into the V ring.  A warp of its own, so that V tiles are issued as soon as their
+// slot frees, not after the next K tile (one warp issuing both took about a whole key-tile step
+// for the TMA issue and waits alone, and left V late).
+template <int HD>
+__device__ void producer_v(const AttnArgs& a, TcShared& sh, uint32_t smem_base,
+                           const CUtensorMap* vmap) {
+  using C = TcCfg<HD>;
+  volatile int* abort = &sh.abort;
+  const int lane = threadIdx.x & 31;
+  uint32_t it = 0, v_armed[C::kStagesV] = {};
+  auto lane0_wait = [&](uint64_t* bar, uint32_t phase) -> bool {
+    int ok = 1;
+    if (lane == 0) ok = tc_wait(bar, phase, abort, a) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  auto slot_wait = [&](uint64_t* bar, uint32_t phase) -> bool {
+    int ok = 1;
+    if (lane == 0)
+      ok = (mbar_test_relaxed(bar, phase) || tc_wait<true>(bar, phase, abort, a)) ? 1 : 0;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  for (int k = 0;; ++k) {
+    const int slot = k % C::kRing;
+    if (!lane0_wait(&sh.unit_full[slot], (k / C::kRing) & 1)) break;
+    const TcUnit un = sh.units[slot];
+    if (!un.valid) break;
+    __syncwarp();
+    if (lane == 0) tc::mbar_arrive(&sh.unit_empty[slot]);  // the descriptor is in registers
+    PageWindow pw(a, un, lane);
+    bool ok = true;
+    for (int j = 0; j < un.n_kt; ++j) {
+      const int id = pw.tile_page(j, false);
+      const uint32_t itv = it + j, st = itv % C::kStagesV;
+      if (!slot_wait(&sh.v_empty[st], ((itv / C::kStagesV) & 1) ^ 1)) { ok = false; break; }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&sh.v_full[st], C::kTileBytes);
+        ++v_armed[st];
+      }
+      __syncwarp();
+      if (lane < C::kPagesPerTile) {
+#pragma unroll
+        for (int hf = 0; hf < C::kHalves; ++hf)
+          tma_load_3d(smem_base + C::kVOffset + st * C::kTileBytes + hf * C::kHalfBytes +
+                          lane * (kPage * 128),
+                      vmap, &sh.v_full[st], hf * 64, un.h, id * kPage);
+      }
+    }
+    if (!ok) break;
+    it += un.n_kt;
+  }
+  if (lane == 0 && *abort) {
     for (int b = 0; b < C::kStagesV; ++b)
       if (v_armed[b]) mbar_wait_bounded(&sh.v_full[b], (v_armed[b] - 1) & 1, 100000000ull);
   }
@@ -692,7 +756,8 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
   if (tid == 0) {
     for (int i = 0; i < C::kRing; ++i) {
       mbar_init(&sh.unit_full[i], 1);
-      mbar_init(&sh.unit_empty[i], 1 + 8);  // the issuer and one lane of each softmax warp
+      // the issuer, one lane of each softmax warp and the V producer
+      mbar_init(&sh.unit_empty[i], 1 + 8 + 1);
     }
     mbar_init(&sh.q_full, 1);
     mbar_init(&sh.q_empty, 1);
@@ -743,7 +808,9 @@ __global__ void __launch_bounds__(TcCfg<HD>::kThreads, 1)
     for (int phase = 0; phase < 2; ++phase) {
       if ((phase == 0) != decode_first) {
         if (warp == C::kProducerWarp) {
-          producer<HD>(a, sh, base, &qmap, &kmap, &vmap);
+          producer_qk<HD>(a, sh, base, &qmap, &kmap);
+        } else if (warp == C::kProducerVWarp) {
+          producer_v<HD>(a, sh, base, &vmap);
         } else if (warp == C::kMmaWarp) {
           if ((tid & 31) == 0) mma_issuer<HD>(a, sh, tmem, base);
         }
