@@ -435,8 +435,6 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
     tc::fence_after_sync();
     issue_s(0, itk);
     if (un.n[1] > 0) issue_s(1, itk);
-    tc::commit(&sh.k_empty[itk % C::kStagesK]);
-    if (un.n_kt == 1) tc::commit(&sh.q_empty);
     bool ok = true;
     for (int j = 0; j < un.n_kt && ok; ++j) {
       const uint32_t kt = itk + j;
@@ -465,9 +463,6 @@ __device__ void mma_issuer(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint3
         if (next_s) issue_s(x, kt + 1);
       }
       if (!ok) break;
-      tc::commit(&sh.v_empty[kt % C::kStagesV]);                        // P V of tile j issued
-      if (j + 1 < un.n_kt) tc::commit(&sh.k_empty[(kt + 1) % C::kStagesK]);  // S of tile j+1
-      if (j + 2 == un.n_kt) tc::commit(&sh.q_empty);                      // unit's last S issued
     }
     if (!ok) break;
     tc::mbar_arrive(&sh.unit_empty[slot]);
@@ -526,6 +521,12 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
     const int lim = !valid ? -1 : (causal ? un.c + jt : un.c);
     const int lim_min = causal ? un.c + tok_base : un.c;
     const bool partial = rows_used < C::kM || tok_base + a.tile_tokens > un.q;
+    // The side that reads every K/V tile of the unit (B, or A when B is empty: B's rows come
+    // later, so it sees at least A's keys) hands the Q, K and V slots back to the producers:
+    // its S of tile j landing means every MMA issued before that S has completed, S_A of tile
+    // j and both P V of tile j - 1 among them; its last P V landing (o_done) frees the last V.
+    // This keeps those arrivals off the MMA issuer, whose commits are its critical path.
+    const bool releases = x == (un.n[1] > 0 ? 1 : 0);
     // running reference (log2 domain) and sum; a row without a query starts at 0, so that only
     // rows with visible keys take the first tile's maximum
     float m_ref = valid ? -INFINITY : 0.f, l = 0.f;
@@ -533,6 +534,12 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
     for (int j = 0; j < n; ++j) {
       const uint32_t tj = tc_x + j;
       if (!wait_all(&sh.s_full[x], tj & 1)) { ok = false; break; }
+      if (releases && t == 0) {
+        const uint32_t kt = itk + j;
+        tc::mbar_arrive(&sh.k_empty[kt % C::kStagesK]);
+        if (j > 0) tc::mbar_arrive(&sh.v_empty[(kt - 1) % C::kStagesV]);
+        if (j + 1 == n) tc::mbar_arrive(&sh.q_empty);
+      }
       tc::fence_after_sync();
       float s[128];
       {
@@ -653,9 +660,11 @@ __device__ void softmax_wg(const AttnArgs& a, TcShared& sh, uint32_t tmem, uint8
       l += rsum;
     }
     if (!ok) break;
+    const uint32_t kt_last = itk + un.n_kt - 1;
     itk += un.n_kt;
     if (n > 0) {
       if (!wait_all(&sh.o_done[x], uc_x & 1)) break;  // the unit's last P V is in O
+      if (releases && t == 0) tc::mbar_arrive(&sh.v_empty[kt_last % C::kStagesV]);
       ++uc_x;
       tc_x += n;
       tc::fence_after_sync();
