@@ -14,8 +14,8 @@
 //   warp 1     TMA producer of units, Q and K: fetches units into a 4-entry ring, loads Q_A and
 //              Q_B once per unit (3-D boxes {64 dims, group heads, T tokens}) and each 128-key
 //              K tile (8 pages x 128-byte boxes, 128B swizzle, one page per lane) into a
-//              3-stage K ring (K is freed once S is done);
-//   warp 2     TMA producer of V: the same boxes into a 2-stage V ring;
+//              2-stage K ring (K is freed once S is done);
+//   warp 2     TMA producer of V: the same boxes into a 3-stage V ring;
 //   warp 0     allocates all 512 TMEM columns (S_A, S_B, O_A, O_B); one thread issues the MMAs
 //              in the order S_A(0) S_B(0) | PV_A(0) S_A(1) | PV_B(0) S_B(1) | PV_A(1) ...
 //              S = Q K^T: M=128, N=128, K=hd, both operands K-major in shared memory;
@@ -48,8 +48,10 @@ struct TcCfg {
   static constexpr int kTileBytes = kHalves * kHalfBytes;
   static constexpr int kQHalfBytes = kM * 128;
   static constexpr int kQBytes = kHalves * kQHalfBytes;   // one Q tile
-  static constexpr int kStagesK = 3;
-  static constexpr int kStagesV = 2;
+  // V tile j is read by the first block of step j, K tile j + 1 by the second half of it, and
+  // both slots free at the same point (S of tile j - 1 landing): the deeper ring goes to V
+  static constexpr int kStagesK = 2;
+  static constexpr int kStagesV = 3;
   static constexpr int kVOffset = kStagesK * kTileBytes;
   static constexpr int kQOffset = kVOffset + kStagesV * kTileBytes;  // Q_A then Q_B
   static constexpr int kUsed = kQOffset + 2 * kQBytes;
