@@ -424,6 +424,29 @@ rb_status rb_step_host(const rb_step_args* args, const rb_host_copy* in, int32_t
                        const rb_host_copy* out, int32_t num_out, void* stream);
 
 /*
+ * rb_step_host_async — rb_step_host with its copies on streams of their own, so that the
+ * copies of consecutive steps overlap the steps themselves (the host link and the GPU work at
+ * once): enqueues the `num_in` host-to-device copies on `in_stream` and records `in_done`
+ * there; makes `stream` wait for `in_done`, enqueues the step exactly as rb_step on `stream`
+ * and records `step_done` there; makes `out_stream` wait for `step_done` and enqueues the
+ * `num_out` device-to-host copies on it.  `in_done` and `step_done` are caller-created
+ * cudaEvent_t (passed as void*); streams may be null (the legacy default stream).
+ * The caller keeps the buffers of steps in flight apart (for example two sets of input and
+ * output buffers used by alternate steps) and orders their reuse: the in-copies of a later
+ * step into a set after the step that read the set (`in_stream` waiting on that step's
+ * `step_done`), a later step's writes to an output set after the out-copies of the step
+ * before (`stream` waiting on an event recorded on `out_stream`).  One cudaMemcpyAsync per
+ * copy; nothing is allocated or synchronised.
+ * Errors: those of rb_step_host, plus RB_ERR_INVALID_ARG for a null `in_done` or
+ * `step_done`, all returned before anything is enqueued; RB_ERR_CUDA if enqueueing a copy, a
+ * record, a wait or a launch fails (what was enqueued before stays enqueued).
+ */
+rb_status rb_step_host_async(const rb_step_args* args, const rb_host_copy* in, int32_t num_in,
+                             const rb_host_copy* out, int32_t num_out, void* stream,
+                             void* in_stream, void* out_stream, void* in_done,
+                             void* step_done);
+
+/*
  * Persistent batch — one row per resident request, every column device-resident and
  * caller-owned ("vLLM 源码完全拆解（五）…", "行号是一种短生命周期地址": the row is the common key
  * of the request's token history, counters and page row; a move must carry every column).

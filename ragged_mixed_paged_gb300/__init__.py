@@ -21,9 +21,9 @@ from ._binding import (Dims, RbError, EBIT_ATTN_META, EBIT_BLOCK_ID, EBIT_NUM_CO
                        paged_attention_cascade)
 from ._binding import EBIT_BATCH_ID, EBIT_BATCH_SIZE
 from .persistent_batch import PersistentBatch, batch_workspace_size
-from .step import StepBuffers, run_step, run_step_fused, run_step_host
+from .step import StepBuffers, run_step, run_step_fused, run_step_host, run_step_host_async
 
 __all__ = ["Dims", "RbError", "gather_rows", "kv_write", "launch_count", "lib", "pad_for_graph",
            "paged_attention", "prepare_inputs", "status_string", "workspace_size", "StepBuffers",
-           "run_step", "run_step_fused", "run_step_host", "LIB_PATH", "PersistentBatch", "batch_workspace_size",
+           "run_step", "run_step_fused", "run_step_host", "run_step_host_async", "LIB_PATH", "PersistentBatch", "batch_workspace_size",
            "cascade_prefix_len", "cascade_workspace_size", "paged_attention_cascade"]

@@ -115,6 +115,8 @@ def _load():
                                    I32, P]),
         "rb_step_host": (I32, [ctypes.POINTER(rb_step_args), ctypes.POINTER(rb_host_copy), I32,
                                ctypes.POINTER(rb_host_copy), I32, P]),
+        "rb_step_host_async": (I32, [ctypes.POINTER(rb_step_args), ctypes.POINTER(rb_host_copy),
+                                     I32, ctypes.POINTER(rb_host_copy), I32, P, P, P, P, P]),
         "rb_paged_attention_cascade_workspace_size": (ctypes.c_size_t, [PD, I32, I32]),
         "rb_paged_attention_cascade": (I32, [PD, I32, I32, I32, I32, P, P, P, P, P, P,
                                              ctypes.c_float, P, P, ctypes.c_size_t, P, P]),

@@ -255,11 +255,11 @@ extern "C" rb_status rb_step_profiled(const rb_step_args* args, void* const* eve
                       StepMarks{events, num_events});
 }
 
-extern "C" rb_status rb_step_host(const rb_step_args* args, const rb_host_copy* in,
-                                  int32_t num_in, const rb_host_copy* out, int32_t num_out,
-                                  void* stream) {
-  rb::CallRange range_("rb_step_host");
-  using namespace rb;
+namespace rb {
+namespace {
+
+rb_status check_host_copies(const rb_step_args* args, const rb_host_copy* in, int32_t num_in,
+                            const rb_host_copy* out, int32_t num_out) {
   if (args == nullptr || args->dims == nullptr || num_in < 0 || num_out < 0 ||
       (num_in > 0 && in == nullptr) || (num_out > 0 && out == nullptr))
     return RB_ERR_INVALID_ARG;
@@ -269,20 +269,58 @@ extern "C" rb_status rb_step_host(const rb_step_args* args, const rb_host_copy* 
   for (int32_t i = 0; i < num_out; ++i)
     if (out[i].bytes > 0 && (out[i].dst == nullptr || out[i].src == nullptr))
       return RB_ERR_INVALID_ARG;
-  StepArgs sa;
-  attn::AttnSetup su;
-  rb_status st = step_build(*args, &sa, &su);
-  if (st != RB_OK) return st;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  for (int32_t i = 0; i < num_in; ++i)
-    if (in[i].bytes > 0 &&
-        cudaMemcpyAsync(in[i].dst, in[i].src, in[i].bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
-      return RB_ERR_CUDA;
-  st = step_enqueue(*args, sa, su, s);
-  if (st != RB_OK) return st;
-  for (int32_t i = 0; i < num_out; ++i)
-    if (out[i].bytes > 0 &&
-        cudaMemcpyAsync(out[i].dst, out[i].src, out[i].bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  return RB_OK;
+}
+
+rb_status enqueue_copies(const rb_host_copy* c, int32_t n, cudaMemcpyKind kind, cudaStream_t s) {
+  for (int32_t i = 0; i < n; ++i)
+    if (c[i].bytes > 0 && cudaMemcpyAsync(c[i].dst, c[i].src, c[i].bytes, kind, s) != cudaSuccess)
       return RB_ERR_CUDA;
   return RB_OK;
+}
+
+}  // namespace
+}  // namespace rb
+
+extern "C" rb_status rb_step_host(const rb_step_args* args, const rb_host_copy* in,
+                                  int32_t num_in, const rb_host_copy* out, int32_t num_out,
+                                  void* stream) {
+  rb::CallRange range_("rb_step_host");
+  using namespace rb;
+  rb_status st = check_host_copies(args, in, num_in, out, num_out);
+  if (st != RB_OK) return st;
+  StepArgs sa;
+  attn::AttnSetup su;
+  st = step_build(*args, &sa, &su);
+  if (st != RB_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = enqueue_copies(in, num_in, cudaMemcpyHostToDevice, s)) != RB_OK) return st;
+  if ((st = step_enqueue(*args, sa, su, s)) != RB_OK) return st;
+  return enqueue_copies(out, num_out, cudaMemcpyDeviceToHost, s);
+}
+
+extern "C" rb_status rb_step_host_async(const rb_step_args* args, const rb_host_copy* in,
+                                        int32_t num_in, const rb_host_copy* out,
+                                        int32_t num_out, void* stream, void* in_stream,
+                                        void* out_stream, void* in_done, void* step_done) {
+  rb::CallRange range_("rb_step_host_async");
+  using namespace rb;
+  rb_status st = check_host_copies(args, in, num_in, out, num_out);
+  if (st != RB_OK) return st;
+  if (in_done == nullptr || step_done == nullptr) return RB_ERR_INVALID_ARG;
+  StepArgs sa;
+  attn::AttnSetup su;
+  st = step_build(*args, &sa, &su);
+  if (st != RB_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t si = static_cast<cudaStream_t>(in_stream);
+  cudaStream_t so = static_cast<cudaStream_t>(out_stream);
+  cudaEvent_t ei = static_cast<cudaEvent_t>(in_done), es = static_cast<cudaEvent_t>(step_done);
+  if ((st = enqueue_copies(in, num_in, cudaMemcpyHostToDevice, si)) != RB_OK) return st;
+  if (cudaEventRecord(ei, si) != cudaSuccess || cudaStreamWaitEvent(s, ei, 0) != cudaSuccess)
+    return RB_ERR_CUDA;
+  if ((st = step_enqueue(*args, sa, su, s)) != RB_OK) return st;
+  if (cudaEventRecord(es, s) != cudaSuccess || cudaStreamWaitEvent(so, es, 0) != cudaSuccess)
+    return RB_ERR_CUDA;
+  return enqueue_copies(out, num_out, cudaMemcpyDeviceToHost, so);
 }

@@ -162,6 +162,25 @@ def _copies(pairs):
     return arr
 
 
+def run_step_host_async(b: StepBuffers, host_in, host_out, stream, in_stream, out_stream,
+                        in_done, step_done, softmax_scale: Optional[float] = None) -> None:
+    """Enqueue one ``rb_step_host_async`` call: the ``host_in`` copies on ``in_stream`` (then
+    ``in_done`` recorded there), the step on ``stream`` after ``in_done`` (then ``step_done``),
+    the ``host_out`` copies on ``out_stream`` after ``step_done``.  The events are
+    torch.cuda.Event objects already recorded once (torch creates them lazily); the caller
+    keeps the buffers of steps in flight apart and orders their reuse."""
+    if b._step_args is None or softmax_scale is not None:
+        b._step_args = _step_args(b, softmax_scale)
+    if not (in_done.cuda_event and step_done.cuda_event):
+        raise ValueError("record each event once before passing it (torch creates them lazily)")
+    ins, outs = _copies(host_in), _copies(host_out)
+    rb._check("rb_step_host_async",
+              rb.lib.rb_step_host_async(ctypes.byref(b._step_args), ins, len(host_in), outs,
+                                        len(host_out), rb._stream(stream), rb._stream(in_stream),
+                                        rb._stream(out_stream), in_done.cuda_event,
+                                        step_done.cuda_event))
+
+
 def run_step_host(b: StepBuffers, host_in, host_out, stream=None,
                   softmax_scale: Optional[float] = None) -> None:
     """Enqueue one ``rb_step_host`` call: the ``host_in`` copies (``(device_dst, host_src)``

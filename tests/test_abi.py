@@ -267,6 +267,28 @@ def test_step_host_copy_checks(lib):
     assert L.rb_step_host(ctypes.byref(args), two, 2, two, 2, None) == 1      # no metadata buffers
 
 
+def test_step_host_async_checks(lib):
+    """rb_step_host_async rejects what rb_step_host rejects and null events, before it enqueues
+    anything: no GPU is touched."""
+    L = lib.lib
+    none = ctypes.POINTER(lib.rb_host_copy)()
+    ev = ctypes.c_void_p(1)  # never dereferenced: every call below fails its host checks first
+    assert L.rb_step_host_async(None, none, 0, none, 0, None, None, None, ev, ev) == 1
+    args = lib.rb_step_args()
+    d = _dims(lib)
+    args.dims = ctypes.pointer(d)
+    args.num_reqs = args.num_reqs_padded = 1
+    args.num_tokens = args.num_tokens_padded = 1
+    assert L.rb_step_host_async(ctypes.byref(args), none, -1, none, 0, None, None, None, ev,
+                                ev) == 1                                     # negative count
+    assert L.rb_step_host_async(ctypes.byref(args), none, 0, none, 0, None, None, None, None,
+                                ev) == 1                                     # null in_done
+    assert L.rb_step_host_async(ctypes.byref(args), none, 0, none, 0, None, None, None, ev,
+                                None) == 1                                   # null step_done
+    assert L.rb_step_host_async(ctypes.byref(args), none, 0, none, 0, None, None, None, ev,
+                                ev) == 1                                     # no metadata buffers
+
+
 def test_wait_limit_hook_checks(lib):
     """The attention wait-limit test hook rejects out-of-range settings and restores defaults
     (host state only; no launch)."""

@@ -156,3 +156,107 @@ def test_step_host_equals_device_step(rb, name):
     assert torch.equal(got["rows"], a.rows_out.cpu())
     assert torch.equal(got["scalars"], a.meta["scalars"].cpu())
     _same(a, b)
+
+
+def test_step_host_async_pipeline_equals_device_steps(rb):
+    """rb_step_host_async over a pipelined run of chunked-prefill stream steps (copies on their
+    own streams, two buffer sets used by alternate steps, each step's copies overlapping its
+    neighbours' compute) gives, step by step, what rb_step gives on inputs already on the
+    device: the same attention output, gathered rows and scalars, bit for bit."""
+    import dataclasses
+
+    import workloads as wl
+
+    stream = wl.MixedChunkStream(seed=4321)
+    steps = [stream.next_step() for _ in range(6)]
+    d = stream.dims
+    dims = rb.Dims.of(d)
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(7)
+    nmax, rmax = stream.BUDGET, d.max_num_reqs
+    rnd = lambda *sh: torch.randn(*sh, generator=g, device=dev).to(torch.bfloat16)
+    q, k, v = rnd(nmax, d.num_q_heads, d.head_dim), rnd(nmax, d.num_kv_heads, d.head_dim), \
+        rnd(nmax, d.num_kv_heads, d.head_dim)
+    hidden = rnd(nmax, 256)
+    kc0, vc0 = rnd(d.num_slots, d.num_kv_heads, d.head_dim), rnd(d.num_slots, d.num_kv_heads,
+                                                                 d.head_dim)
+    twins = []
+    for t in range(2):  # the same stream applied to two batches with their own KV caches
+        batch = rb.PersistentBatch(d.max_num_reqs, d.max_model_len, d.max_blocks_per_req,
+                                   device=dev)
+        tables = dict(token_table=batch.token_table, block_table=batch.block_table,
+                      num_computed=batch.num_computed, num_scheduled=batch.num_scheduled,
+                      num_prompt=batch.num_prompt)
+        kc, vc = (kc0, vc0) if t == 0 else (kc0.clone(), vc0.clone())
+        twins.append((batch, tables, kc, vc))
+    # reference: rb_step on the device inputs, one step at a time
+    batch, tables, kc, vc = twins[0]
+    ref = rb.StepBuffers.allocate(dims, rmax, rmax, nmax, nmax, tables, q, k, v, hidden, kc, vc)
+    want = []
+    for st in steps:
+        batch.apply(st)
+        R, N = batch.num_reqs, batch.num_tokens_scheduled
+        b = dataclasses.replace(ref, num_reqs=R, num_reqs_padded=R, num_tokens=N,
+                                num_tokens_padded=N, q=q[:N], k=k[:N], v=v[:N], hidden=hidden[:N],
+                                attn_out=ref.attn_out[:N], rows_out=ref.rows_out[:R],
+                                _step_args=None)
+        rb.run_step_fused(b)
+        torch.cuda.synchronize()
+        want.append((b.attn_out.cpu(), b.rows_out.cpu(), b.meta["scalars"].cpu()))
+    # pipelined: inputs from pinned host memory, two sets, three streams
+    batch, tables, kc, vc = twins[1]
+    hq, hk, hv, hh = (t.cpu().pin_memory() for t in (q, k, v, hidden))
+    sets = []
+    for _ in range(2):
+        sb = rb.StepBuffers.allocate(dims, rmax, rmax, nmax, nmax, tables, torch.zeros_like(q),
+                                     torch.zeros_like(k), torch.zeros_like(v),
+                                     torch.zeros_like(hidden), kc, vc)
+        ho = (torch.empty(tuple(sb.attn_out.shape), dtype=sb.attn_out.dtype).pin_memory(),
+              torch.empty(tuple(sb.rows_out.shape), dtype=sb.rows_out.dtype).pin_memory(),
+              torch.empty(4, dtype=torch.int32).pin_memory())
+        sets.append((sb, ho))
+    s_comp, s_in, s_out = torch.cuda.current_stream(), torch.cuda.Stream(), torch.cuda.Stream()
+
+    def ev():
+        e = torch.cuda.Event()
+        e.record(s_comp)
+        return e
+
+    in_done, step_done, out_done = ([ev(), ev()] for _ in range(3))
+    pending = [None, None]
+    seen = {}
+
+    def collect(x):
+        if pending[x] is not None:
+            out_done[x].synchronize()
+            i, N, R = pending[x]
+            o_attn, o_rows, o_sc = sets[x][1]
+            seen[i] = (o_attn[:N].clone(), o_rows[:R].clone(), o_sc.clone())
+            pending[x] = None
+
+    for i, st in enumerate(steps):
+        x = i % 2
+        sb, (o_attn, o_rows, o_sc) = sets[x]
+        collect(x)
+        s_in.wait_event(step_done[x])
+        s_comp.wait_event(out_done[x])
+        batch.apply(st, stream=s_comp)
+        R, N = batch.num_reqs, batch.num_tokens_scheduled
+        b = dataclasses.replace(sb, num_reqs=R, num_reqs_padded=R, num_tokens=N,
+                                num_tokens_padded=N, q=sb.q[:N], k=sb.k[:N], v=sb.v[:N],
+                                hidden=sb.hidden[:N], attn_out=sb.attn_out[:N],
+                                rows_out=sb.rows_out[:R], _step_args=None)
+        ins = [(b.q, hq[:N]), (b.k, hk[:N]), (b.v, hv[:N]), (b.hidden, hh[:N])]
+        outs = [(o_attn[:N], b.attn_out), (o_rows[:R], b.rows_out), (o_sc, b.meta["scalars"])]
+        rb.run_step_host_async(b, ins, outs, s_comp, s_in, s_out, in_done[x], step_done[x])
+        out_done[x].record(s_out)
+        pending[x] = (i, N, R)
+    collect(0), collect(1)
+    torch.cuda.synchronize()
+    assert int(batch.error_word.item()) == 0
+    for i, (a_attn, a_rows, a_sc) in enumerate(want):
+        g_attn, g_rows, g_sc = seen[i]
+        assert int(g_sc[3]) == 0, f"step {i}"
+        assert torch.equal(g_attn, a_attn), f"step {i}"
+        assert torch.equal(g_rows, a_rows), f"step {i}"
+        assert torch.equal(g_sc, a_sc), f"step {i}"
