@@ -175,7 +175,7 @@ def peaks():
 
 
 FUSED_SOURCES = ("attn_prefill_tc.cu", "attn_decode_warp.cuh", "tc_ptx.cuh", "attn_common.cuh",
-                 "rb_internal.cuh")
+                 "rb_internal.cuh", "attn_plan.cuh")
 
 
 def kernel_sources_hash():

@@ -252,6 +252,15 @@ __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim, ReqSr
     // leaves out, and the decode-first pass measured faster whenever the two were close.
     unsigned long long best =
         tid == 0 ? key(0.9f * (t_dec(C) + t_pre(C)), tot_d > 0 ? C : 0) : ~0ull;
+    // d = 0: everything prefills first, so the longest units start at once, and the decode
+    // units fill the CTAs as they run out of prefill units (the last, partial wave of prefill
+    // units leaves CTAs idle otherwise).  Only for decode work that is bandwidth-heavy next to
+    // one decode unit's latency: a few short decode units run after the prefill as a tail of
+    // their own (the padding example measured 65 -> 77 us), many long ones stream at full HBM
+    // rate beside the prefill's last wave (long context 6.27 -> 6.08 ms).
+    const float dec_stream = dec_bytes / kHbmBytesPerUs;
+    if (tid == 1 && tot_d > 0 && tot_p > 0 && dec_stream > 4.f * t_unit)
+      best = key(0.9f * fmaxf(pre_long, pre_total / C + dec_stream), 0);
     if (tot_d > 0 && tot_p > 0)
       for (int d = 1 + tid; d < C; d += nthreads)
         best = min(best, key(fmaxf(t_dec(d), t_pre(C - d)), d));
