@@ -256,10 +256,11 @@ __device__ __forceinline__ void plan_body(const AttnArgs& a, int head_dim, ReqSr
     // units fill the CTAs as they run out of prefill units (the last, partial wave of prefill
     // units leaves CTAs idle otherwise).  Only for decode work that is bandwidth-heavy next to
     // one decode unit's latency: a few short decode units run after the prefill as a tail of
-    // their own (the padding example measured 65 -> 77 us), many long ones stream at full HBM
-    // rate beside the prefill's last wave (long context 6.27 -> 6.08 ms).
+    // their own.  Measured against decode-first: long context (decode HBM time 9.5 unit
+    // latencies) 6.27 -> 6.05 ms; the same batch at 1/8 of its lengths (5.8) 0.99 -> 1.13 ms
+    // and the padding example (0.9) 65 -> 77 us, both slower; hence the threshold of 8.
     const float dec_stream = dec_bytes / kHbmBytesPerUs;
-    if (tid == 1 && tot_d > 0 && tot_p > 0 && dec_stream > 4.f * t_unit)
+    if (tid == 1 && tot_d > 0 && tot_p > 0 && dec_stream > 8.f * t_unit)
       best = key(0.9f * fmaxf(pre_long, pre_total / C + dec_stream), 0);
     if (tot_d > 0 && tot_p > 0)
       for (int d = 1 + tid; d < C; d += nthreads)
