@@ -61,11 +61,11 @@ FLUSH_BYTES = 512 << 20
 # (dram__bytes_read.sum + dram__bytes_write.sum), keyed by (workload, hash of the kernel's
 # sources): a figure is reported only while the sources are the ones it was measured on.
 KNOWN_TRAFFIC = {
-    (2, "187df0cc9db252f1"): 79019776 + 3876608,
-    (3, "187df0cc9db252f1"): 4545736704 + 26042368,
+    (2, "a2978268e1587523"): 79017728 + 3901440,
+    (3, "a2978268e1587523"): 4545561856 + 26183424,
     # the stream: mean over the launches of stream steps 5..99 (the default timed steps)
-    (4, "187df0cc9db252f1"): 9536432627 + 80765798,
-    (5, "187df0cc9db252f1"): 8574837760 + 107234560,
+    (4, "a2978268e1587523"): 9499339202 + 80951309,
+    (5, "a2978268e1587523"): 6555419392 + 115067648,
 }
 
 WORKLOAD_NAMES = {1: "pages' worked example A/B/C", 2: "pages' padding example",
