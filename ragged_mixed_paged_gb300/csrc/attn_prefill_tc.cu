@@ -7,10 +7,10 @@
 // Prefill unit = (request, kv head, pair of 128-row query tiles A and B); rows are (query token,
 // head of the group) pairs, token-major, so every K/V tile serves the whole query-head group
 // and both tiles of the pair.  A tile holds T = 128 / group whole tokens (T * group rows; for a
-// group that does not divide 128 the last rows hold no query and are masked out).  One CTA per SM (persistent; units pulled from an atomic
-// counter, the most expensive pair of each request first), 12 warps with fixed roles (the
-// single-thread MMA issuer is warp 0, the oldest warp of its SM sub-partition, which shares that
-// scheduler with one softmax warp of each tile):
+// group that does not divide 128 the last rows hold no query and are masked out).  One CTA per
+// SM (persistent; units pulled from an atomic counter, the most expensive pair of each request
+// first), 12 warps with fixed roles (the single-thread MMA issuer is warp 0, the oldest warp of
+// its SM sub-partition, which shares that scheduler with one softmax warp of each tile):
 //   warp 1     TMA producer of units, Q and K: fetches units into a 4-entry ring, loads Q_A and
 //              Q_B once per unit (3-D boxes {64 dims, group heads, T tokens}) and each 128-key
 //              K tile (8 pages x 128-byte boxes, 128B swizzle, one page per lane) into a
@@ -27,7 +27,9 @@
 //              reference is the row's first-tile maximum and moves (O rescaled in TMEM, the
 //              tile's exponents taken again) only when a tile's sum exceeds 2^20 (exact either
 //              way: P and the sum share the reference), so a common tile takes no row maximum.
-//              The epilogue reads O, divides by the sum, stores bf16 rows.
+//              The epilogue reads O, divides by the sum, stores bf16 rows.  The side that reads
+//              every K/V tile of the unit (B, or A alone) hands the Q, K and V slots back to the
+//              producers as its S tiles land, so the issuer commits only S, O and its drain.
 // All mbarrier waits are bounded; a timeout sets RB_EBIT_TIMEOUT, every role stops, in-flight
 // copies and MMAs are drained with bounded waits and TMEM is freed before the CTA exits.
 #include "attn_common.cuh"
