@@ -155,3 +155,25 @@ def check_kv_write(spec, k_before, v_before, tens, slot_mapping):
     assert torch.equal(tens.k_cache[slots], tens.k[:N])
     assert torch.equal(tens.v_cache[slots], tens.v[:N])
 
+
+def jump_tensors(spec, hot, device="cuda"):
+    """Inputs whose scores jump across key tiles: every query is a common direction u plus small
+    noise and the keys at the positions of `hot` ({(start, end): beta}) are beta * u, so a row's
+    scores rise by ~16 beta (log2 units, head_dim 128) where it reaches those keys."""
+    tens = wl.make_tensors(spec, device=device)
+    d = spec.dims
+    g = torch.Generator(device=device).manual_seed(spec.seed + 17)
+    u = torch.randn(d.head_dim, generator=g, device=device)
+    q = u + 0.1 * torch.randn(tens.q.shape, generator=g, device=device)
+    tens.q.copy_(q.to(torch.bfloat16))
+    qsl = np.concatenate([[0], np.cumsum(spec.num_scheduled)])
+    for i in range(spec.num_reqs):
+        c = int(spec.num_computed[i])
+        for (s, e), beta in hot.items():
+            key = (beta * u).to(torch.bfloat16)
+            hs, he = min(s, c), min(e, c)          # hot keys in the history
+            tens.hist_k[i][hs:he] = key
+            ns, ne = max(s, c) - c, max(min(e, c + int(spec.num_scheduled[i])), c) - c
+            tens.k[int(qsl[i]) + ns:int(qsl[i]) + ne] = key   # hot keys among the new tokens
+    wl.place_history(spec, tens.hist_k, tens.k_cache)
+    return tens

@@ -5,8 +5,8 @@ import pytest
 import torch
 
 import workloads as wl
-from gpu_cases import (compare_attention, config4_specs, dims_of, i32, oracle_attention,
-                       oracle_meta, run_attention, sample_rows)
+from gpu_cases import (compare_attention, config4_specs, dims_of, i32, jump_tensors,
+                       oracle_attention, oracle_meta, run_attention, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -126,29 +126,6 @@ def test_metadata_errors_are_flagged(rb):
     assert int(err.item()) & 0x010
 
 
-def _jump_tensors(spec, hot, device="cuda"):
-    """Inputs whose scores jump across key tiles: every query is a common direction u plus small
-    noise and the keys at the positions of `hot` ({(start, end): beta}) are beta * u, so a row's
-    scores rise by ~16 beta (log2 units, head_dim 128) where it reaches those keys."""
-    tens = wl.make_tensors(spec, device=device)
-    d = spec.dims
-    g = torch.Generator(device=device).manual_seed(spec.seed + 17)
-    u = torch.randn(d.head_dim, generator=g, device=device)
-    q = u + 0.1 * torch.randn(tens.q.shape, generator=g, device=device)
-    tens.q.copy_(q.to(torch.bfloat16))
-    qsl = np.concatenate([[0], np.cumsum(spec.num_scheduled)])
-    for i in range(spec.num_reqs):
-        c = int(spec.num_computed[i])
-        for (s, e), beta in hot.items():
-            key = (beta * u).to(torch.bfloat16)
-            hs, he = min(s, c), min(e, c)          # hot keys in the history
-            tens.hist_k[i][hs:he] = key
-            ns, ne = max(s, c) - c, max(min(e, c + int(spec.num_scheduled[i])), c) - c
-            tens.k[int(qsl[i]) + ns:int(qsl[i]) + ne] = key   # hot keys among the new tokens
-    wl.place_history(spec, tens.hist_k, tens.k_cache)
-    return tens
-
-
 @pytest.mark.parametrize("nh,nkv,hd", [(32, 8, 128), (8, 1, 128), (12, 2, 64)])
 def test_score_jumps_across_key_tiles(rb, nh, nkv, hd):
     """A row's maximum rising by far more than 2^20 between key tiles (once, then again): the
@@ -157,7 +134,7 @@ def test_score_jumps_across_key_tiles(rb, nh, nkv, hd):
     spec = wl.batch_from_lists([600, 0, 700], [300, 400, 1], num_q_heads=nh, num_kv_heads=nkv,
                                head_dim=hd, seed=nh * 100 + hd)
     scale = 128 / hd  # the same jumps in log2 units at head_dim 64
-    tens = _jump_tensors(spec, {(300, 340): 2.0 * scale, (560, 570): 4.0 * scale})
+    tens = jump_tensors(spec, {(300, 340): 2.0 * scale, (560, 570): 4.0 * scale})
     meta = oracle_meta(spec)
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     got = run_attention(rb, spec, tens, meta, error_word=err)

@@ -9,7 +9,8 @@ import torch
 
 import oracle
 import workloads as wl
-from gpu_cases import compare_attention, dims_of, i32, oracle_attention, oracle_meta, sample_rows
+from gpu_cases import (compare_attention, dims_of, i32, jump_tensors, oracle_attention,
+                       oracle_meta, sample_rows)
 
 pytestmark = pytest.mark.gpu
 
@@ -98,3 +99,23 @@ def test_broken_contract_sets_attn_meta(rb):
         err = torch.zeros(1, dtype=torch.int32, device="cuda")
         _run(rb, s, tens, meta, P, err)
         assert int(err.item()) & 0x080, (P, mutate)
+
+
+def test_shared_prefix_score_jumps(rb):
+    """Scores rising by ~2^29 and then ~2^58 inside the shared prefix: the prefix pass (no
+    causal mask) re-references its key tiles, and the epilogues merge its log-sum-exp with the
+    suffix pass's rows across those magnitudes."""
+    spec = wl.shared_prefix_batch(5, num_decodes=6, prefix_tokens=704, suffix_range=(0, 200),
+                                  num_chunks=2, chunk_q=130, num_q_heads=32, num_kv_heads=8,
+                                  head_dim=128, hidden_size=64)
+    tens = jump_tensors(spec, {(300, 340): 2.0, (560, 570): 4.0})
+    meta = oracle_meta(spec)
+    d = spec.dims
+    P = rb.cascade_prefix_len(spec.shared_prefix_tokens, spec.num_computed.tolist(),
+                              d.block_size * d.kernel_blocks_per_manager_block)
+    assert P >= 576  # both jumps lie inside the shared prefix
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = _run(rb, spec, tens, meta, P, err)
+    assert int(err.item()) == 0
+    ref = oracle_attention(spec, tens, meta)
+    compare_attention(got, ref, spec.num_tokens)
