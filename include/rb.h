@@ -9,6 +9,8 @@
  *   rb_paged_attention  varlen causal GQA attention through the page table
  *   rb_gather_rows      hidden rows at logits_indices (the rows the LM head needs)
  *   rb_step             all four in one call (one memset and two launches)
+ *   rb_step_host        rb_step with the caller's host-to-device and device-to-host copies
+ *   rb_step_host_async  the same with the copies on streams of their own (pipelined steps)
  *
  * and, before rb_prepare_inputs, the runner's per-step merge of scheduler deltas into the
  * persistent batch:
@@ -21,7 +23,9 @@
  *    allocates it and keeps it alive until the work queued on `stream` has finished.  The
  *    library allocates no device memory and never synchronises: each call only enqueues
  *    kernels (and, for rb_prepare_inputs, one 4-byte memset) on `stream`, a cudaStream_t passed
- *    as void* (NULL = the legacy default stream).  The one exception to "no device memory" is
+ *    as void* (NULL = the legacy default stream); rb_step_host and rb_step_host_async also
+ *    enqueue the caller's copies, the latter on the caller's copy streams with event records
+ *    and waits between them.  The one exception to "no device memory" is
  *    the 64 MiB scratch array of rb_paged_attention_static_ws: a static device array of the
  *    library's module, so every GPU that loads the library holds it until the process exits.
  *  - All index arrays are int32.  bf16 tensors are passed as void* holding IEEE bfloat16 bits.
