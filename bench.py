@@ -63,11 +63,11 @@ FLUSH_BYTES = 512 << 20
 # its planner's code, comments left out): a figure is reported only while the code is the code
 # it was measured on.
 KNOWN_TRAFFIC = {
-    (2, "792140ab91671f77"): 79017728 + 3901440,
-    (3, "792140ab91671f77"): 4545561856 + 26183424,
+    (2, "37fd426dfcd8dad5"): 79017728 + 3901440,
+    (3, "37fd426dfcd8dad5"): 4545561856 + 26183424,
     # the stream: mean over the launches of stream steps 5..99 (the default timed steps)
-    (4, "792140ab91671f77"): 9499339202 + 80951309,
-    (5, "792140ab91671f77"): 6555419392 + 115067648,
+    (4, "37fd426dfcd8dad5"): 9499339202 + 80951309,
+    (5, "37fd426dfcd8dad5"): 6555419392 + 115067648,
 }
 
 WORKLOAD_NAMES = {1: "pages' worked example A/B/C", 2: "pages' padding example",
@@ -181,9 +181,10 @@ FUSED_SOURCES = ("attn_prefill_tc.cu", "attn_decode_warp.cuh", "tc_ptx.cuh", "at
 
 
 def _code_only(text: str) -> str:
-    """Source text without comments and blank lines (a comment edit keeps the hash)."""
-    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    lines = (re.sub(r"//.*", "", ln).rstrip() for ln in text.splitlines())
+    """Source text without comments, blank lines and runs of spaces (an edit of comments or
+    layout keeps the hash)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    lines = (" ".join(re.sub(r"//.*", "", ln).split()) for ln in text.splitlines())
     return "\n".join(ln for ln in lines if ln)
 
 
