@@ -36,6 +36,28 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(raw, n), n
 
 
+def _declared_param_counts():
+    """Parameter count of every function prototype in rb.h (comments stripped)."""
+    src = open(os.path.join(ROOT, "include", "rb.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    counts = {}
+    for m in re.finditer(r"\b(rb_[a-z0-9_]+)\s*\(([^;{]*?)\)\s*;", src):
+        params = " ".join(m.group(2).split())
+        counts[m.group(1)] = 0 if params in ("", "void") else params.count(",") + 1
+    return counts
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every function the binding types has the parameter count rb.h declares for it."""
+    counts = _declared_param_counts()
+    typed = {n: len(getattr(lib.lib, n).argtypes) for n in counts
+             if getattr(getattr(lib.lib, n, None), "argtypes", None) is not None}
+    assert {"rb_step_host_async", "rb_paged_attention", "rb_prepare_inputs"} <= set(typed)
+    for n, k in typed.items():
+        assert k == counts[n], (n, k, counts[n])
+
+
 def test_status_strings(lib):
     assert lib.status_string(0) == "ok"
     assert lib.status_string(5) == "unsupported shape"
