@@ -84,7 +84,7 @@ def make_spec(config: int, rank: int = 0, manager_ratio: int = 1, context_scale:
     if config == 2:
         return wl.config2(step=rank, manager_ratio=manager_ratio)
     if config == 3:
-        return wl.config3(step=rank, manager_ratio=manager_ratio)
+        return wl.config3(step=rank, manager_ratio=manager_ratio, context_scale=context_scale)
     if config == 5:
         return wl.config5(step=rank, context_scale=context_scale)
     raise SystemExit(f"config {config} is not a single fixed batch")
@@ -898,7 +898,10 @@ def measure_fixed(config, rank, world, local, steps, warmup, manager_ratio=1, wa
     out = {"value": toks / (med_max / 1000.0), "ms_per_step": med_max,
            "ms_per_step_mean": statistics.mean(step_times), "steps": steps, "warmup": warmup,
            "config": fixed_config_desc(spec, config),
-           "roofline": roofline(spec_work(spec), launch_s, config),
+           # measured traffic belongs to the workload as named: none for a scaled or
+           # manager-block variant
+           "roofline": roofline(spec_work(spec), launch_s,
+                                config if context_scale == 1.0 and manager_ratio == 1 else None),
            "components_ms": {"prep_launch": statistics.median(pre),
                              "attention_launch": statistics.median(att)},
            "gpu_launches": per_step * steps, "launch": "cuda_graph_replay", "wall_s": wall,
@@ -1073,7 +1076,7 @@ def main(argv=None):
     ap.add_argument("--manager-ratio", type=int, default=1,
                     help="--config 2/3: page tables of manager blocks of this many kernel pages")
     ap.add_argument("--context-scale", type=float, default=1.0,
-                    help="--config 5: cached lengths times this factor (a smaller case, e.g. "
+                    help="--config 3 or 5: cached lengths times this factor (a smaller case, e.g. "
                          "for a profiler; not a headline)")
     ap.add_argument("--cascade", action="store_true",
                     help="time one attention call on a shared-prefix batch, plain vs cascade")

@@ -192,15 +192,18 @@ def config2(step: int = 0, manager_ratio: int = 1) -> BatchSpec:
                        4096, seed)
 
 
-def config3(step: int = 0, num_real: int = 256, manager_ratio: int = 1) -> BatchSpec:
+def config3(step: int = 0, num_real: int = 256, manager_ratio: int = 1,
+            context_scale: float = 1.0) -> BatchSpec:
     """Pure decode: ``num_real`` requests x 1 token, cached context U[512, 8192], padded to 256.
 
     ``num_real=256`` is the workload as stated (no padding tokens); ``num_real=250`` exercises the
-    null-page route for 6 padding tokens and 6 padding requests.
+    null-page route for 6 padding tokens and 6 padding requests.  ``context_scale`` < 1 shrinks
+    every cached length by that factor (a smaller case of the same shape, e.g. for a profiler).
     """
     seed = 1000 * 3 + step + (0 if num_real == 256 else 500)
     rng = np.random.default_rng(seed)
-    computed = [int(x) for x in rng.integers(512, 8192, size=num_real, endpoint=True)]
+    computed = [max(1, int(int(x) * context_scale))
+                for x in rng.integers(512, 8192, size=num_real, endpoint=True)]
     scheduled = [1] * num_real
     M = _round_up(8192 + 1, 16)
     dims = Dims(block_size=16, num_q_heads=32, num_kv_heads=8, head_dim=128, max_num_reqs=256,
