@@ -63,11 +63,11 @@ FLUSH_BYTES = 512 << 20
 # its planner's code, comments left out): a figure is reported only while the code is the code
 # it was measured on.
 KNOWN_TRAFFIC = {
-    (2, "37fd426dfcd8dad5"): 79017728 + 3901440,
-    (3, "37fd426dfcd8dad5"): 4545561856 + 26183424,
+    (2, "9a8026878da7e19f"): 78976256 + 3943680,
+    (3, "9a8026878da7e19f"): 4545474816 + 26148352,
     # the stream: mean over the launches of stream steps 5..99 (the default timed steps)
-    (4, "37fd426dfcd8dad5"): 9499339202 + 80951309,
-    (5, "37fd426dfcd8dad5"): 6555419392 + 115067648,
+    (4, "9a8026878da7e19f"): 9567950312 + 80911815,
+    (5, "9a8026878da7e19f"): 8588893440 + 115581440,
 }
 
 WORKLOAD_NAMES = {1: "pages' worked example A/B/C", 2: "pages' padding example",

@@ -13,9 +13,11 @@
 // most 8 columns, far below a tcgen05 tile, and the unit is bound by HBM, not by the tensor
 // pipe.  P^T's fragments come from S^T's with a register transpose (movmatrix), so each page
 // costs 2 x hd/16 MMAs and every K/V byte is read once per kv head, shared by the whole
-// query-head group.  Softmax statistics are per column, reduced with warp shuffles; a unit with
-// several splits leaves (m, l, o) partials and the last split of its (request, kv head) to
-// finish merges them; a single-split unit writes the normalised bf16 output directly.
+// query-head group.  Softmax statistics are per column: exponents are taken against a
+// reference maximum that is re-reduced with warp shuffles (and O rescaled) only on the pages
+// where a score climbs well above it; a unit with several splits leaves (m, l, o) partials
+// and the last split of its (request, kv head) to finish merges them; a single-split unit
+// writes the normalised bf16 output directly.
 #pragma once
 
 #include "attn_common.cuh"
@@ -247,25 +249,37 @@ __device__ void decode_warp(const CUtensorMap* kmap_p, const CUtensorMap* vmap_p
       const float x1 = key0 <= lim1 ? s[1] * a.scale_log2 : -INFINITY;
       const float x2 = key1 <= lim0 ? s[2] * a.scale_log2 : -INFINITY;
       const float x3 = key1 <= lim1 ? s[3] * a.scale_log2 : -INFINITY;
-      float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+      // The exponents are taken against a reference m per column that moves only when a score
+      // exceeds it by more than kGrowth (log2 units): then the column maxima are reduced and
+      // O and l rescaled, as an online softmax does on every page.  Otherwise the page costs
+      // no shuffles and no rescale; every term stays below 2^kGrowth and the result, O / l, is
+      // the same (the partials' (m, l) are relative to the same m, which the merge accounts for).
+      constexpr float kGrowth = 8.f;
+      const float g0 = fmaxf(x0, x2), g1 = fmaxf(x1, x3);
+      if (__any_sync(0xffffffffu, g0 > m0 + kGrowth || g1 > m1 + kGrowth)) {
+        float mx0 = g0, mx1 = g1;
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        for (int o = 4; o < 32; o <<= 1) {
+          mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+          mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+        }
+        const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+        const float al0 = fast_exp2(m0 - (mn0 == -INFINITY ? 0.f : mn0));
+        const float al1 = fast_exp2(m1 - (mn1 == -INFINITY ? 0.f : mn1));
+        l0 *= al0;
+        l1 *= al1;
+#pragma unroll
+        for (int mt = 0; mt < C::kKS; ++mt) {
+          acc[mt][0] *= al0; acc[mt][1] *= al1; acc[mt][2] *= al0; acc[mt][3] *= al1;
+        }
+        m0 = mn0;
+        m1 = mn1;
       }
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-      const float ms0 = mn0 == -INFINITY ? 0.f : mn0, ms1 = mn1 == -INFINITY ? 0.f : mn1;
-      const float al0 = fast_exp2(m0 - ms0), al1 = fast_exp2(m1 - ms1);
+      const float ms0 = m0 == -INFINITY ? 0.f : m0, ms1 = m1 == -INFINITY ? 0.f : m1;
       const float p0 = fast_exp2(x0 - ms0), p1 = fast_exp2(x1 - ms1);
       const float p2 = fast_exp2(x2 - ms0), p3 = fast_exp2(x3 - ms1);
-      l0 = l0 * al0 + p0 + p2;
-      l1 = l1 * al1 + p1 + p3;
-      m0 = mn0;
-      m1 = mn1;
-#pragma unroll
-      for (int mt = 0; mt < C::kKS; ++mt) {
-        acc[mt][0] *= al0; acc[mt][1] *= al1; acc[mt][2] *= al0; acc[mt][3] *= al1;
-      }
+      l0 += p0 + p2;
+      l1 += p1 + p3;
       // rows past the end of the sequence may hold anything: zero their V before P.V
       if (pg * kPage + kPage > L) {
         const int kmin = L - pg * kPage;
