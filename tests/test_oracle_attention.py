@@ -150,3 +150,20 @@ def test_threaded_evaluation_equals_one_call():
     np.testing.assert_allclose(got[rows], full[rows], rtol=0, atol=1e-13)
     others = [r for r in range(16) if r not in rows]
     assert np.isnan(got[others]).all() and np.all(got[16:] == 0)
+
+
+def test_threaded_evaluation_cuts_long_requests():
+    """A request holding most of the rows x keys is cut into several calls on parts of its rows
+    (so that it does not keep one thread busy while the others wait): the rows come out as one
+    call over the whole batch gives them."""
+    from oracle.threads import oracle_attention_threads
+
+    rng = np.random.default_rng(7)
+    c, qn = [300, 2, 0], [48, 1, 3]
+    q, k, v, hk, hv = _rand_batch(rng, c, qn, 8, 2, 16, pad=1)
+    qsl, sl = _meta(c, qn)
+    rows = list(range(0, 52, 1))
+    full = oracle.paged_attention(q, hk, hv, k, v, qsl, sl, 3)
+    got = oracle_attention_threads(q, hk, hv, k, v, qsl, sl, 3, rows, workers=4)
+    np.testing.assert_allclose(got[rows], full[rows], rtol=0, atol=1e-13)
+    assert np.all(got[52:] == 0)
