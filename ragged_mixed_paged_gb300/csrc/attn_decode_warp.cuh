@@ -243,7 +243,7 @@ __device__ void decode_warp(const CUtensorMap* kmap_p, const CUtensorMap* vmap_p
 #pragma unroll
         for (int i = 0; i < 4; ++i) s[i] += s2[i];
       }
-      // causal mask per column, online softmax per column (log2 domain)
+      // causal mask per column, then the softmax per column (log2 domain)
       const int key0 = pg * kPage + (lane >> 2), key1 = key0 + 8;
       const float x0 = key0 <= lim0 ? s[0] * a.scale_log2 : -INFINITY;
       const float x1 = key0 <= lim1 ? s[1] * a.scale_log2 : -INFINITY;
